@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged gated-MLA decode step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl plmla|reference]
+
+A step is one pass of the whole hot path (split plan -> split decode -> LSE
+combine + sigmoid gate) over the steady-decode workload: 64 requests x 1 query
+token, 64 heads, 576-wide bf16 latent rows (512 latent + 64 rope), histories
+uniform in [8192, 32768] tokens, scattered over a 2048-page pool of 1,536-token
+pages (seed 1).  The metric is achieved HBM bandwidth on the KV bytes a step
+must read (sum of histories x 1,152 bytes), also given as request-steps/s.
+
+Prints ONE JSON line on rank 0.  Multi-GPU runs (torchrun, one rank per GPU)
+are weak-scaling replicas: every rank decodes its own copy of the workload, no
+data moves between GPUs, and the value is the total over ranks divided by the
+slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged MLA decode: achieved HBM GB/s (% of GB300 peak), request-steps/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+KERNELS_PER_STEP = 3          # plan, split decode, combine+gate
+DECODE_SOURCES = ["plmla_decode_simt.cu", "plmla_internal.cuh"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["plmla", "reference"], default="plmla")
+    ap.add_argument("--workload", default="steady",
+                    choices=["tiny", "steady", "agentic", "spec", "long"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--out", default=None, help="also append the JSON line to this file")
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------------
+# distributed plumbing (weak-scaling replicas; the only collectives are the
+# barrier and the max/sum of timing scalars)
+# --------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def barrier(dist, device=None):
+    if dist is not None:
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate(dist, local_ms, local_units, device="cpu"):
+    """(max time over ranks, total units over ranks)."""
+    if dist is None:
+        return local_ms, local_units
+    import torch
+    t = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+    u = torch.tensor([float(local_units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# --------------------------------------------------------------------------
+# clocks sampled during the timed region
+# --------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed region"
+        if len(inside) < 2:
+            # a short timed region: widen to the surrounding busy period
+            inside = [p for (t, p) in self.samples if t0 - 2.0 <= t <= t1 + 2.0]
+            window = "timed region +/- 2 s"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        smax = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[5 + i].lower() == "active"})
+        power = [num(p[3]) for p in inside if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(inside), "window": window,
+                "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------------------
+# peaks and profile-derived traffic
+# --------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def decode_source_hash():
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "paged_latent_attention_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, kv_bytes):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on the current decode kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("decode_source_hash") != decode_source_hash():
+        return None
+    per_unit = rec.get("dram_bytes_per_kv_byte")
+    return None if per_unit is None else per_unit * kv_bytes
+
+
+# --------------------------------------------------------------------------
+# CPU oracle baseline (a bounded sample of the same workload)
+# --------------------------------------------------------------------------
+
+def oracle_sample(w, qn, qr, gate, slab_dev, req_ids):
+    """Host inputs for the oracle restricted to `req_ids` (pages remapped)."""
+    import numpy as np
+    import torch
+    pages_per_req = [-(-int(w.seq_lens[r]) // w.page_tokens) for r in req_ids]
+    phys = [int(p) for r, n in zip(req_ids, pages_per_req) for p in w.page_table[r, :n]]
+    idx = torch.as_tensor(phys, dtype=torch.long, device=slab_dev.device)
+    host_slab = slab_dev.index_select(0, idx).cpu()
+    table = np.zeros((len(req_ids), max(1, max(pages_per_req))), dtype=np.int32)
+    pos = 0
+    for i, n in enumerate(pages_per_req):
+        table[i, :n] = np.arange(pos, pos + n)
+        pos += n
+    rows_q = torch.cat([torch.arange(r * w.n_q, (r + 1) * w.n_q) for r in req_ids])
+    lens = w.seq_lens[list(req_ids)].astype(np.int32)
+    return (qn[rows_q].cpu(), qr[rows_q].cpu(), gate[rows_q].cpu(), host_slab, table, lens,
+            len(phys))
+
+
+def run_oracle(w, sample):
+    import oracle
+    qn, qr, gate, slab, table, lens, npages = sample
+    t = time.perf_counter()
+    oracle.mla_decode_reference(qn, qr, gate, slab, table, lens, w.n_q, w.num_heads,
+                                1.0 / math.sqrt(192.0), num_pages=npages,
+                                page_stride=w.page_stride)
+    return time.perf_counter() - t
+
+
+def cpu_baseline(w, qn, qr, gate, slab_dev, target_s):
+    import oracle
+    cores = oracle.oracle.default_threads()
+    order = list(range(w.num_reqs))
+    one = oracle_sample(w, qn, qr, gate, slab_dev, order[:1])
+    t1 = run_oracle(w, one)
+    n = max(1, min(w.num_reqs, int(target_s / max(t1, 1e-3))))
+    sample = oracle_sample(w, qn, qr, gate, slab_dev, order[:n])
+    elapsed, reps = 0.0, 0
+    while elapsed < 0.5 * target_s or reps == 0:
+        elapsed += run_oracle(w, sample)
+        reps += 1
+    kv = int(sum(int(w.seq_lens[r]) for r in order[:n])) * (w.dc + w.dr) * 2
+    gbs = kv * reps / elapsed / 1e9
+    return {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.num_reqs} requests x all {w.num_heads} heads, {reps} pass(es), "
+                      f"{elapsed:.1f} s of double-precision oracle time",
+            "request_steps_per_s": n * reps / elapsed}
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+
+def workload_description(w):
+    lens = w.seq_lens
+    return (f"{w.name} decode: {w.num_reqs} requests x {w.n_q} query token(s), {w.num_heads} "
+            f"heads, 512 latent + 64 rope bf16, histories {int(lens.min())}..{int(lens.max())} "
+            f"tokens (sum {int(lens.sum())}), {w.num_pages} pages of 1536 tokens, "
+            f"{w.num_slabs} slab(s), seed {w.seed}")
+
+
+def run_gpu(args):
+    import torch
+    import paged_latent_attention_gb300 as plmla
+    from paged_latent_attention_gb300 import inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+
+    w = inputs.make_workload(args.workload)
+    layers = w.num_slabs
+    qs = [inputs.make_queries(w, device, layer=l) for l in range(layers)]
+    slabs = [inputs.make_slab(w, device, layer=l) for l in range(layers)]
+    table = torch.as_tensor(w.page_table, device=device)
+    lens = torch.as_tensor(w.seq_lens, device=device)
+    ws = plmla.allocate_workspace(w.num_reqs, w.n_q, w.num_heads, 0, w.min_splits, device)
+    outs = [torch.empty_like(q[0]) for q in qs]
+    lses = [torch.empty(w.num_tokens, w.num_heads, dtype=torch.float32, device=device)
+            for _ in qs]
+    kv_bytes_layer = w.kv_bytes_per_layer
+    kv_bytes_step = kv_bytes_layer * layers
+
+    K, W = args.steps, args.warmup
+    n_ev = K * layers
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_ev)]
+    stream = torch.cuda.current_stream(device)
+    for quad in evs:           # create every event handle before the timed region
+        for e in quad:
+            e.record(stream)
+
+    def step(ev_base=None):
+        for l in range(layers):
+            qn, qr, gate = qs[l]
+            plmla.mla_decode(qn, qr, gate, slabs[l], table, lens, n_q=w.n_q, out=outs[l],
+                             lse=lses[l], workspace=ws, min_splits=w.min_splits,
+                             events=None if ev_base is None else evs[ev_base + l])
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize(device)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid).start()
+    time.sleep(0.3)
+    barrier(dist, device)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    host_t0 = time.time()
+    start.record(stream)
+    for k in range(K):
+        step(k * layers)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    host_t1 = time.time()
+    barrier(dist, device)
+    local_ms = start.elapsed_time(end)
+    decode_ms = [q[1].elapsed_time(q[2]) for q in evs]
+    plan_ms = [q[0].elapsed_time(q[1]) for q in evs]
+    combine_ms = [q[2].elapsed_time(q[3]) for q in evs]
+    max_ms, total_units = aggregate(dist, local_ms, kv_bytes_step * K, device)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, qs, slabs, table, lens, ws, device, dist)
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(host_t0, host_t1)
+
+    if rank != 0:
+        return None
+    ms_per_step = max_ms / K
+    value = total_units / (max_ms / 1e3) / 1e9
+    peak, peak_src = hbm_peak()
+    dec_avg = statistics.mean(decode_ms)
+    achieved = kv_bytes_layer / (dec_avg / 1e3) / 1e9
+    traffic = profiled_traffic(args.workload, kv_bytes_layer)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_description(w), "requests": w.num_reqs,
+                   "n_q": w.n_q, "heads": w.num_heads, "layers": layers,
+                   "kv_tokens": w.kv_tokens, "kv_bytes_per_step": kv_bytes_step,
+                   "l2": "inputs larger than L2 (KV per step >> 129 MB L2), no flush",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_hbm_peak": 100.0 * value / world / peak,
+        "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
+        "request_steps_per_s": w.num_reqs * world / (max_ms / K / 1e3),
+        "kernel_ms": {"plan": statistics.mean(plan_ms), "decode": dec_avg,
+                      "combine": statistics.mean(combine_ms)},
+        "roofline": {"bound": "hbm", "kernel": "split decode", "achieved": achieved,
+                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": kv_bytes_layer},
+        "gpu_launches": KERNELS_PER_STEP * K * layers,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, qs[0][0], qs[0][1], qs[0][2], slabs[0],
+                                            args.cpu_seconds)
+    return line
+
+
+def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist):
+    """Same metric through the public call with pinned host buffers: each step
+    copies its inputs host->device, decodes, and reads the result back."""
+    import torch
+    import paged_latent_attention_gb300 as plmla
+    layers = w.num_slabs
+    host_q = [[t.cpu().pin_memory() for t in q] for q in qs]
+    host_table = table.cpu().pin_memory()
+    host_lens = lens.cpu().pin_memory()
+    dev_q = [[torch.empty_like(t) for t in q] for q in qs]
+    dev_table, dev_lens = torch.empty_like(table), torch.empty_like(lens)
+    host_out = [torch.empty(q[0].shape, dtype=q[0].dtype).pin_memory() for q in qs]
+    host_lse = [torch.empty(w.num_tokens, w.num_heads, dtype=torch.float32).pin_memory()
+                for _ in qs]
+    dev_out = [torch.empty_like(q[0]) for q in qs]
+    dev_lse = [torch.empty(w.num_tokens, w.num_heads, dtype=torch.float32, device=device)
+               for _ in qs]
+    h2d = sum(t.numel() * t.element_size() for q in host_q for t in q)
+    h2d += host_table.numel() * 4 + host_lens.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in host_out + host_lse)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        dev_table.copy_(host_table, non_blocking=True)
+        dev_lens.copy_(host_lens, non_blocking=True)
+        for l in range(layers):
+            for d, h in zip(dev_q[l], host_q[l]):
+                d.copy_(h, non_blocking=True)
+            plmla.mla_decode(dev_q[l][0], dev_q[l][1], dev_q[l][2], slabs[l], dev_table,
+                             dev_lens, n_q=w.n_q, out=dev_out[l], lse=dev_lse[l], workspace=ws,
+                             min_splits=w.min_splits)
+            host_out[l].copy_(dev_out[l], non_blocking=True)
+            host_lse[l].copy_(dev_lse[l], non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    barrier(dist, device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    ms = start.elapsed_time(end)
+    max_ms, units = aggregate(dist, ms, w.kv_bytes_per_layer * layers * args.steps, device)
+    return {"value": units / (max_ms / 1e3) / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": max_ms / args.steps,
+            "note": "KV pool resident in HBM (it is the cache); per-step queries, gates, "
+                    "page table and lengths copied in, outputs and LSE copied out"}
+
+
+# --------------------------------------------------------------------------
+# reference arm: the oracle as it stands, on host cores
+# --------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    import torch
+    import oracle
+    from paged_latent_attention_gb300 import inputs
+    w = inputs.make_workload(args.workload)
+    qn, qr, gate = inputs.make_queries(w, "cpu")
+    # the pool rows the sampled requests read, generated on the host
+    slab = inputs.make_slab(w, "cpu", pages_per_chunk=16) if w.num_pages <= 4096 else None
+    if slab is None:
+        return {"impl": "reference", "unavailable": "pool too large for a host copy"}
+    cores = oracle.oracle.default_threads()
+    total = args.steps + args.warmup
+    budget_s = 150.0
+    one = oracle_sample(w, qn, qr, gate, slab, [0])
+    t1 = run_oracle(w, one)
+    per_step = max(1, min(w.num_reqs, int(budget_s / total / max(t1, 1e-3))))
+    times, kv = [], []
+    for s in range(total):
+        ids = [(s * per_step + i) % w.num_reqs for i in range(per_step)]
+        sample = oracle_sample(w, qn, qr, gate, slab, ids)
+        dt = run_oracle(w, sample)
+        if s >= args.warmup:
+            times.append(dt)
+            kv.append(sum(int(w.seq_lens[r]) for r in ids) * (w.dc + w.dr) * 2)
+    elapsed = sum(times)
+    value = sum(kv) / elapsed / 1e9
+    desc = (f"{per_step} of {w.num_reqs} requests x all {w.num_heads} heads per step "
+            f"(requests taken in rotation), double-precision oracle")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_description(w)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_gpu(args)
+    if line is not None:
+        text = json.dumps(line)
+        print(text, flush=True)
+        if args.out:
+            with open(args.out, "a") as f:
+                f.write(text + "\n")
+    world, _, _ = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * plmla.h -- C ABI of libplmla: gated Multi-head Latent Attention (MLA) decode
+ * over a flat, paged KV pool, for NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operation (web pages, cited by title and section):
+ *   [K3]  TokenSpeed, Day-0 Kimi K3 post (lightseek.org/blog/tokenspeed-kimi-k3.html):
+ *         architecture list (Gated MLA: full softmax attention over stored
+ *         compressed latent KV, with a gate on its output); section "A Generic,
+ *         Unified Flat KV Layout for Cache Management" (one page pool, 1,536-token
+ *         MLA pages, one global page ID per page across slabs); section "Gluon
+ *         kernels on AMD GPUs", Gated MLA decode paragraph (split the history
+ *         along the context, merge partial softmax states in a second kernel).
+ *   [AX]  "331 output tokens/s per GPU on AgentX: Serving Kimi K3 on GB300 with
+ *         TokenSpeed": section "Balance MLA work with per-request KV splitting"
+ *         (Figure 4: chunk length from total history and parallelism budget,
+ *         more splits for longer requests, CUDA-graph compatible); section
+ *         "Kernel fusion and overlap complete the decode path" (sigmoid output
+ *         gating); section "Use TP4 selectively ..." (four drafted tokens are
+ *         verified per request).
+ *   [IX]  "AgentX - InferenceXv3: Does CUDA Moat Hold up in Agentic Inferencing?":
+ *         the ROCm AITER section (64-bit MLA offsets for pools above 2 GB); the
+ *         TensorRT-LLM section (honour block-index strides); the SGLang section
+ *         (context length as a runtime scalar, no per-step device-to-host sync).
+ *
+ * Fixed shape of the latent cache: every token row holds 576 bf16 values, the
+ * 512-wide compressed latent c_kv followed by the 64-wide rope key; a page holds
+ * 1,536 consecutive token rows.
+ *
+ * Conventions shared by every entry point:
+ *   - bf16 means IEEE bfloat16 (2 bytes); pointers to bf16 data are void*.
+ *   - Every pointer is a DEVICE pointer of the current CUDA device, owned by
+ *     the caller.  The library never allocates, frees or synchronises on these
+ *     calls; all work is enqueued on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream) and no call reads device data back to the host, so the
+ *     calls can be captured in a CUDA graph.
+ *   - Errors are returned as plmla_status; nothing is thrown across the ABI.
+ *     PLMLA_CUDA_ERROR means a launch failed: cudaGetLastError() has the cause.
+ *     Arguments are checked on the host before anything is enqueued.
+ */
+#ifndef PLMLA_H
+#define PLMLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum plmla_status {
+    PLMLA_OK = 0,
+    PLMLA_INVALID_ARGUMENT = 1,     /* null or misaligned pointer, bad size or count */
+    PLMLA_UNSUPPORTED = 2,          /* valid request outside what the kernels cover */
+    PLMLA_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes < mla_workspace_size(...) */
+    PLMLA_CUDA_ERROR = 4,           /* a CUDA runtime/driver call failed */
+} plmla_status;
+
+enum {
+    PLMLA_LATENT_DIM = 512,  /* c_kv width */
+    PLMLA_ROPE_DIM = 64,     /* rope key width */
+    PLMLA_ROW_DIM = 576,     /* elements per token row in a page */
+    PLMLA_PAGE_TOKENS = 1536 /* token rows per MLA page [K3, flat KV layout] */
+};
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *mla_strerror(plmla_status status);
+
+/*
+ * mla_split_budget -- number of KV chunks ("splits") one decode step may use in
+ * total, derived from the machine as [IX] asks (a hard-coded budget starved a
+ * large GPU).  Pure host arithmetic.
+ *
+ *   row_groups = n_q * num_heads / group_rows, where group_rows is the largest
+ *                of 64, 32, 16 dividing n_q * num_heads (rows a decode CTA owns)
+ *   slots      = cta_budget, or the current device's SM count when 0
+ *   waves      = max(1, ceil(num_reqs * row_groups * min_splits_per_req / slots))
+ *   budget     = max(1, floor(waves * slots / row_groups))
+ *
+ * Returns the budget, or -1 for invalid arguments / no CUDA device when
+ * cta_budget == 0.
+ */
+int32_t mla_split_budget(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_budget,
+                         int32_t min_splits_per_req);
+
+/*
+ * mla_workspace_size -- bytes of device workspace mla_decode needs for this
+ * shape (plan arrays, fp32 partial outputs and partial log-sum-exps for up to
+ * max(budget, num_reqs) chunks).  0 on invalid arguments.  Pure host arithmetic.
+ */
+size_t mla_workspace_size(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_budget,
+                          int32_t min_splits_per_req);
+
+/*
+ * mla_plan_splits -- per-request KV split plan [AX, Figure 4], on the device.
+ *
+ *   chunk     = ceil(sum_r L_r / split_budget) rounded up to a multiple of 128,
+ *               then grown by 128 while sum_r ceil(L_r / chunk) > split_budget,
+ *               never past the longest history (then every request has 1 chunk)
+ *   splits_r  = ceil(L_r / chunk)  (0 when L_r = 0)
+ *   split s of request r covers tokens [s*chunk, min((s+1)*chunk, L_r)).
+ *
+ * seq_lens      [num_reqs] int32, device, L_r >= 0;  num_reqs 1 .. 1024.
+ * split_indptr  [num_reqs + 1] int32, device, written: exclusive prefix sum of
+ *               splits_r in request order (split ids of request r are
+ *               split_indptr[r] .. split_indptr[r+1]-1).
+ * split_chunk   [1] int64, device, written: chunk.
+ * Runs as one kernel; never reads device data on the host.
+ */
+plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_reqs, int32_t split_budget,
+                             int32_t *split_indptr, int64_t *split_chunk, void *stream);
+
+/*
+ * mla_decode -- one gated-MLA decode step for a batch of requests [K3, AX].
+ *
+ * For request r, draft token j < n_q_per_req and head h, with
+ * L' = seq_lens[r] - (n_q_per_req - 1 - j) (drafts see each other causally) and
+ * token row x_t = slab_base[page_table[r*page_table_ld + t/1536]*page_stride_elems
+ *                           + (t % 1536)*576 + 0..575]:
+ *
+ *   s_t = scale * (q_nope_absorbed[r,j,h,:] . x_t[0:512] + q_rope[r,j,h,:] . x_t[512:576])
+ *   o   = sum_{t < L'} softmax(s)_t * x_t[0:512]
+ *   lse = ln sum_{t < L'} exp(s_t)                      (natural log, before the gate)
+ *   out = bf16_rn( sigmoid(gate[r,j,h,:]) * o )        (elementwise gate)
+ *
+ * Rows with L' <= 0 give out = 0 and lse = -inf.  Token rows at t >= L' and
+ * pages the table does not reach are never used, whatever they hold (NaN safe).
+ *
+ * q_nope_absorbed  bf16 [num_reqs*n_q_per_req, num_heads, 512], contiguous
+ * q_rope           bf16 [num_reqs*n_q_per_req, num_heads, 64], contiguous
+ * gate             bf16 [num_reqs*n_q_per_req, num_heads, 512] gate logits
+ * slab_base        bf16 pool of num_pages pages, 16-byte aligned
+ * num_pages        pages in the pool (1 .. 2^31-1); offsets are computed in 64 bits
+ * page_stride_elems elements from one page to the next, >= 1536*576, multiple of 8
+ * page_table       int32, row r at page_table + r*page_table_ld (row stride honoured)
+ * page_table_ld    >= ceil(max_r L_r / 1536)
+ * seq_lens         int32 [num_reqs], device (history incl. the n_q drafts)
+ * num_reqs         1 .. 1024;  n_q_per_req 1 .. 16;  num_heads multiple of 16, <= 128
+ * scale            softmax scale (1/sqrt(192) for a 128+64 head)
+ * out              bf16 [num_reqs*n_q_per_req, num_heads, 512], written
+ * lse              fp32 [num_reqs*n_q_per_req, num_heads], written (may be NULL)
+ * workspace        device scratch of workspace_bytes >= mla_workspace_size(...),
+ *                  256-byte aligned; contents on entry are irrelevant
+ * cta_budget       concurrent CTA slots for the split budget (0 = SM count)
+ * min_splits_per_req  >= 1; raises the budget so that equal-length requests get
+ *                  at least this many chunks each
+ * stream           cudaStream_t
+ *
+ * Enqueues: plan kernel -> split-decode kernel -> combine/gate kernel.
+ * Page IDs are trusted: an ID outside [0, num_pages) is undefined behaviour.
+ */
+plmla_status mla_decode(const void *q_nope_absorbed, const void *q_rope, const void *gate,
+                        const void *slab_base, int64_t num_pages, int64_t page_stride_elems,
+                        const int32_t *page_table, int64_t page_table_ld,
+                        const int32_t *seq_lens, int32_t num_reqs, int32_t n_q_per_req,
+                        int32_t num_heads, float scale, void *out, float *lse, void *workspace,
+                        size_t workspace_bytes, int32_t cta_budget, int32_t min_splits_per_req,
+                        void *stream);
+
+/*
+ * Optional stage events for mla_decode_ex: each non-NULL member is a cudaEvent_t
+ * that is recorded on `stream` at that point of the step (before the plan
+ * kernel, before the split-decode kernel, before the combine kernel, after the
+ * combine kernel).  Used to time each kernel inside a measured step; recording
+ * adds no device work.
+ */
+typedef struct plmla_stage_events {
+    void *plan_begin;
+    void *decode_begin;
+    void *combine_begin;
+    void *combine_end;
+} plmla_stage_events;
+
+/*
+ * mla_decode_ex -- mla_decode with optional stage events (NULL = none).  Same
+ * arguments, results and errors as mla_decode.
+ */
+plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q_rope, const void *gate,
+                           const void *slab_base, int64_t num_pages, int64_t page_stride_elems,
+                           const int32_t *page_table, int64_t page_table_ld,
+                           const int32_t *seq_lens, int32_t num_reqs, int32_t n_q_per_req,
+                           int32_t num_heads, float scale, void *out, float *lse,
+                           void *workspace, size_t workspace_bytes, int32_t cta_budget,
+                           int32_t min_splits_per_req, void *stream,
+                           const plmla_stage_events *events);
+
+/*
+ * mla_split_combine -- merge the partial softmax states of each request's KV
+ * chunks and apply the sigmoid output gate [K3, Gated MLA decode paragraph;
+ * AX, gating bullet].  Split order is fixed, so results are deterministic.
+ *
+ *   lse = ln sum_i exp(lse_part_i);  o = sum_i exp(lse_part_i - lse) * o_part_i
+ *   out = bf16_rn(sigmoid(gate) * o)
+ *
+ * o_part       fp32 [num_splits, n_q_per_req*num_heads, 512]: split i's output,
+ *              normalised over its own chunk (row index j*num_heads + h)
+ * lse_part     fp32 [num_splits, n_q_per_req*num_heads], natural log; -inf for
+ *              an empty chunk
+ * split_indptr int32 [num_reqs + 1], device; request r owns splits
+ *              split_indptr[r] .. split_indptr[r+1]-1 (none: out = 0, lse = -inf)
+ * gate, out    bf16 [num_reqs*n_q_per_req, num_heads, 512]
+ * lse          fp32 [num_reqs*n_q_per_req, num_heads] (may be NULL)
+ */
+plmla_status mla_split_combine(const float *o_part, const float *lse_part,
+                               const int32_t *split_indptr, const void *gate, int32_t num_reqs,
+                               int32_t n_q_per_req, int32_t num_heads, void *out, float *lse,
+                               void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PLMLA_H */

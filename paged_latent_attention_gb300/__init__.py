@@ -1,0 +1,14 @@
+"""paged_latent_attention_gb300: gated MLA decode over a flat paged KV pool on GB300.
+
+The compute path is the CUDA library libplmla.so (C ABI in include/plmla.h);
+this package only marshals torch tensors into it.
+"""
+from .api import (  # noqa: F401
+    DEFAULT_SCALE,
+    allocate_workspace,
+    mla_decode,
+    mla_plan_splits,
+    mla_split_budget,
+    mla_split_combine,
+    mla_workspace_size,
+)

@@ -1,0 +1,170 @@
+"""Torch-tensor front end of libplmla (argument marshalling only).
+
+Every step of the decode runs in the CUDA library; these functions check
+shapes, dtypes and devices, then pass raw device pointers and sizes through the
+C ABI.  PyTorch only supplies device memory and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _native
+
+LATENT = 512
+ROPE = 64
+ROW = LATENT + ROPE
+PAGE_TOKENS = 1536
+DEFAULT_SCALE = 1.0 / math.sqrt(192.0)   # a 128-wide nope + 64-wide rope head
+
+
+def _stream_ptr(stream, device):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes_void(s.cuda_stream)
+
+
+def ctypes_void(v):
+    return None if v in (0, None) else int(v)
+
+
+def _require(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _check_bf16(t, name, shape=None):
+    _require(isinstance(t, torch.Tensor), f"{name} must be a tensor")
+    _require(t.is_cuda, f"{name} must be a CUDA tensor")
+    _require(t.dtype == torch.bfloat16, f"{name} must be bfloat16")
+    _require(t.is_contiguous(), f"{name} must be contiguous")
+    if shape is not None:
+        _require(tuple(t.shape) == tuple(shape), f"{name} has shape {tuple(t.shape)}, "
+                                                 f"expected {tuple(shape)}")
+
+
+def mla_split_budget(num_reqs, n_q, num_heads, cta_budget=0, min_splits=1) -> int:
+    b = _native.lib().mla_split_budget(num_reqs, n_q, num_heads, cta_budget, min_splits)
+    if b < 1:
+        raise ValueError("invalid shape for mla_split_budget")
+    return int(b)
+
+
+def mla_workspace_size(num_reqs, n_q, num_heads, cta_budget=0, min_splits=1) -> int:
+    n = _native.lib().mla_workspace_size(num_reqs, n_q, num_heads, cta_budget, min_splits)
+    if n == 0:
+        raise ValueError("invalid shape for mla_workspace_size")
+    return int(n)
+
+
+def allocate_workspace(num_reqs, n_q, num_heads, cta_budget=0, min_splits=1, device=None):
+    """A caller-owned workspace tensor (uint8) of the size mla_decode needs."""
+    n = mla_workspace_size(num_reqs, n_q, num_heads, cta_budget, min_splits)
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def mla_decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *, n_q=1,
+               scale=DEFAULT_SCALE, out=None, lse=None, workspace=None, cta_budget=0,
+               min_splits=1, stream=None, with_lse=True, events=None):
+    """One gated-MLA decode step; returns (out, lse).
+
+    ``events`` (optional): four torch.cuda.Event (or None) recorded before the
+    plan kernel, before the split-decode kernel, before the combine kernel and
+    after it, on the launch stream.  Each event must have been recorded once
+    already, so that torch has created its handle.
+
+    q_nope_absorbed, gate: [R*n_q, H, 512] bf16; q_rope: [R*n_q, H, 64] bf16.
+    slab: [num_pages, page_stride] bf16 (page_stride >= 1536*576; row r of a
+    page at r*576).  page_table: [R, ld] int32 with unit column stride (its row
+    stride is passed through, so a strided view works).  seq_lens: [R] int32.
+    """
+    _require(q_nope_absorbed.dim() == 3, "q_nope_absorbed must be [R*n_q, H, 512]")
+    T, H, _ = q_nope_absorbed.shape
+    _require(T % n_q == 0, "first dimension must be num_reqs * n_q")
+    R = T // n_q
+    device = q_nope_absorbed.device
+    _check_bf16(q_nope_absorbed, "q_nope_absorbed", (T, H, LATENT))
+    _check_bf16(q_rope, "q_rope", (T, H, ROPE))
+    _check_bf16(gate, "gate", (T, H, LATENT))
+    _require(slab.is_cuda and slab.dtype == torch.bfloat16 and slab.dim() == 2,
+             "slab must be a 2-D CUDA bf16 tensor [num_pages, page_stride]")
+    _require(slab.stride(1) == 1, "slab pages must be contiguous")
+    num_pages, page_stride = slab.shape[0], slab.stride(0)
+    _require(slab.shape[1] >= PAGE_TOKENS * ROW, "slab page too small")
+    _require(page_table.is_cuda and page_table.dtype == torch.int32 and page_table.dim() == 2,
+             "page_table must be a 2-D CUDA int32 tensor")
+    _require(page_table.shape[0] == R and page_table.stride(1) == 1,
+             "page_table must be [R, ld] with unit column stride")
+    _require(seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+             and tuple(seq_lens.shape) == (R,), "seq_lens must be a contiguous CUDA int32 [R]")
+    if out is None:
+        out = torch.empty_like(q_nope_absorbed)
+    _check_bf16(out, "out", (T, H, LATENT))
+    if lse is None and with_lse:
+        lse = torch.empty(T, H, dtype=torch.float32, device=device)
+    if lse is not None:
+        _require(lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()
+                 and tuple(lse.shape) == (T, H), "lse must be a contiguous CUDA fp32 [T, H]")
+    if workspace is None:
+        workspace = allocate_workspace(R, n_q, H, cta_budget, min_splits, device)
+    _require(workspace.is_cuda and workspace.is_contiguous(), "workspace must be CUDA memory")
+    nbytes = workspace.numel() * workspace.element_size()
+    ev = None
+    if events is not None:
+        handles = []
+        for e in events:
+            h = None if e is None else int(e.cuda_event)
+            _require(h != 0, "stage events must have been recorded once before use")
+            handles.append(h)
+        ev = _native.StageEvents(*handles)
+    status = _native.lib().mla_decode_ex(
+        q_nope_absorbed.data_ptr(), q_rope.data_ptr(), gate.data_ptr(), slab.data_ptr(),
+        num_pages, page_stride, page_table.data_ptr(), page_table.stride(0),
+        seq_lens.data_ptr(), R, n_q, H, float(scale), out.data_ptr(),
+        lse.data_ptr() if lse is not None else None, workspace.data_ptr(), nbytes,
+        int(cta_budget), int(min_splits), _stream_ptr(stream, device),
+        ctypes.byref(ev) if ev is not None else None)
+    _native.check(status, "mla_decode")
+    return out, lse
+
+
+def mla_plan_splits(seq_lens, split_budget, stream=None):
+    """Device split plan: (split_indptr [R+1] int32, chunk [1] int64)."""
+    _require(seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+             and seq_lens.dim() == 1, "seq_lens must be a contiguous CUDA int32 vector")
+    R = seq_lens.shape[0]
+    indptr = torch.empty(R + 1, dtype=torch.int32, device=seq_lens.device)
+    chunk = torch.empty(1, dtype=torch.int64, device=seq_lens.device)
+    status = _native.lib().mla_plan_splits(seq_lens.data_ptr(), R, int(split_budget),
+                                           indptr.data_ptr(), chunk.data_ptr(),
+                                           _stream_ptr(stream, seq_lens.device))
+    _native.check(status, "mla_plan_splits")
+    return indptr, chunk
+
+
+def mla_split_combine(o_part, lse_part, split_indptr, gate, *, n_q=1, out=None, lse=None,
+                      stream=None, with_lse=True):
+    """Merge chunk partials and apply the sigmoid gate; returns (out, lse)."""
+    _check_bf16(gate, "gate")
+    T, H, _ = gate.shape
+    R = T // n_q
+    rows = n_q * H
+    _require(o_part.is_cuda and o_part.dtype == torch.float32 and o_part.is_contiguous()
+             and o_part.dim() == 3 and o_part.shape[1:] == (rows, LATENT),
+             "o_part must be contiguous CUDA fp32 [splits, n_q*H, 512]")
+    _require(lse_part.is_cuda and lse_part.dtype == torch.float32 and lse_part.is_contiguous()
+             and tuple(lse_part.shape) == (o_part.shape[0], rows),
+             "lse_part must be contiguous CUDA fp32 [splits, n_q*H]")
+    _require(split_indptr.is_cuda and split_indptr.dtype == torch.int32
+             and tuple(split_indptr.shape) == (R + 1,), "split_indptr must be CUDA int32 [R+1]")
+    if out is None:
+        out = torch.empty_like(gate)
+    if lse is None and with_lse:
+        lse = torch.empty(T, H, dtype=torch.float32, device=gate.device)
+    status = _native.lib().mla_split_combine(
+        o_part.data_ptr(), lse_part.data_ptr(), split_indptr.data_ptr(), gate.data_ptr(), R,
+        n_q, H, out.data_ptr(), lse.data_ptr() if lse is not None else None,
+        _stream_ptr(stream, gate.device))
+    _native.check(status, "mla_split_combine")
+    return out, lse

@@ -1,0 +1,267 @@
+// plmla_abi.cu -- host implementation of the C ABI declared in include/plmla.h.
+//
+// Validates arguments, lays out the caller's workspace, and enqueues the plan,
+// split-decode and combine kernels on the caller's stream.  Nothing here
+// allocates device memory, synchronises, or reads device data back.
+#include <math.h>
+#include <stdint.h>
+
+#include "plmla.h"
+#include "plmla_internal.cuh"
+
+using namespace plmla;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int current_sm_count()
+{
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        return -1;
+    if (dev < 64 && cached[dev] > 0)
+        return cached[dev];
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return -1;
+    if (dev < 64)
+        cached[dev] = sms;
+    return sms;
+}
+
+bool shape_ok(int32_t num_reqs, int32_t n_q, int32_t num_heads)
+{
+    return num_reqs >= 1 && num_reqs <= kMaxReqs && n_q >= 1 && n_q <= kMaxNq &&
+           num_heads >= 16 && num_heads <= 128 && num_heads % 16 == 0;
+}
+
+struct WorkspaceLayout {
+    size_t indptr, chunk, count, items, o_part, lse_part, total;
+    int32_t max_items;
+};
+
+WorkspaceLayout layout_for(int32_t num_reqs, int32_t rows_per_req, int32_t budget)
+{
+    WorkspaceLayout w;
+    w.max_items = budget > num_reqs ? budget : num_reqs;
+    size_t off = 0;
+    w.indptr = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)(num_reqs + 1));
+    w.chunk = off;
+    off = align_up(off + sizeof(int64_t));
+    w.count = off;
+    off = align_up(off + sizeof(int32_t));
+    w.items = off;
+    off = align_up(off + sizeof(WorkItem) * (size_t)w.max_items);
+    w.o_part = off;
+    off = align_up(off + sizeof(float) * (size_t)w.max_items * rows_per_req * kLatent);
+    w.lse_part = off;
+    off = align_up(off + sizeof(float) * (size_t)w.max_items * rows_per_req);
+    w.total = off;
+    return w;
+}
+
+}  // namespace
+
+extern "C" const char *mla_strerror(plmla_status status)
+{
+    switch (status) {
+    case PLMLA_OK: return "PLMLA_OK";
+    case PLMLA_INVALID_ARGUMENT: return "PLMLA_INVALID_ARGUMENT";
+    case PLMLA_UNSUPPORTED: return "PLMLA_UNSUPPORTED";
+    case PLMLA_WORKSPACE_TOO_SMALL: return "PLMLA_WORKSPACE_TOO_SMALL";
+    case PLMLA_CUDA_ERROR: return "PLMLA_CUDA_ERROR";
+    }
+    return "PLMLA_UNKNOWN_STATUS";
+}
+
+extern "C" int32_t mla_split_budget(int32_t num_reqs, int32_t n_q, int32_t num_heads,
+                                    int32_t cta_budget, int32_t min_splits_per_req)
+{
+    if (!shape_ok(num_reqs, n_q, num_heads) || cta_budget < 0 || min_splits_per_req < 1)
+        return -1;
+    const int rows = n_q * num_heads;
+    const int group_rows = group_rows_for(rows);
+    if (group_rows == 0)
+        return -1;
+    const int64_t groups = rows / group_rows;
+    const int64_t slots = cta_budget > 0 ? cta_budget : current_sm_count();
+    if (slots <= 0)
+        return -1;
+    const int64_t units = (int64_t)num_reqs * groups * min_splits_per_req;
+    int64_t waves = (units + slots - 1) / slots;
+    if (waves < 1)
+        waves = 1;
+    int64_t budget = (waves * slots) / groups;
+    if (budget < 1)
+        budget = 1;
+    if (budget > (int64_t)1 << 20)
+        return -1;
+    return (int32_t)budget;
+}
+
+extern "C" size_t mla_workspace_size(int32_t num_reqs, int32_t n_q, int32_t num_heads,
+                                     int32_t cta_budget, int32_t min_splits_per_req)
+{
+    const int32_t budget = mla_split_budget(num_reqs, n_q, num_heads, cta_budget,
+                                            min_splits_per_req);
+    if (budget < 1)
+        return 0;
+    return layout_for(num_reqs, n_q * num_heads, budget).total;
+}
+
+extern "C" plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_reqs,
+                                        int32_t split_budget, int32_t *split_indptr,
+                                        int64_t *split_chunk, void *stream)
+{
+    if (seq_lens == nullptr || split_indptr == nullptr || split_chunk == nullptr ||
+        num_reqs < 1 || num_reqs > kMaxReqs || split_budget < 1 || !aligned(seq_lens, 4) ||
+        !aligned(split_indptr, 4) || !aligned(split_chunk, 8))
+        return PLMLA_INVALID_ARGUMENT;
+    // Same kernel as inside mla_decode, without the work-item list.
+    PlanBuffers plan;
+    plan.indptr = split_indptr;
+    plan.chunk = split_chunk;
+    plan.count = nullptr;
+    plan.items = nullptr;
+    cudaError_t err = launch_plan(seq_lens, num_reqs, split_budget, plan,
+                                  static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
+}
+
+extern "C" plmla_status mla_split_combine(const float *o_part, const float *lse_part,
+                                          const int32_t *split_indptr, const void *gate,
+                                          int32_t num_reqs, int32_t n_q_per_req,
+                                          int32_t num_heads, void *out, float *lse,
+                                          void *stream)
+{
+    if (o_part == nullptr || lse_part == nullptr || split_indptr == nullptr ||
+        gate == nullptr || out == nullptr)
+        return PLMLA_INVALID_ARGUMENT;
+    if (!shape_ok(num_reqs, n_q_per_req, num_heads))
+        return PLMLA_INVALID_ARGUMENT;
+    if (!aligned(o_part, 16) || !aligned(lse_part, 4) || !aligned(gate, 8) ||
+        !aligned(out, 8) || (lse != nullptr && !aligned(lse, 4)))
+        return PLMLA_INVALID_ARGUMENT;
+    cudaError_t err = launch_combine(o_part, lse_part, split_indptr,
+                                     static_cast<const __nv_bfloat16 *>(gate), num_reqs,
+                                     n_q_per_req, num_heads, static_cast<__nv_bfloat16 *>(out),
+                                     lse, static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
+}
+
+namespace {
+cudaError_t record(void *event, cudaStream_t stream)
+{
+    return event != nullptr ? cudaEventRecord(static_cast<cudaEvent_t>(event), stream)
+                            : cudaSuccess;
+}
+}  // namespace
+
+extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q_rope,
+                                      const void *gate, const void *slab_base,
+                                      int64_t num_pages, int64_t page_stride_elems,
+                                      const int32_t *page_table, int64_t page_table_ld,
+                                      const int32_t *seq_lens, int32_t num_reqs,
+                                      int32_t n_q_per_req, int32_t num_heads, float scale,
+                                      void *out, float *lse, void *workspace,
+                                      size_t workspace_bytes, int32_t cta_budget,
+                                      int32_t min_splits_per_req, void *stream,
+                                      const plmla_stage_events *events)
+{
+    if (q_nope_absorbed == nullptr || q_rope == nullptr || gate == nullptr ||
+        slab_base == nullptr || page_table == nullptr || seq_lens == nullptr ||
+        out == nullptr || workspace == nullptr)
+        return PLMLA_INVALID_ARGUMENT;
+    if (!shape_ok(num_reqs, n_q_per_req, num_heads) || min_splits_per_req < 1 || cta_budget < 0)
+        return PLMLA_INVALID_ARGUMENT;
+    if (num_pages < 1 || num_pages > INT32_MAX || page_table_ld < 1 ||
+        page_stride_elems < (int64_t)kPageTokens * kRow || page_stride_elems % 8 != 0)
+        return PLMLA_INVALID_ARGUMENT;
+    if (!(isfinite(scale)))
+        return PLMLA_INVALID_ARGUMENT;
+    if (!aligned(q_nope_absorbed, 16) || !aligned(q_rope, 16) || !aligned(gate, 16) ||
+        !aligned(slab_base, 16) || !aligned(out, 16) || !aligned(workspace, kAlign) ||
+        !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
+        (lse != nullptr && !aligned(lse, 4)))
+        return PLMLA_INVALID_ARGUMENT;
+
+    const int32_t budget = mla_split_budget(num_reqs, n_q_per_req, num_heads, cta_budget,
+                                            min_splits_per_req);
+    if (budget < 1)
+        return cta_budget == 0 ? PLMLA_CUDA_ERROR : PLMLA_INVALID_ARGUMENT;
+    const int rows_per_req = n_q_per_req * num_heads;
+    const WorkspaceLayout w = layout_for(num_reqs, rows_per_req, budget);
+    if (workspace_bytes < w.total)
+        return PLMLA_WORKSPACE_TOO_SMALL;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned char *ws = static_cast<unsigned char *>(workspace);
+    PlanBuffers plan;
+    plan.indptr = reinterpret_cast<int32_t *>(ws + w.indptr);
+    plan.chunk = reinterpret_cast<int64_t *>(ws + w.chunk);
+    plan.count = reinterpret_cast<int32_t *>(ws + w.count);
+    plan.items = reinterpret_cast<WorkItem *>(ws + w.items);
+    float *o_part = reinterpret_cast<float *>(ws + w.o_part);
+    float *lse_part = reinterpret_cast<float *>(ws + w.lse_part);
+
+    const plmla_stage_events none = {nullptr, nullptr, nullptr, nullptr};
+    const plmla_stage_events &ev = events != nullptr ? *events : none;
+    if (record(ev.plan_begin, s) != cudaSuccess)
+        return PLMLA_CUDA_ERROR;
+    cudaError_t err = launch_plan(seq_lens, num_reqs, budget, plan, s);
+    if (err != cudaSuccess || record(ev.decode_begin, s) != cudaSuccess)
+        return PLMLA_CUDA_ERROR;
+
+    DecodeArgs a;
+    a.q_nope = static_cast<const __nv_bfloat16 *>(q_nope_absorbed);
+    a.q_rope = static_cast<const __nv_bfloat16 *>(q_rope);
+    a.slab = static_cast<const __nv_bfloat16 *>(slab_base);
+    a.page_stride = page_stride_elems;
+    a.num_pages = num_pages;
+    a.page_table = page_table;
+    a.table_ld = page_table_ld;
+    a.seq_lens = seq_lens;
+    a.num_reqs = num_reqs;
+    a.n_q = n_q_per_req;
+    a.num_heads = num_heads;
+    a.rows_per_req = rows_per_req;
+    a.group_rows = group_rows_for(rows_per_req);
+    a.num_groups = rows_per_req / a.group_rows;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.items = plan.items;
+    a.item_count = plan.count;
+    a.o_part = o_part;
+    a.lse_part = lse_part;
+    err = launch_decode_simt(a, w.max_items, s);
+    if (err != cudaSuccess || record(ev.combine_begin, s) != cudaSuccess)
+        return PLMLA_CUDA_ERROR;
+
+    err = launch_combine(o_part, lse_part, plan.indptr,
+                         static_cast<const __nv_bfloat16 *>(gate), num_reqs, n_q_per_req,
+                         num_heads, static_cast<__nv_bfloat16 *>(out), lse, s);
+    if (err != cudaSuccess || record(ev.combine_end, s) != cudaSuccess)
+        return PLMLA_CUDA_ERROR;
+    return PLMLA_OK;
+}
+
+extern "C" plmla_status mla_decode(const void *q_nope_absorbed, const void *q_rope,
+                                   const void *gate, const void *slab_base, int64_t num_pages,
+                                   int64_t page_stride_elems, const int32_t *page_table,
+                                   int64_t page_table_ld, const int32_t *seq_lens,
+                                   int32_t num_reqs, int32_t n_q_per_req, int32_t num_heads,
+                                   float scale, void *out, float *lse, void *workspace,
+                                   size_t workspace_bytes, int32_t cta_budget,
+                                   int32_t min_splits_per_req, void *stream)
+{
+    return mla_decode_ex(q_nope_absorbed, q_rope, gate, slab_base, num_pages, page_stride_elems,
+                         page_table, page_table_ld, seq_lens, num_reqs, n_q_per_req, num_heads,
+                         scale, out, lse, workspace, workspace_bytes, cta_budget,
+                         min_splits_per_req, stream, nullptr);
+}

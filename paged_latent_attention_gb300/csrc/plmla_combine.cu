@@ -1,0 +1,102 @@
+// plmla_combine.cu -- partial-softmax (LSE) merge of KV chunks + sigmoid gate.
+//
+// TokenSpeed Kimi K3 post, section "Gluon kernels on AMD GPUs" (Gated MLA decode:
+// chunk states are merged in a second kernel) and the AgentX post's decode
+// context parallelism paragraph (ranks combine partial attention results).  The
+// gate is the sigmoid output gate of Gated MLA (AgentX post, "Kernel fusion and
+// overlap complete the decode path").
+//
+// One warp per output row (draft token, head).  Each lane owns 16 of the 512
+// latent columns as four float4 groups (lane + 32k), so every split's row is
+// read with fully coalesced 512-byte transactions.  Splits are visited in a
+// fixed order: the result does not depend on scheduling.
+#include <math.h>
+
+#include "plmla_internal.cuh"
+
+namespace plmla {
+namespace {
+
+constexpr int kThreads = 256;
+
+__global__ void __launch_bounds__(kThreads)
+combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
+               const int32_t *__restrict__ indptr, const __nv_bfloat16 *__restrict__ gate,
+               int num_reqs, int n_q, int num_heads, __nv_bfloat16 *__restrict__ out,
+               float *__restrict__ lse)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
+    if (row >= rows)
+        return;
+    const int rows_per_req = n_q * num_heads;
+    const int r = (int)(row / rows_per_req);
+    const int rw = (int)(row % rows_per_req);   // j * H + h within the request
+    const int s0 = indptr[r], s1 = indptr[r + 1];
+
+    float m = -INFINITY;
+    for (int s = s0; s < s1; ++s)
+        m = fmaxf(m, lse_part[(int64_t)s * rows_per_req + rw]);
+
+    float4 acc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+        for (int s = s0; s < s1; ++s) {
+            const float l = lse_part[(int64_t)s * rows_per_req + rw];
+            if (l == -INFINITY)
+                continue;
+            const float w = expf(l - m);
+            wsum += w;
+            const float4 *src = reinterpret_cast<const float4 *>(
+                o_part + ((int64_t)s * rows_per_req + rw) * kLatent);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 v = src[lane + 32 * k];
+                acc[k].x = fmaf(w, v.x, acc[k].x);
+                acc[k].y = fmaf(w, v.y, acc[k].y);
+                acc[k].z = fmaf(w, v.z, acc[k].z);
+                acc[k].w = fmaf(w, v.w, acc[k].w);
+            }
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    const uint2 *g = reinterpret_cast<const uint2 *>(gate + row * kLatent);
+    uint2 *dst = reinterpret_cast<uint2 *>(out + row * kLatent);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint2 graw = g[lane + 32 * k];
+        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw.x));
+        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw.y));
+        const float o0 = acc[k].x * inv / (1.f + expf(-g01.x));
+        const float o1 = acc[k].y * inv / (1.f + expf(-g01.y));
+        const float o2 = acc[k].z * inv / (1.f + expf(-g23.x));
+        const float o3 = acc[k].w * inv / (1.f + expf(-g23.y));
+        const __nv_bfloat162 p01 = __floats2bfloat162_rn(o0, o1);
+        const __nv_bfloat162 p23 = __floats2bfloat162_rn(o2, o3);
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t *>(&p01);
+        packed.y = *reinterpret_cast<const uint32_t *>(&p23);
+        dst[lane + 32 * k] = packed;
+    }
+    if (lse != nullptr && lane == 0)
+        lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const float *o_part, const float *lse_part, const int32_t *indptr,
+                           const __nv_bfloat16 *gate, int num_reqs, int n_q, int num_heads,
+                           __nv_bfloat16 *out, float *lse, cudaStream_t stream)
+{
+    const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
+    const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
+    combine_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(o_part, lse_part, indptr, gate,
+                                                              num_reqs, n_q, num_heads, out, lse);
+    return cudaGetLastError();
+}
+
+}  // namespace plmla

@@ -1,0 +1,83 @@
+"""The C-ABI library builds for sm_103a, loads, and exports what include/plmla.h
+declares (CPU only: no kernel is launched here)."""
+import ctypes
+
+import pytest
+
+import oracle
+from paged_latent_attention_gb300 import _native
+from paged_latent_attention_gb300.build import build_library
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return _native.lib()
+
+
+def test_every_declared_function_is_exported(lib):
+    declared = _native.header_functions()
+    assert set(declared) == set(_native.SIGNATURES), "binding table out of sync with header"
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_names(lib):
+    for code, name in [(0, "PLMLA_OK"), (1, "PLMLA_INVALID_ARGUMENT"), (2, "PLMLA_UNSUPPORTED"),
+                       (3, "PLMLA_WORKSPACE_TOO_SMALL"), (4, "PLMLA_CUDA_ERROR")]:
+        assert _native.strerror(code) == name
+    assert _native.strerror(99) == "PLMLA_UNKNOWN_STATUS"
+
+
+@pytest.mark.parametrize("R,n_q,H,slots,min_splits", [
+    (64, 1, 64, 152, 1), (32, 1, 64, 152, 1), (128, 4, 64, 152, 1), (4, 1, 64, 152, 128),
+    (2, 1, 16, 152, 1), (1, 1, 128, 152, 1), (1000, 2, 48, 148, 3), (7, 3, 16, 16, 2)])
+def test_split_budget_matches_oracle_rule(lib, R, n_q, H, slots, min_splits):
+    rows = n_q * H
+    group = 64 if rows % 64 == 0 else 32 if rows % 32 == 0 else 16
+    expect = oracle.split_budget(R, rows // group, slots, min_splits)
+    assert lib.mla_split_budget(R, n_q, H, slots, min_splits) == expect
+
+
+def test_workspace_grows_with_budget(lib):
+    small = lib.mla_workspace_size(64, 1, 64, 152, 1)
+    big = lib.mla_workspace_size(64, 1, 64, 304, 1)
+    assert 0 < small < big
+    # 152 chunks x 64 rows x 512 fp32 partials dominate
+    assert small >= 152 * 64 * 512 * 4
+
+
+@pytest.mark.parametrize("args", [(0, 1, 64, 152, 1), (2, 0, 64, 152, 1), (2, 1, 24, 152, 1),
+                                  (2, 1, 64, -1, 1), (2, 1, 64, 152, 0), (2000, 1, 64, 152, 1)])
+def test_bad_shapes_are_rejected_on_the_host(lib, args):
+    assert lib.mla_split_budget(*args) == -1
+    assert lib.mla_workspace_size(*args) == 0
+
+
+def test_null_pointers_are_rejected_before_any_launch(lib):
+    st = lib.mla_decode(None, None, None, None, 8, 1536 * 576, None, 1, None, 2, 1, 16,
+                        ctypes.c_float(0.07), None, None, None, 0, 152, 1, None)
+    assert st == 1
+    st = lib.mla_split_combine(None, None, None, None, 2, 1, 16, None, None, None)
+    assert st == 1
+    st = lib.mla_plan_splits(None, 2, 16, None, None, None)
+    assert st == 1
+
+
+def test_misaligned_and_out_of_range_arguments(lib):
+    fake = 1 << 20  # never dereferenced: validation fails first
+    base = dict(q=fake, qr=fake, g=fake, slab=fake, pages=8, stride=1536 * 576, pt=fake, ld=1,
+                lens=fake, R=2, n_q=1, H=16, out=fake, ws=fake)
+
+    def call(**kw):
+        a = {**base, **kw}
+        return lib.mla_decode(a["q"], a["qr"], a["g"], a["slab"], a["pages"], a["stride"],
+                              a["pt"], a["ld"], a["lens"], a["R"], a["n_q"], a["H"],
+                              ctypes.c_float(0.07), a["out"], None, a["ws"], 1 << 30, 152, 1,
+                              None)
+    assert call(q=fake + 2) == 1                 # query not 16-byte aligned
+    assert call(stride=1536 * 576 - 8) == 1      # page stride below a page
+    assert call(stride=1536 * 576 + 4) == 1      # page stride not a multiple of 8 elements
+    assert call(pages=0) == 1
+    assert call(H=24) == 1
+    assert call(ws=fake + 128) == 1              # workspace not 256-byte aligned
