@@ -51,7 +51,8 @@ def assert_parity(out, lse, ref_out, ref_lse, rows=None, what=""):
     assert not bad.any(), (f"{what}: {int(bad.sum())} outputs out of tolerance, "
                            f"max err {err.max():.3e}")
     both_inf = np.isneginf(l) & np.isneginf(ref_lse)
-    lerr = np.where(both_inf, 0.0, np.abs(l - ref_lse))
+    with np.errstate(invalid="ignore"):
+        lerr = np.where(both_inf, 0.0, np.abs(l - ref_lse))
     assert np.all(lerr <= LSE_ATOL), f"{what}: lse max err {np.nanmax(lerr):.3e}"
     return float(err.max()), float(lerr.max())
 
