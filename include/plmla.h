@@ -156,6 +156,44 @@ plmla_status mla_decode(const void *q_nope_absorbed, const void *q_rope, const v
                         size_t workspace_bytes, int32_t cta_budget, int32_t min_splits_per_req,
                         void *stream);
 
+/* Size of the scratch array compiled into the library for mla_decode_static_scratch. */
+#define PLMLA_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * mla_decode_static_scratch -- mla_decode for callers that cannot allocate
+ * device memory.  The source pages have no counterpart to this entry point: it
+ * exists for the library's callers, not for the method.
+ *
+ * Who needs it: a serving engine that reserved nearly all device memory for its
+ * KV page pool up front and allows no later cudaMalloc; a plugin running inside
+ * a framework that owns the device allocator; a latency-critical loop that
+ * cannot afford the device synchronisation cudaMalloc/cudaFree may cause.
+ *
+ * Arguments, results and errors are those of mla_decode without `workspace`
+ * and `workspace_bytes`.  The workspace is a PLMLA_STATIC_SCRATCH_BYTES (32 MiB)
+ * array compiled into the library; every GPU that loads the library holds it
+ * until the process exits.  A shape whose mla_workspace_size(...) exceeds that
+ * size is rejected with PLMLA_WORKSPACE_TOO_SMALL before anything is enqueued.
+ * The call allocates nothing (no cudaMalloc/cudaFree, no allocating library
+ * routine).
+ *
+ * The first call on each device, made with that device current, looks up the
+ * array's device address once (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture.  All calls on a device share the one
+ * array, which keeps the previous call's contents (nothing in it needs to start
+ * at zero).  Calls whose executions overlap on the GPU -- on different streams,
+ * or from several host threads -- race on the array and corrupt each other's
+ * results: serialise them, e.g. on one stream.
+ */
+plmla_status mla_decode_static_scratch(const void *q_nope_absorbed, const void *q_rope,
+                                       const void *gate, const void *slab_base,
+                                       int64_t num_pages, int64_t page_stride_elems,
+                                       const int32_t *page_table, int64_t page_table_ld,
+                                       const int32_t *seq_lens, int32_t num_reqs,
+                                       int32_t n_q_per_req, int32_t num_heads, float scale,
+                                       void *out, float *lse, int32_t cta_budget,
+                                       int32_t min_splits_per_req, void *stream);
+
 /*
  * Optional stage events for mla_decode_ex: each non-NULL member is a cudaEvent_t
  * that is recorded on `stream` at that point of the step (before the plan

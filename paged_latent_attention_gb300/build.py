@@ -26,6 +26,7 @@ SOURCES = [
     "plmla_plan.cu",
     "plmla_combine.cu",
     "plmla_decode_simt.cu",
+    "plmla_static_scratch.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
