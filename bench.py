@@ -36,7 +36,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 KERNELS_PER_STEP = 3          # plan, split decode, combine+gate
-DECODE_SOURCES = ["plmla_decode_simt.cu", "plmla_internal.cuh"]
+DECODE_SOURCES = ["plmla_decode_tc.cu", "plmla_internal.cuh"]
 
 
 def parse_args(argv=None):

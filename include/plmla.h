@@ -139,7 +139,11 @@ plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_reqs, int32_t 
  * out              bf16 [num_reqs*n_q_per_req, num_heads, 512], written
  * lse              fp32 [num_reqs*n_q_per_req, num_heads], written (may be NULL)
  * workspace        device scratch of workspace_bytes >= mla_workspace_size(...),
- *                  256-byte aligned; contents on entry are irrelevant
+ *                  256-byte aligned; contents on entry are irrelevant.  After the
+ *                  step, its first 4 bytes hold the device status word (int32):
+ *                  0 = ok; nonzero = a pipeline wait inside the decode kernel
+ *                  gave up after its time bound and the outputs are invalid
+ *                  (the kernel never traps or spins forever)
  * cta_budget       concurrent CTA slots for the split budget (0 = SM count)
  * min_splits_per_req  >= 1; raises the budget so that equal-length requests get
  *                  at least this many chunks each

@@ -6,6 +6,7 @@ this package only marshals torch tensors into it.
 from .api import (  # noqa: F401
     DEFAULT_SCALE,
     allocate_workspace,
+    device_status,
     mla_decode,
     mla_plan_splits,
     mla_split_budget,

@@ -129,6 +129,12 @@ def mla_decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *, n_q
     return out, lse
 
 
+def device_status(workspace) -> int:
+    """The decode kernel's status word from the workspace of the last step
+    (0 = ok).  Reads device memory: synchronises with the workspace's stream."""
+    return int(workspace[:4].view(torch.int32).item())
+
+
 def mla_plan_splits(seq_lens, split_budget, stream=None):
     """Device split plan: (split_indptr [R+1] int32, chunk [1] int64)."""
     _require(seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()

@@ -25,7 +25,7 @@ SOURCES = [
     "plmla_abi.cu",
     "plmla_plan.cu",
     "plmla_combine.cu",
-    "plmla_decode_simt.cu",
+    "plmla_decode_tc.cu",
     "plmla_static_scratch.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -42,7 +42,7 @@ bool shape_ok(int32_t num_reqs, int32_t n_q, int32_t num_heads)
 }
 
 struct WorkspaceLayout {
-    size_t indptr, chunk, count, items, o_part, lse_part, total;
+    size_t status, indptr, chunk, count, items, o_part, lse_part, total;
     int32_t max_items;
 };
 
@@ -51,6 +51,8 @@ WorkspaceLayout layout_for(int32_t num_reqs, int32_t rows_per_req, int32_t budge
     WorkspaceLayout w;
     w.max_items = budget > num_reqs ? budget : num_reqs;
     size_t off = 0;
+    w.status = off;
+    off = align_up(off + sizeof(int32_t));
     w.indptr = off;
     off = align_up(off + sizeof(int32_t) * (size_t)(num_reqs + 1));
     w.chunk = off;
@@ -126,6 +128,7 @@ extern "C" plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_req
         return PLMLA_INVALID_ARGUMENT;
     // Same kernel as inside mla_decode, without the work-item list.
     PlanBuffers plan;
+    plan.status = nullptr;
     plan.indptr = split_indptr;
     plan.chunk = split_chunk;
     plan.count = nullptr;
@@ -204,6 +207,7 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     unsigned char *ws = static_cast<unsigned char *>(workspace);
     PlanBuffers plan;
+    plan.status = reinterpret_cast<int32_t *>(ws + w.status);
     plan.indptr = reinterpret_cast<int32_t *>(ws + w.indptr);
     plan.chunk = reinterpret_cast<int64_t *>(ws + w.chunk);
     plan.count = reinterpret_cast<int32_t *>(ws + w.count);
@@ -239,7 +243,8 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
     a.item_count = plan.count;
     a.o_part = o_part;
     a.lse_part = lse_part;
-    err = launch_decode_simt(a, w.max_items, s);
+    a.status = plan.status;
+    err = launch_decode_tc(a, w.max_items, s);
     if (err != cudaSuccess || record(ev.combine_begin, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
 

@@ -1,0 +1,758 @@
+// plmla_decode_tc.cu -- split-KV gated-MLA decode on the 5th-generation tensor
+// cores (tcgen05 + TMEM) with TMA page loads, for sm_103a.
+//
+// What one CTA computes: the partial softmax state of one KV chunk [t0, t1) of
+// one request for NG query rows (draft token j, head h):
+//   o_part = sum_t softmax(s)_t c_t over the chunk,   lse_part = ln sum_t e^{s_t}
+// with s_t = scale * (q_nope_absorbed . c_t + q_rope . k_rope_t), all rows
+// sharing the chunk's latent rows (absorbed MLA: TokenSpeed Kimi K3 post,
+// architecture list; chunks and their merge: its "Gluon kernels on AMD GPUs"
+// section, and the AgentX post's per-request splitting).
+//
+// Layout of the work (the "transposed" form, so that every MMA is M = 128 and
+// uses the one-row-per-TMEM-lane accumulator layout):
+//   S^T[t, r]  = K_tile[t, 0:576] . Q[r, 0:576]      M = 128 tokens, N = NG rows
+//   O^T[l, r] += V_tile^T[l, t] . P^T[t, r]          M = 128 latent (x4), N = NG
+// A = the KV tile in shared memory (K-major for S^T, MN-major for O^T: the same
+// bytes), B = Q^T (K-major) or P^T (MN-major).  TMEM holds O^T in four 128-lane
+// blocks (columns 0..255) and S^T at columns 256..256+NG.
+//
+// KV tiles are 128 tokens (always inside one 1,536-token page), loaded by TMA as
+// nine 128 x 64 sub-tiles (16 KB, 128-byte swizzle) from a 3-D tensor map
+// [page][token][576] over the slab: page IDs come from the page table with the
+// table's row stride, and the page offset is 64-bit inside the TMA unit (pools
+// above 2 GB; AgentX - InferenceXv3 report, ROCm AITER section).  Shared memory
+// holds Q^T (9 x NG x 128 B) and exactly one tile; the probability tile P^T
+// (bf16) is written into the rope sub-tile's slot once S^T is done with it, so
+// slots are refilled for the next tile as soon as each O^T block has consumed
+// its two latent sub-tiles.
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
+// owner, warps 2..5 = softmax (one thread per token lane of S^T; the same
+// threads write the partial output, one thread per latent row of O^T).
+//
+// Online softmax in fp32 with a lagged maximum: each tile's column maxima are
+// reduced across the 128 token lanes (warp shuffles + shared memory); the
+// reference maximum m of a row moves only when a tile exceeds it by more than
+// 2^kTau, and only then are O^T's columns and the running sums rescaled.  P =
+// 2^(s*scale*log2e - m) <= 2^kTau stays finite in bf16.
+//
+// Tokens at or past the chunk end (the request's last, partial tile) are
+// masked in the scores and their latent rows are zeroed in shared memory before
+// P^T V, so stale or NaN page contents never reach the output.
+//
+// Every mbarrier wait is bounded: after kWaitLimitNs the waiting thread sets
+// the workspace status word and a CTA-wide abort flag, the producer waits (with
+// its own bound) for the copies it issued, the MMA thread waits for its MMAs,
+// and TMEM is freed before the CTA exits.
+#include <cuda.h>
+#include <math.h>
+
+#include "plmla_internal.cuh"
+
+namespace plmla {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kSub = 9;                         // 8 latent sub-tiles + 1 rope sub-tile
+constexpr int kSubBytes = kTile * 64 * 2;       // 128 tokens x 64 columns bf16
+constexpr int kKvBytes = kSub * kSubBytes;
+constexpr int kTmemCols = 512;
+constexpr int kTmemS = 256;
+constexpr float kTau = 8.0f;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;
+
+template <int NG>
+struct Smem {
+    static constexpr int q_chunk = NG * 128;                // one 64-column chunk of Q^T
+    static constexpr int q_off = kKvBytes;
+    static constexpr int bar_off = q_off + kSub * q_chunk;  // 1024-aligned
+    static constexpr int n_bars = 2 * kSub + 5;
+    static constexpr int red_off = bar_off + 256;           // float red[4][64]
+    static constexpr int fin_off = red_off + 4 * 64 * 4;    // float fin[64]
+    static constexpr int m_off = fin_off + 64 * 4;          // float m[64]   (log2 units)
+    static constexpr int al_off = m_off + 64 * 4;           // float alpha[64]
+    static constexpr int misc_off = al_off + 64 * 4;        // tmem addr, abort, need
+    static constexpr int bytes = misc_off + 16;
+    static constexpr int alloc = bytes + 1024;              // slack for 1024-B alignment
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Slow path of wait_bounded.
+__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                       int32_t *status, int32_t code)
+{
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0u) {
+            if (*abort_flag)
+                return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                atomicExch(status, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Gives up
+// (returns false) when another thread of the CTA aborted, or after
+// kWaitLimitNs, in which case it raises the abort flag and the status word.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int *abort_flag, int32_t *status,
+                                             int32_t code)
+{
+    return mbar_try_wait(bar, parity) || wait_slow(bar, parity, abort_flag, status, code);
+}
+
+// Wait used while tearing down: only time-bounded.
+__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity)
+{
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_ns() - t0 > kDrainLimitNs)
+            return;
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor (tcgen05): start, leading/stride byte offsets
+// (16-byte units), descriptor version 1, swizzle layout in bits 61..63.
+constexpr uint32_t kSw128 = 2, kSw64 = 4, kSw32 = 6;
+
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout)
+{
+    uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)layout << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Named barrier over the 128 softmax threads that also ORs a predicate: every
+// thread gets the same answer, so an abort decided here is taken uniformly.
+__device__ __forceinline__ bool softmax_bar_or(bool pred)
+{
+    uint32_t res;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "selp.b32 %0, 1, 0, p;\n\t}"
+        : "=r"(res)
+        : "r"(pred ? 1u : 0u)
+        : "memory");
+    return res != 0;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Butterfly reduce-scatter of NG per-lane values across a warp.  Afterwards
+// lane l holds the warp-wide result for columns [l*NG/32, (l+1)*NG/32) when
+// NG >= 32, or for column l/2 when NG == 16.
+template <int NG, bool kMax>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[NG], int lane)
+{
+#pragma unroll
+    for (int st = 0; st < 5; ++st) {
+        const int o = 16 >> st;
+        const int half = NG >> (st + 1);
+        if (half >= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < half; ++i) {
+                const float lo = v[i], hi = v[i + half];
+                const float send = upper ? lo : hi;
+                const float keep = upper ? hi : lo;
+                const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+                v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+            }
+        } else {
+            const float recv = __shfl_xor_sync(0xffffffffu, v[0], o);
+            v[0] = kMax ? fmaxf(v[0], recv) : v[0] + recv;
+        }
+    }
+}
+
+template <int NG>
+__device__ __forceinline__ void scatter_to_red(const float (&v)[NG], float *red_q, int lane)
+{
+    if (NG >= 32) {
+#pragma unroll
+        for (int e = 0; e < (NG >= 32 ? NG / 32 : 1); ++e)
+            red_q[lane * (NG / 32) + e] = v[e];
+    } else if ((lane & 1) == 0) {
+        red_q[lane >> 1] = v[0];
+    }
+}
+
+// This thread's row of S^T (one token, NG query rows) in log2 units, with the
+// tokens a row may not see set to -inf: past the chunk end, or past the row's
+// causal limit L - (n_q - 1 - j) among the draft tokens.
+template <int NG>
+__device__ __forceinline__ void load_scores(uint32_t taddr, float scale_log2, bool tile_visible,
+                                            int t, int t_end, int vis_all, int row0, int heads,
+                                            float (&x)[NG])
+{
+#pragma unroll
+    for (int b = 0; b < NG / 16; ++b) {
+        uint32_t r[16];
+        tmem_ld16(taddr + 16 * b, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+            x[16 * b + e] = __uint_as_float(r[e]) * scale_log2;
+    }
+    if (!tile_visible) {
+#pragma unroll
+        for (int c = 0; c < NG; ++c) {
+            const int lim = vis_all + (row0 + c) / heads;
+            if (t >= lim || t >= t_end)
+                x[c] = -INFINITY;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+
+template <int NG>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qn,
+                 const __grid_constant__ CUtensorMap tm_qr, const DecodeArgs a)
+{
+    using L = Smem<NG>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem = reinterpret_cast<unsigned char *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_kv = smem_u32(smem);
+    const uint32_t s_q = s_kv + L::q_off;
+    const uint32_t bars = s_kv + L::bar_off;
+    const uint32_t bar_full = bars;                 // [9]
+    const uint32_t bar_empty = bars + 8 * kSub;     // [9]
+    const uint32_t bar_q = bars + 16 * kSub;
+    const uint32_t bar_s = bar_q + 8;
+    const uint32_t bar_p = bar_q + 16;
+    const uint32_t bar_pv = bar_q + 24;
+    const uint32_t bar_drain = bar_q + 32;
+    float *red = reinterpret_cast<float *>(smem + L::red_off);
+    float *fin = reinterpret_cast<float *>(smem + L::fin_off);
+    float *m_sm = reinterpret_cast<float *>(smem + L::m_off);
+    float *al_sm = reinterpret_cast<float *>(smem + L::al_off);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
+    volatile int *need_sm = reinterpret_cast<volatile int *>(smem + L::misc_off + 8);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int item_idx = blockIdx.x / a.num_groups;
+    const int group = blockIdx.x % a.num_groups;
+    if (item_idx >= *a.item_count)
+        return;
+    const WorkItem it = a.items[item_idx];
+    const int row0 = group * NG;
+    const int n_tiles = (it.t1 - it.t0 + kTile - 1) / kTile;
+
+    if (threadIdx.x == 0) {
+        for (int k = 0; k < kSub; ++k) {
+            mbar_init(bar_full + 8 * k, 1);
+            mbar_init(bar_empty + 8 * k, 1);
+        }
+        mbar_init(bar_q, 1);
+        mbar_init(bar_s, 1);
+        mbar_init(bar_p, 128);
+        mbar_init(bar_pv, 1);
+        mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        *need_sm = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        fence_proxy_async();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0 && n_tiles > 0) {
+            int last_tile = -1, last_k = kSub - 1;
+            const int qrow = it.req * a.rows_per_req + row0;
+            mbar_arrive_expect_tx(bar_q, kSub * L::q_chunk);
+            for (int k = 0; k < kSub - 1; ++k)
+                tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 64 * k, qrow, bar_q);
+            tma_load_2d(s_q + (kSub - 1) * L::q_chunk, &tm_qr, 0, qrow, bar_q);
+            const int32_t *trow = a.page_table + (int64_t)it.req * a.table_ld;
+            for (int i = 0; i < n_tiles; ++i) {
+                const int t = it.t0 + i * kTile;
+                const int page = trow[t / kPageTokens];
+                const int tok = t % kPageTokens;
+                bool ok = true;
+                for (int k = 0; k < kSub; ++k) {
+                    if (!wait_bounded(bar_empty + 8 * k, (i & 1) ^ 1, abort_flag, a.status, 1)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar_full + 8 * k, kSubBytes);
+                    tma_load_3d(s_kv + k * kSubBytes, &tm_kv, 64 * k, tok, page, bar_full + 8 * k);
+                    last_tile = i;
+                    last_k = k;
+                }
+                if (!ok)
+                    break;
+            }
+            // every issued copy must land before the CTA can exit
+            wait_drain(bar_q, 0);
+            for (int k = 0; k < kSub; ++k) {
+                const int tile_k = k <= last_k ? last_tile : last_tile - 1;
+                if (tile_k >= 0)
+                    wait_drain(bar_full + 8 * k, tile_k & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0 && n_tiles > 0) {
+            bool issued = false;
+            constexpr uint32_t idesc_s = idesc_bf16(128, NG, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(128, NG, true, true);
+            constexpr uint32_t p_layout = NG == 64 ? kSw128 : (NG == 32 ? kSw64 : kSw32);
+            const uint32_t s_p = s_kv + (kSub - 1) * kSubBytes;  // P^T lives in the rope slot
+            if (wait_bounded(bar_q, 0, abort_flag, a.status, 2)) {
+                for (int i = 0; i < n_tiles; ++i) {
+                    const uint32_t par = i & 1;
+                    bool ok = true;
+                    // S^T = K_tile . Q^T over the 576 columns
+                    for (int k = 0; k < kSub && ok; ++k) {
+                        if (!wait_bounded(bar_full + 8 * k, par, abort_flag, a.status, 3)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t da = sdesc(s_kv + k * kSubBytes + 32 * kk, 16, 1024, kSw128);
+                            const uint64_t db = sdesc(s_q + k * L::q_chunk + 32 * kk, 16, 1024, kSw128);
+                            mma_bf16(tmem + kTmemS, da, db, idesc_s, (k | kk) != 0);
+                        }
+                        issued = true;
+                    }
+                    if (!ok)
+                        break;
+                    mma_commit(bar_s);
+                    // O^T += V^T . P^T, four 128-row latent blocks over the 128 tokens
+                    if (!wait_bounded(bar_p, par, abort_flag, a.status, 4))
+                        break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t da = sdesc(s_kv + 2 * j * kSubBytes + 2048 * kk,
+                                                      kSubBytes, 1024, kSw128);
+                            const uint64_t db = sdesc(s_p + kk * 32 * NG, 8192, 16 * NG, p_layout);
+                            mma_bf16(tmem + 64 * j, da, db, idesc_pv, (i | kk) != 0);
+                        }
+                        mma_commit(bar_empty + 8 * (2 * j));
+                        mma_commit(bar_empty + 8 * (2 * j + 1));
+                    }
+                    mma_commit(bar_empty + 8 * (kSub - 1));
+                    mma_commit(bar_pv);
+                }
+            }
+            if (issued) {
+                mma_commit(bar_drain);
+                wait_drain(bar_drain, 0);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------- softmax
+        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        const int tok = 32 * q + lane;          // token lane of S^T / latent row of O^T
+        const uint32_t t_lane = (uint32_t)(32 * q) << 16;
+        const int Lr = a.seq_lens[it.req];
+        const int vis_all = Lr - (a.n_q - 1);   // tokens below this are visible to every row
+        const uint32_t s_p = s_kv + (kSub - 1) * kSubBytes;
+        float lsum[NG];
+#pragma unroll
+        for (int c = 0; c < NG; ++c)
+            lsum[c] = 0.f;
+        for (int c = threadIdx.x - 64; c < NG; c += 128)
+            m_sm[c] = -INFINITY;
+        softmax_bar();
+
+        bool ok = n_tiles > 0;
+        for (int i = 0; i < n_tiles; ++i) {
+            const uint32_t par = i & 1;
+            const int t_base = it.t0 + i * kTile;
+            const int t = t_base + tok;
+            const bool tile_visible = t_base + kTile <= vis_all;
+            // warp-uniform, because tcgen05.ld below is a .sync.aligned instruction
+            const bool got = __all_sync(0xffffffffu, wait_bounded(bar_s, par, abort_flag, a.status, 5));
+            float x[NG];
+            if (got) {
+                tc_fence_after();
+                load_scores<NG>(tmem + t_lane + kTmemS, a.scale_log2, tile_visible, t, it.t1,
+                                vis_all, row0, a.num_heads, x);
+                // column maxima over the tile's 128 tokens (x is consumed)
+                warp_reduce_scatter<NG, true>(x, lane);
+                scatter_to_red<NG>(x, red + 64 * q, lane);
+            }
+            if (softmax_bar_or(!got || *abort_flag)) {
+                ok = false;
+                break;
+            }
+            if (q == 0) {
+                bool any = false;
+                for (int c = lane; c < NG; c += 32) {
+                    const float mt = fmaxf(fmaxf(red[c], red[64 + c]), fmaxf(red[128 + c], red[192 + c]));
+                    const float mu = m_sm[c];
+                    float alpha = 1.f;
+                    if (mt > mu + kTau) {
+                        alpha = fast_exp2(mu - mt);   // 0 when mu = -inf
+                        m_sm[c] = mt;
+                        any = true;
+                    }
+                    al_sm[c] = alpha;
+                }
+                any = __any_sync(0xffffffffu, any);
+                if (lane == 0)
+                    *need_sm = any ? 1 : 0;
+            }
+            softmax_bar();
+            if (*need_sm != 0) {
+#pragma unroll
+                for (int c = 0; c < NG; ++c)
+                    lsum[c] *= al_sm[c];
+                if (i > 0) {
+                    // O^T columns are rescaled once the previous tile's P^T V is done
+                    const bool done = wait_bounded(bar_pv, (i - 1) & 1, abort_flag, a.status, 6);
+                    if (softmax_bar_or(!done)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                        for (int b = 0; b < NG / 16; ++b) {
+                            uint32_t r[16];
+                            const uint32_t ta = tmem + t_lane + 64 * j + 16 * b;
+                            tmem_ld16(ta, r);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                r[e] = __float_as_uint(__uint_as_float(r[e]) * al_sm[16 * b + e]);
+                            tmem_st16(ta, r);
+                        }
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // probabilities, running sums, and this token's P^T row (bf16, swizzled)
+            load_scores<NG>(tmem + t_lane + kTmemS, a.scale_log2, tile_visible, t, it.t1, vis_all,
+                            row0, a.num_heads, x);
+            {
+                constexpr int row_bytes = 2 * NG;
+                constexpr int swz_bits = NG == 64 ? 3 : (NG == 32 ? 2 : 1);
+#pragma unroll
+                for (int ch = 0; ch < row_bytes / 16; ++ch) {
+                    uint32_t w4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = 8 * ch + 2 * e;
+                        const float p0 = x[c] == -INFINITY ? 0.f : fast_exp2(x[c] - m_sm[c]);
+                        const float p1 =
+                            x[c + 1] == -INFINITY ? 0.f : fast_exp2(x[c + 1] - m_sm[c + 1]);
+                        lsum[c] += p0;
+                        lsum[c + 1] += p1;
+                        w4[e] = pack_bf16x2(p0, p1);
+                    }
+                    const uint32_t off = (uint32_t)(tok * row_bytes + 16 * ch);
+                    const uint32_t sw = off ^ (((off >> 7) & ((1u << swz_bits) - 1u)) << 4);
+                    st_shared_v4(s_p + sw, w4[0], w4[1], w4[2], w4[3]);
+                }
+            }
+            if (t >= it.t1) {
+                // past the request's history: zero this token's latent row so
+                // that P = 0 never meets a stale (possibly NaN) value in the MMA
+#pragma unroll
+                for (int k = 0; k < kSub - 1; ++k)
+#pragma unroll
+                    for (int ch = 0; ch < 8; ++ch)
+                        st_shared_v4(s_kv + k * kSubBytes + tok * 128 + 16 * ch, 0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(bar_p);
+        }
+
+        if (ok) {
+            const bool done = wait_bounded(bar_pv, (n_tiles - 1) & 1, abort_flag, a.status, 7);
+            ok = !softmax_bar_or(!done);
+        }
+        if (ok) {
+            tc_fence_after();
+            // row sums over the 128 token lanes
+            warp_reduce_scatter<NG, false>(lsum, lane);
+            scatter_to_red<NG>(lsum, red + 64 * q, lane);
+            softmax_bar();
+            if (q == 0)
+                for (int c = lane; c < NG; c += 32)
+                    fin[c] = red[c] + red[64 + c] + red[128 + c] + red[192 + c];
+            softmax_bar();
+            // normalised partial output: thread = latent row of each O^T block
+            const int64_t out_row0 = (int64_t)it.split * a.rows_per_req + row0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                for (int b = 0; b < NG / 16; ++b) {
+                    uint32_t r[16];
+                    tmem_ld16(tmem + t_lane + 64 * j + 16 * b, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int c = 16 * b + e;
+                        const float l = fin[c];
+                        const float o = l > 0.f ? __uint_as_float(r[e]) / l : 0.f;
+                        a.o_part[(out_row0 + c) * kLatent + 128 * j + tok] = o;
+                    }
+                }
+            }
+            for (int c = threadIdx.x - 64; c < NG; c += 128) {
+                const float l = fin[c];
+                a.lse_part[out_row0 + c] = l > 0.f ? (m_sm[c] + log2f(l)) * kLn2 : -INFINITY;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// host side: tensor maps and launch
+// ---------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
+              const cuuint64_t *strides, const cuuint32_t *box)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr)
+        return false;
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
+              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NG>
+cudaError_t launch_ng(const DecodeArgs &a, int max_items, cudaStream_t stream)
+{
+    CUtensorMap tm_kv, tm_qn, tm_qr;
+    const cuuint64_t kv_dims[3] = {(cuuint64_t)kRow, (cuuint64_t)kPageTokens,
+                                   (cuuint64_t)a.num_pages};
+    const cuuint64_t kv_strides[2] = {(cuuint64_t)kRow * 2, (cuuint64_t)a.page_stride * 2};
+    const cuuint32_t kv_box[3] = {64, (cuuint32_t)kTile, 1};
+    const cuuint64_t rows = (cuuint64_t)a.num_reqs * a.rows_per_req;
+    const cuuint64_t qn_dims[2] = {(cuuint64_t)kLatent, rows};
+    const cuuint64_t qn_strides[1] = {(cuuint64_t)kLatent * 2};
+    const cuuint64_t qr_dims[2] = {(cuuint64_t)kRope, rows};
+    const cuuint64_t qr_strides[1] = {(cuuint64_t)kRope * 2};
+    const cuuint32_t q_box[2] = {64, (cuuint32_t)NG};
+    if (!make_map(&tm_kv, a.slab, 3, kv_dims, kv_strides, kv_box) ||
+        !make_map(&tm_qn, a.q_nope, 2, qn_dims, qn_strides, q_box) ||
+        !make_map(&tm_qr, a.q_rope, 2, qr_dims, qr_strides, q_box))
+        return cudaErrorInvalidValue;
+    constexpr int smem = Smem<NG>::alloc;
+    static_assert(Smem<NG>::alloc <= 232448, "shared memory budget");
+    cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<NG>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess)
+        return err;
+    const unsigned grid = (unsigned)max_items * (unsigned)a.num_groups;
+    decode_tc_kernel<NG><<<grid, kThreads, smem, stream>>>(tm_kv, tm_qn, tm_qr, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_tc(const DecodeArgs &args, int max_items, cudaStream_t stream)
+{
+    switch (args.group_rows) {
+    case 64: return launch_ng<64>(args, max_items, stream);
+    case 32: return launch_ng<32>(args, max_items, stream);
+    case 16: return launch_ng<16>(args, max_items, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace plmla

@@ -27,6 +27,7 @@ struct __align__(16) WorkItem {
 };
 
 struct PlanBuffers {
+    int32_t *status;   // [1] device status word, reset to 0 by the plan kernel
     int32_t *indptr;   // [R + 1]
     int64_t *chunk;    // [1]
     int32_t *count;    // [1] number of work items
@@ -51,6 +52,7 @@ struct DecodeArgs {
     const int32_t *item_count;
     float *o_part;                 // [splits, rows_per_req, 512]
     float *lse_part;               // [splits, rows_per_req], natural log
+    int32_t *status;               // device status word (0 = ok, else the failed wait)
 };
 
 // Largest of 64, 32, 16 that divides `rows`, or 0.
@@ -64,7 +66,7 @@ inline int group_rows_for(int rows)
 
 cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, PlanBuffers plan,
                         cudaStream_t stream);
-cudaError_t launch_decode_simt(const DecodeArgs &args, int max_items, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeArgs &args, int max_items, cudaStream_t stream);
 cudaError_t launch_combine(const float *o_part, const float *lse_part, const int32_t *indptr,
                            const __nv_bfloat16 *gate, int num_reqs, int n_q, int num_heads,
                            __nv_bfloat16 *out, float *lse, cudaStream_t stream);

@@ -179,6 +179,8 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, Plan
         }
     }
     if (tid == 0) {
+        if (plan.status != nullptr)
+            *plan.status = 0;
         plan.indptr[num_reqs] = n_splits;
         *plan.chunk = chunk;
         if (plan.count != nullptr)

@@ -24,10 +24,13 @@ def to_device(w: inputs.Workload, qn, qr, gate, slab, device="cuda"):
 
 
 def gpu_decode(w, d, *, cta_budget=0, min_splits=None, scale=SCALE):
+    ms = min_splits or w.min_splits
+    ws = api.allocate_workspace(w.num_reqs, w.n_q, w.num_heads, cta_budget, ms, "cuda")
     out, lse = api.mla_decode(d["qn"], d["qr"], d["gate"], d["slab"], d["table"], d["lens"],
-                              n_q=w.n_q, scale=scale, cta_budget=cta_budget,
-                              min_splits=min_splits or w.min_splits)
+                              n_q=w.n_q, scale=scale, cta_budget=cta_budget, min_splits=ms,
+                              workspace=ws)
     torch.cuda.synchronize()
+    assert api.device_status(ws) == 0, "a decode pipeline wait timed out"
     return out, lse
 
 
