@@ -66,26 +66,29 @@ enum {
 const char *mla_strerror(plmla_status status);
 
 /*
- * mla_split_budget -- number of KV chunks ("splits") one decode step may use in
- * total, derived from the machine as [IX] asks (a hard-coded budget starved a
- * large GPU).  Pure host arithmetic.
+ * mla_split_budget -- the chunk budget mla_decode plans with: how many KV chunks
+ * the per-request split rule of [AX, Figure 4] may create for this shape, taken
+ * from the machine as [IX] asks (a hard-coded budget starved a large GPU).  Pure
+ * host arithmetic.
  *
- *   row_groups = n_q * num_heads / group_rows, where group_rows is the largest
- *                of 64, 32, 16 dividing n_q * num_heads (rows a decode CTA owns)
+ *   group_rows = the largest of 64, 32, 16 dividing n_q * num_heads (query rows
+ *                one CTA owns); row_groups = n_q * num_heads / group_rows
  *   slots      = cta_budget, or the current device's SM count when 0
- *   waves      = max(1, ceil(num_reqs * row_groups * min_splits_per_req / slots))
- *   budget     = max(1, floor(waves * slots / row_groups))
+ *   members    = max(1, floor(slots / row_groups))   (persistent CTAs per group)
+ *   budget     = max(16 * members, num_reqs * min_splits_per_req), at most 4096
  *
- * Returns the budget, or -1 for invalid arguments / no CUDA device when
- * cta_budget == 0.
+ * mla_decode runs row_groups x members persistent CTAs; each takes a contiguous,
+ * tile-balanced run of the chunks.  Returns the budget, or -1 for invalid
+ * arguments, a budget above 4096, or no CUDA device when cta_budget == 0.
  */
 int32_t mla_split_budget(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_budget,
                          int32_t min_splits_per_req);
 
 /*
  * mla_workspace_size -- bytes of device workspace mla_decode needs for this
- * shape (plan arrays, fp32 partial outputs and partial log-sum-exps for up to
- * max(budget, num_reqs) chunks).  0 on invalid arguments.  Pure host arithmetic.
+ * shape: the plan and schedule arrays, and fp32 partial outputs and partial
+ * log-sum-exps for at most row_groups x (num_reqs + members) segments.  0 on
+ * invalid arguments.  Pure host arithmetic.
  */
 size_t mla_workspace_size(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_budget,
                           int32_t min_splits_per_req);
@@ -100,6 +103,7 @@ size_t mla_workspace_size(int32_t num_reqs, int32_t n_q, int32_t num_heads, int3
  *   split s of request r covers tokens [s*chunk, min((s+1)*chunk, L_r)).
  *
  * seq_lens      [num_reqs] int32, device, L_r >= 0;  num_reqs 1 .. 1024.
+ * split_budget  1 .. 4096 (PLMLA_UNSUPPORTED above).
  * split_indptr  [num_reqs + 1] int32, device, written: exclusive prefix sum of
  *               splits_r in request order (split ids of request r are
  *               split_indptr[r] .. split_indptr[r+1]-1).
@@ -149,7 +153,8 @@ plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_reqs, int32_t 
  *                  at least this many chunks each
  * stream           cudaStream_t
  *
- * Enqueues: plan kernel -> split-decode kernel -> combine/gate kernel.
+ * Enqueues: plan kernel (split plan + persistent schedule) -> split-decode
+ * kernel (one persistent CTA per SM and row group) -> combine/gate kernel.
  * Page IDs are trusted: an ID outside [0, num_pages) is undefined behaviour.
  */
 plmla_status mla_decode(const void *q_nope_absorbed, const void *q_rope, const void *gate,

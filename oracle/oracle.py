@@ -202,11 +202,15 @@ def plan_splits(seq_lens, budget: int, tile: int):
     return chunk, [_ceil_div(L, chunk) if L > 0 else 0 for L in lens]
 
 
-def split_budget(num_reqs: int, row_groups: int, cta_slots: int, min_splits: int) -> int:
-    """Split budget derived from the machine: enough whole waves of CTA slots to
-    give every request at least ``min_splits`` chunks, divided among the row
-    groups that share each chunk.  A hard-coded budget left most of a large GPU
-    idle at batch 1 (AgentX - InferenceXv3 report, context-parallel section on
-    in-GPU parallelism limits)."""
-    waves = max(1, _ceil_div(num_reqs * row_groups * max(1, min_splits), cta_slots))
-    return max(1, (waves * cta_slots) // row_groups)
+def split_budget(num_reqs: int, row_groups: int, cta_slots: int, min_splits: int,
+                 chunks_per_member: int = 16, limit: int = 4096) -> int:
+    """Chunk budget derived from the machine: 16 chunks for every persistent CTA
+    of a row group, or enough for ``min_splits`` chunks per request if that is
+    more.  A hard-coded budget left most of a large GPU idle at batch 1 (AgentX -
+    InferenceXv3 report, context-parallel section on in-GPU parallelism limits).
+    Raises ValueError above ``limit``."""
+    members = max(1, cta_slots // row_groups)
+    budget = max(chunks_per_member * members, num_reqs * max(1, min_splits))
+    if budget > limit:
+        raise ValueError("budget above the planner's limit")
+    return budget

@@ -42,14 +42,52 @@ bool shape_ok(int32_t num_reqs, int32_t n_q, int32_t num_heads)
 }
 
 struct WorkspaceLayout {
-    size_t status, indptr, chunk, count, items, o_part, lse_part, total;
-    int32_t max_items;
+    size_t status, indptr, chunk, seg_count, segments, seg_req, seg_member, o_part, lse_part,
+        total;
+    int32_t max_segments;
 };
 
-WorkspaceLayout layout_for(int32_t num_reqs, int32_t rows_per_req, int32_t budget)
+struct Shape {
+    int32_t rows_per_req, group_rows, groups, members, budget;
+};
+
+// Split budget and team layout for a decode shape (see mla_split_budget).
+bool shape_for(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_budget,
+               int32_t min_splits, Shape *out)
+{
+    if (!shape_ok(num_reqs, n_q, num_heads) || cta_budget < 0 || min_splits < 1)
+        return false;
+    Shape sh;
+    sh.rows_per_req = n_q * num_heads;
+    sh.group_rows = group_rows_for(sh.rows_per_req);
+    if (sh.group_rows == 0)
+        return false;
+    sh.groups = sh.rows_per_req / sh.group_rows;
+    const int64_t slots = cta_budget > 0 ? cta_budget : current_sm_count();
+    if (slots <= 0)
+        return false;
+    sh.members = (int32_t)(slots / sh.groups > 0 ? slots / sh.groups : 1);
+    int64_t budget = (int64_t)kChunksPerMember * sh.members;
+    const int64_t wanted = (int64_t)num_reqs * min_splits;
+    if (wanted > budget)
+        budget = wanted;
+    if (budget > kMaxPlanSplits)
+        budget = kMaxPlanSplits;
+    if (wanted > budget)
+        return false;
+    sh.budget = (int32_t)budget;
+    *out = sh;
+    return true;
+}
+
+WorkspaceLayout layout_for(int32_t num_reqs, const Shape &sh)
 {
     WorkspaceLayout w;
-    w.max_items = budget > num_reqs ? budget : num_reqs;
+    // a segment starts only where the request or the CTA changes along the
+    // request-ordered chunks, so there are at most R + members - 1 of them
+    const int32_t max_chunks = sh.budget > num_reqs ? sh.budget : num_reqs;
+    const int32_t max_runs = num_reqs + sh.members;
+    w.max_segments = max_chunks < max_runs ? max_chunks : max_runs;
     size_t off = 0;
     w.status = off;
     off = align_up(off + sizeof(int32_t));
@@ -57,14 +95,19 @@ WorkspaceLayout layout_for(int32_t num_reqs, int32_t rows_per_req, int32_t budge
     off = align_up(off + sizeof(int32_t) * (size_t)(num_reqs + 1));
     w.chunk = off;
     off = align_up(off + sizeof(int64_t));
-    w.count = off;
+    w.seg_count = off;
     off = align_up(off + sizeof(int32_t));
-    w.items = off;
-    off = align_up(off + sizeof(WorkItem) * (size_t)w.max_items);
+    w.segments = off;
+    off = align_up(off + sizeof(int4) * (size_t)w.max_segments);
+    w.seg_req = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)(num_reqs + 1));
+    w.seg_member = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)(sh.members + 1));
+    const size_t part_rows = (size_t)sh.groups * w.max_segments * sh.group_rows;
     w.o_part = off;
-    off = align_up(off + sizeof(float) * (size_t)w.max_items * rows_per_req * kLatent);
+    off = align_up(off + sizeof(float) * part_rows * kLatent);
     w.lse_part = off;
-    off = align_up(off + sizeof(float) * (size_t)w.max_items * rows_per_req);
+    off = align_up(off + sizeof(float) * part_rows);
     w.total = off;
     return w;
 }
@@ -86,36 +129,19 @@ extern "C" const char *mla_strerror(plmla_status status)
 extern "C" int32_t mla_split_budget(int32_t num_reqs, int32_t n_q, int32_t num_heads,
                                     int32_t cta_budget, int32_t min_splits_per_req)
 {
-    if (!shape_ok(num_reqs, n_q, num_heads) || cta_budget < 0 || min_splits_per_req < 1)
+    Shape sh;
+    if (!shape_for(num_reqs, n_q, num_heads, cta_budget, min_splits_per_req, &sh))
         return -1;
-    const int rows = n_q * num_heads;
-    const int group_rows = group_rows_for(rows);
-    if (group_rows == 0)
-        return -1;
-    const int64_t groups = rows / group_rows;
-    const int64_t slots = cta_budget > 0 ? cta_budget : current_sm_count();
-    if (slots <= 0)
-        return -1;
-    const int64_t units = (int64_t)num_reqs * groups * min_splits_per_req;
-    int64_t waves = (units + slots - 1) / slots;
-    if (waves < 1)
-        waves = 1;
-    int64_t budget = (waves * slots) / groups;
-    if (budget < 1)
-        budget = 1;
-    if (budget > (int64_t)1 << 20)
-        return -1;
-    return (int32_t)budget;
+    return sh.budget;
 }
 
 extern "C" size_t mla_workspace_size(int32_t num_reqs, int32_t n_q, int32_t num_heads,
                                      int32_t cta_budget, int32_t min_splits_per_req)
 {
-    const int32_t budget = mla_split_budget(num_reqs, n_q, num_heads, cta_budget,
-                                            min_splits_per_req);
-    if (budget < 1)
+    Shape sh;
+    if (!shape_for(num_reqs, n_q, num_heads, cta_budget, min_splits_per_req, &sh))
         return 0;
-    return layout_for(num_reqs, n_q * num_heads, budget).total;
+    return layout_for(num_reqs, sh).total;
 }
 
 extern "C" plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_reqs,
@@ -126,14 +152,13 @@ extern "C" plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_req
         num_reqs < 1 || num_reqs > kMaxReqs || split_budget < 1 || !aligned(seq_lens, 4) ||
         !aligned(split_indptr, 4) || !aligned(split_chunk, 8))
         return PLMLA_INVALID_ARGUMENT;
-    // Same kernel as inside mla_decode, without the work-item list.
-    PlanBuffers plan;
-    plan.status = nullptr;
+    if (split_budget > kMaxPlanSplits)
+        return PLMLA_UNSUPPORTED;
+    // Same kernel as inside mla_decode, without the persistent schedule.
+    PlanBuffers plan = {};
     plan.indptr = split_indptr;
     plan.chunk = split_chunk;
-    plan.count = nullptr;
-    plan.items = nullptr;
-    cudaError_t err = launch_plan(seq_lens, num_reqs, split_budget, plan,
+    cudaError_t err = launch_plan(seq_lens, num_reqs, split_budget, 1, plan,
                                   static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
 }
@@ -152,7 +177,8 @@ extern "C" plmla_status mla_split_combine(const float *o_part, const float *lse_
     if (!aligned(o_part, 16) || !aligned(lse_part, 4) || !aligned(gate, 8) ||
         !aligned(out, 8) || (lse != nullptr && !aligned(lse, 4)))
         return PLMLA_INVALID_ARGUMENT;
-    cudaError_t err = launch_combine(o_part, lse_part, split_indptr,
+    cudaError_t err = launch_combine(o_part, lse_part, split_indptr, nullptr,
+                                     n_q_per_req * num_heads,
                                      static_cast<const __nv_bfloat16 *>(gate), num_reqs,
                                      n_q_per_req, num_heads, static_cast<__nv_bfloat16 *>(out),
                                      lse, static_cast<cudaStream_t>(stream));
@@ -195,12 +221,11 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
         (lse != nullptr && !aligned(lse, 4)))
         return PLMLA_INVALID_ARGUMENT;
 
-    const int32_t budget = mla_split_budget(num_reqs, n_q_per_req, num_heads, cta_budget,
-                                            min_splits_per_req);
-    if (budget < 1)
-        return cta_budget == 0 ? PLMLA_CUDA_ERROR : PLMLA_INVALID_ARGUMENT;
-    const int rows_per_req = n_q_per_req * num_heads;
-    const WorkspaceLayout w = layout_for(num_reqs, rows_per_req, budget);
+    Shape sh;
+    if (!shape_for(num_reqs, n_q_per_req, num_heads, cta_budget, min_splits_per_req, &sh))
+        return (cta_budget == 0 && current_sm_count() <= 0) ? PLMLA_CUDA_ERROR
+                                                            : PLMLA_UNSUPPORTED;
+    const WorkspaceLayout w = layout_for(num_reqs, sh);
     if (workspace_bytes < w.total)
         return PLMLA_WORKSPACE_TOO_SMALL;
 
@@ -210,8 +235,10 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
     plan.status = reinterpret_cast<int32_t *>(ws + w.status);
     plan.indptr = reinterpret_cast<int32_t *>(ws + w.indptr);
     plan.chunk = reinterpret_cast<int64_t *>(ws + w.chunk);
-    plan.count = reinterpret_cast<int32_t *>(ws + w.count);
-    plan.items = reinterpret_cast<WorkItem *>(ws + w.items);
+    plan.seg_count = reinterpret_cast<int32_t *>(ws + w.seg_count);
+    plan.segments = reinterpret_cast<int4 *>(ws + w.segments);
+    plan.seg_req_indptr = reinterpret_cast<int32_t *>(ws + w.seg_req);
+    plan.seg_member_indptr = reinterpret_cast<int32_t *>(ws + w.seg_member);
     float *o_part = reinterpret_cast<float *>(ws + w.o_part);
     float *lse_part = reinterpret_cast<float *>(ws + w.lse_part);
 
@@ -219,7 +246,7 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
     const plmla_stage_events &ev = events != nullptr ? *events : none;
     if (record(ev.plan_begin, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
-    cudaError_t err = launch_plan(seq_lens, num_reqs, budget, plan, s);
+    cudaError_t err = launch_plan(seq_lens, num_reqs, sh.budget, sh.members, plan, s);
     if (err != cudaSuccess || record(ev.decode_begin, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
 
@@ -235,20 +262,22 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
     a.num_reqs = num_reqs;
     a.n_q = n_q_per_req;
     a.num_heads = num_heads;
-    a.rows_per_req = rows_per_req;
-    a.group_rows = group_rows_for(rows_per_req);
-    a.num_groups = rows_per_req / a.group_rows;
+    a.rows_per_req = sh.rows_per_req;
+    a.group_rows = sh.group_rows;
+    a.num_groups = sh.groups;
+    a.members = sh.members;
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.items = plan.items;
-    a.item_count = plan.count;
+    a.segments = plan.segments;
+    a.seg_member_indptr = plan.seg_member_indptr;
+    a.seg_count = plan.seg_count;
     a.o_part = o_part;
     a.lse_part = lse_part;
     a.status = plan.status;
-    err = launch_decode_tc(a, w.max_items, s);
+    err = launch_decode_tc(a, s);
     if (err != cudaSuccess || record(ev.combine_begin, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
 
-    err = launch_combine(o_part, lse_part, plan.indptr,
+    err = launch_combine(o_part, lse_part, plan.seg_req_indptr, plan.seg_count, sh.group_rows,
                          static_cast<const __nv_bfloat16 *>(gate), num_reqs, n_q_per_req,
                          num_heads, static_cast<__nv_bfloat16 *>(out), lse, s);
     if (err != cudaSuccess || record(ev.combine_end, s) != cudaSuccess)

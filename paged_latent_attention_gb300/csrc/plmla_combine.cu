@@ -21,9 +21,9 @@ constexpr int kThreads = 256;
 
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
-               const int32_t *__restrict__ indptr, const __nv_bfloat16 *__restrict__ gate,
-               int num_reqs, int n_q, int num_heads, __nv_bfloat16 *__restrict__ out,
-               float *__restrict__ lse)
+               const int32_t *__restrict__ indptr, const int32_t *__restrict__ seg_stride,
+               int group_rows, const __nv_bfloat16 *__restrict__ gate, int num_reqs, int n_q,
+               int num_heads, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse)
 {
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -33,11 +33,14 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     const int rows_per_req = n_q * num_heads;
     const int r = (int)(row / rows_per_req);
     const int rw = (int)(row % rows_per_req);   // j * H + h within the request
-    const int s0 = indptr[r], s1 = indptr[r + 1];
+    const int g = rw / group_rows;               // row group (team) of this row
+    const int gi = rw % group_rows;              // row inside the group's partials
+    const int base = seg_stride != nullptr ? g * (*seg_stride) : 0;
+    const int s0 = base + indptr[r], s1 = base + indptr[r + 1];
 
     float m = -INFINITY;
     for (int s = s0; s < s1; ++s)
-        m = fmaxf(m, lse_part[(int64_t)s * rows_per_req + rw]);
+        m = fmaxf(m, lse_part[(int64_t)s * group_rows + gi]);
 
     float4 acc[4];
 #pragma unroll
@@ -46,13 +49,13 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     float wsum = 0.f;
     if (m != -INFINITY) {
         for (int s = s0; s < s1; ++s) {
-            const float l = lse_part[(int64_t)s * rows_per_req + rw];
+            const float l = lse_part[(int64_t)s * group_rows + gi];
             if (l == -INFINITY)
                 continue;
             const float w = expf(l - m);
             wsum += w;
             const float4 *src = reinterpret_cast<const float4 *>(
-                o_part + ((int64_t)s * rows_per_req + rw) * kLatent);
+                o_part + ((int64_t)s * group_rows + gi) * kLatent);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const float4 v = src[lane + 32 * k];
@@ -64,11 +67,11 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
         }
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const uint2 *g = reinterpret_cast<const uint2 *>(gate + row * kLatent);
+    const uint2 *gp = reinterpret_cast<const uint2 *>(gate + row * kLatent);
     uint2 *dst = reinterpret_cast<uint2 *>(out + row * kLatent);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const uint2 graw = g[lane + 32 * k];
+        const uint2 graw = gp[lane + 32 * k];
         const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw.x));
         const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw.y));
         const float o0 = acc[k].x * inv / (1.f + expf(-g01.x));
@@ -89,12 +92,14 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
 }  // namespace
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, const int32_t *indptr,
+                           const int32_t *seg_stride, int group_rows,
                            const __nv_bfloat16 *gate, int num_reqs, int n_q, int num_heads,
                            __nv_bfloat16 *out, float *lse, cudaStream_t stream)
 {
     const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
     const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
-    combine_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(o_part, lse_part, indptr, gate,
+    combine_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(o_part, lse_part, indptr,
+                                                              seg_stride, group_rows, gate,
                                                               num_reqs, n_q, num_heads, out, lse);
     return cudaGetLastError();
 }

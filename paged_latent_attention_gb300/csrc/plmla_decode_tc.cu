@@ -31,11 +31,13 @@
 // owner, warps 2..5 = softmax (one thread per token lane of S^T; the same
 // threads write the partial output, one thread per latent row of O^T).
 //
-// Online softmax in fp32 with a lagged maximum: each tile's column maxima are
-// reduced across the 128 token lanes (warp shuffles + shared memory); the
-// reference maximum m of a row moves only when a tile exceeds it by more than
-// 2^kTau, and only then are O^T's columns and the running sums rescaled.  P =
-// 2^(s*scale*log2e - m) <= 2^kTau stays finite in bf16.
+// Online softmax in fp32 with a lagged maximum: the reference maximum m of a
+// row moves only when a score exceeds it by more than kTau (log2 units).  Each
+// tile, every token lane tests its scores against m and one barrier ORs the
+// answers; only then (always on a segment's first tile, rarely after) are the
+// column maxima reduced across the 128 lanes (warp shuffles + shared memory)
+// and O^T's columns and the running sums rescaled.  P = 2^(s*scale*log2e - m)
+// <= 2^kTau stays finite in bf16.
 //
 // Tokens at or past the chunk end (the request's last, partial tile) are
 // masked in the scores and their latent rows are zeroed in shared memory before
@@ -69,8 +71,7 @@ struct Smem {
     static constexpr int q_chunk = NG * 128;                // one 64-column chunk of Q^T
     static constexpr int q_off = kKvBytes;
     static constexpr int bar_off = q_off + kSub * q_chunk;  // 1024-aligned
-    static constexpr int n_bars = 2 * kSub + 5;
-    static constexpr int red_off = bar_off + 256;           // float red[4][64]
+    static constexpr int red_off = bar_off + 256;           // float red[4][64] (25 mbarriers before)
     static constexpr int fin_off = red_off + 4 * 64 * 4;    // float fin[64]
     static constexpr int m_off = fin_off + 64 * 4;          // float m[64]   (log2 units)
     static constexpr int al_off = m_off + 64 * 4;           // float alpha[64]
@@ -326,7 +327,8 @@ __device__ __forceinline__ void scatter_to_red(const float (&v)[NG], float *red_
 
 // This thread's row of S^T (one token, NG query rows) in log2 units, with the
 // tokens a row may not see set to -inf: past the chunk end, or past the row's
-// causal limit L - (n_q - 1 - j) among the draft tokens.
+// causal limit L - (n_q - 1 - j) among the draft tokens.  The mask runs behind
+// one branch that is taken only on a request's last tiles.
 template <int NG>
 __device__ __forceinline__ void load_scores(uint32_t taddr, float scale_log2, bool tile_visible,
                                             int t, int t_end, int vis_all, int row0, int heads,
@@ -351,6 +353,36 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, float scale_log2, bo
     }
 }
 
+// Shift this thread's scores to x - m (m = the row's reference maximum, 0
+// while still -inf) and report whether any score lies more than kTau above m.
+// A row whose m is -inf yields +inf for a visible score (flagged) and NaN for
+// a masked one (ignored by fmaxf).
+template <int NG>
+__device__ __forceinline__ bool shift_and_test(float (&x)[NG], uint32_t m_addr)
+{
+    float vmax = -INFINITY;
+#pragma unroll
+    for (int c4 = 0; c4 < NG; c4 += 4) {
+        float m[4];
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(m[0]), "=f"(m[1]), "=f"(m[2]), "=f"(m[3])
+                     : "r"(m_addr + 4 * c4));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            vmax = fmaxf(vmax, x[c4 + e] - m[e]);
+            x[c4 + e] -= m[e] == -INFINITY ? 0.f : m[e];
+        }
+    }
+    return vmax > kTau;
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -367,13 +399,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     const uint32_t s_kv = smem_u32(smem);
     const uint32_t s_q = s_kv + L::q_off;
     const uint32_t bars = s_kv + L::bar_off;
-    const uint32_t bar_full = bars;                 // [9]
-    const uint32_t bar_empty = bars + 8 * kSub;     // [9]
-    const uint32_t bar_q = bars + 16 * kSub;
-    const uint32_t bar_s = bar_q + 8;
-    const uint32_t bar_p = bar_q + 16;
-    const uint32_t bar_pv = bar_q + 24;
-    const uint32_t bar_drain = bar_q + 32;
+    const uint32_t bar_full = bars;                 // [9] sub-tile landed
+    const uint32_t bar_empty = bars + 8 * kSub;     // [9] sub-tile slot free
+    const uint32_t bar_q = bars + 16 * kSub;        // Q^T landed
+    const uint32_t bar_qe = bar_q + 8;              // Q^T no longer read (segment's last S^T done)
+    const uint32_t bar_s = bar_q + 16;              // S^T of a tile complete
+    const uint32_t bar_p = bar_q + 24;              // P^T of a tile written (128 arrivals)
+    const uint32_t bar_pv = bar_q + 32;             // P^T V of a tile complete
+    const uint32_t bar_of = bar_q + 40;             // O^T read out by the epilogue (128 arrivals)
+    const uint32_t bar_drain = bar_q + 48;
     float *red = reinterpret_cast<float *>(smem + L::red_off);
     float *fin = reinterpret_cast<float *>(smem + L::fin_off);
     float *m_sm = reinterpret_cast<float *>(smem + L::m_off);
@@ -383,13 +417,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     volatile int *need_sm = reinterpret_cast<volatile int *>(smem + L::misc_off + 8);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int item_idx = blockIdx.x / a.num_groups;
-    const int group = blockIdx.x % a.num_groups;
-    if (item_idx >= *a.item_count)
+    const int team = blockIdx.x / a.members;
+    const int member = blockIdx.x % a.members;
+    const int seg_begin = a.seg_member_indptr[member];
+    const int seg_end = a.seg_member_indptr[member + 1];
+    if (seg_begin >= seg_end)
         return;
-    const WorkItem it = a.items[item_idx];
-    const int row0 = group * NG;
-    const int n_tiles = (it.t1 - it.t0 + kTile - 1) / kTile;
+    const int seg_total = *a.seg_count;
+    const int row0 = team * NG;
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < kSub; ++k) {
@@ -397,9 +432,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             mbar_init(bar_empty + 8 * k, 1);
         }
         mbar_init(bar_q, 1);
+        mbar_init(bar_qe, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_p, 128);
         mbar_init(bar_pv, 1);
+        mbar_init(bar_of, 128);
         mbar_init(bar_drain, 1);
         *abort_flag = 0;
         *need_sm = 0;
@@ -419,55 +456,76 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && n_tiles > 0) {
-            int last_tile = -1, last_k = kSub - 1;
-            const int qrow = it.req * a.rows_per_req + row0;
-            mbar_arrive_expect_tx(bar_q, kSub * L::q_chunk);
-            for (int k = 0; k < kSub - 1; ++k)
-                tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 64 * k, qrow, bar_q);
-            tma_load_2d(s_q + (kSub - 1) * L::q_chunk, &tm_qr, 0, qrow, bar_q);
-            const int32_t *trow = a.page_table + (int64_t)it.req * a.table_ld;
-            for (int i = 0; i < n_tiles; ++i) {
-                const int t = it.t0 + i * kTile;
-                const int page = trow[t / kPageTokens];
-                const int tok = t % kPageTokens;
-                bool ok = true;
-                for (int k = 0; k < kSub; ++k) {
-                    if (!wait_bounded(bar_empty + 8 * k, (i & 1) ^ 1, abort_flag, a.status, 1)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(bar_full + 8 * k, kSubBytes);
-                    tma_load_3d(s_kv + k * kSubBytes, &tm_kv, 64 * k, tok, page, bar_full + 8 * k);
-                    last_tile = i;
-                    last_k = k;
-                }
-                if (!ok)
+        if (lane == 0) {
+            int gt = 0;                              // tiles issued so far (all segments)
+            int li_gt = -1, li_k = kSub - 1;         // last issued (tile, sub-tile)
+            int q_loads = 0;
+            bool ok = true;
+            for (int s = seg_begin; s < seg_end && ok; ++s) {
+                const int local = s - seg_begin;
+                const int4 seg = a.segments[s];
+                if (local > 0 &&
+                    !wait_bounded(bar_qe, (local - 1) & 1, abort_flag, a.status, 1)) {
+                    ok = false;
                     break;
+                }
+                const int qrow = seg.x * a.rows_per_req + row0;
+                mbar_arrive_expect_tx(bar_q, kSub * L::q_chunk);
+                for (int k = 0; k < kSub - 1; ++k)
+                    tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 64 * k, qrow, bar_q);
+                tma_load_2d(s_q + (kSub - 1) * L::q_chunk, &tm_qr, 0, qrow, bar_q);
+                ++q_loads;
+                const int32_t *trow = a.page_table + (int64_t)seg.x * a.table_ld;
+                const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
+                for (int i = 0; i < n_tiles && ok; ++i, ++gt) {
+                    const int t = seg.y + i * kTile;
+                    const int page = trow[t / kPageTokens];
+                    const int tok = t % kPageTokens;
+                    for (int k = 0; k < kSub; ++k) {
+                        if (!wait_bounded(bar_empty + 8 * k, (gt & 1) ^ 1, abort_flag, a.status,
+                                          2)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(bar_full + 8 * k, kSubBytes);
+                        tma_load_3d(s_kv + k * kSubBytes, &tm_kv, 64 * k, tok, page,
+                                    bar_full + 8 * k);
+                        li_gt = gt;
+                        li_k = k;
+                    }
+                }
             }
             // every issued copy must land before the CTA can exit
-            wait_drain(bar_q, 0);
+            if (q_loads > 0)
+                wait_drain(bar_q, (q_loads - 1) & 1);
             for (int k = 0; k < kSub; ++k) {
-                const int tile_k = k <= last_k ? last_tile : last_tile - 1;
+                const int tile_k = k <= li_k ? li_gt : li_gt - 1;
                 if (tile_k >= 0)
                     wait_drain(bar_full + 8 * k, tile_k & 1);
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0 && n_tiles > 0) {
-            bool issued = false;
+        if (lane == 0) {
+            bool issued = false, ok = true;
             constexpr uint32_t idesc_s = idesc_bf16(128, NG, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, NG, true, true);
             constexpr uint32_t p_layout = NG == 64 ? kSw128 : (NG == 32 ? kSw64 : kSw32);
             const uint32_t s_p = s_kv + (kSub - 1) * kSubBytes;  // P^T lives in the rope slot
-            if (wait_bounded(bar_q, 0, abort_flag, a.status, 2)) {
-                for (int i = 0; i < n_tiles; ++i) {
-                    const uint32_t par = i & 1;
-                    bool ok = true;
+            int gt = 0;
+            for (int s = seg_begin; s < seg_end && ok; ++s) {
+                const int local = s - seg_begin;
+                const int4 seg = a.segments[s];
+                const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
+                if (!wait_bounded(bar_q, local & 1, abort_flag, a.status, 3)) {
+                    ok = false;
+                    break;
+                }
+                for (int i = 0; i < n_tiles; ++i, ++gt) {
+                    const uint32_t par = gt & 1;
                     // S^T = K_tile . Q^T over the 576 columns
                     for (int k = 0; k < kSub && ok; ++k) {
-                        if (!wait_bounded(bar_full + 8 * k, par, abort_flag, a.status, 3)) {
+                        if (!wait_bounded(bar_full + 8 * k, par, abort_flag, a.status, 4)) {
                             ok = false;
                             break;
                         }
@@ -483,9 +541,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     if (!ok)
                         break;
                     mma_commit(bar_s);
-                    // O^T += V^T . P^T, four 128-row latent blocks over the 128 tokens
-                    if (!wait_bounded(bar_p, par, abort_flag, a.status, 4))
+                    if (i == n_tiles - 1)
+                        mma_commit(bar_qe);
+                    if (i == 0 && local > 0 &&
+                        !wait_bounded(bar_of, (local - 1) & 1, abort_flag, a.status, 5)) {
+                        ok = false;
                         break;
+                    }
+                    // O^T += V^T . P^T, four 128-row latent blocks over the 128 tokens
+                    if (!wait_bounded(bar_p, par, abort_flag, a.status, 6)) {
+                        ok = false;
+                        break;
+                    }
                     tc_fence_after();
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -512,160 +579,201 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         // ------------------------------------------------------------- softmax
         const int q = warp & 3;                 // TMEM lane quadrant of this warp
         const int tok = 32 * q + lane;          // token lane of S^T / latent row of O^T
+        const int st = threadIdx.x - 64;        // 0..127
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
-        const int Lr = a.seq_lens[it.req];
-        const int vis_all = Lr - (a.n_q - 1);   // tokens below this are visible to every row
         const uint32_t s_p = s_kv + (kSub - 1) * kSubBytes;
-        float lsum[NG];
-#pragma unroll
-        for (int c = 0; c < NG; ++c)
-            lsum[c] = 0.f;
-        for (int c = threadIdx.x - 64; c < NG; c += 128)
-            m_sm[c] = -INFINITY;
-        softmax_bar();
-
-        bool ok = n_tiles > 0;
-        for (int i = 0; i < n_tiles; ++i) {
-            const uint32_t par = i & 1;
-            const int t_base = it.t0 + i * kTile;
-            const int t = t_base + tok;
-            const bool tile_visible = t_base + kTile <= vis_all;
-            // warp-uniform, because tcgen05.ld below is a .sync.aligned instruction
-            const bool got = __all_sync(0xffffffffu, wait_bounded(bar_s, par, abort_flag, a.status, 5));
-            float x[NG];
-            if (got) {
-                tc_fence_after();
-                load_scores<NG>(tmem + t_lane + kTmemS, a.scale_log2, tile_visible, t, it.t1,
-                                vis_all, row0, a.num_heads, x);
-                // column maxima over the tile's 128 tokens (x is consumed)
-                warp_reduce_scatter<NG, true>(x, lane);
-                scatter_to_red<NG>(x, red + 64 * q, lane);
-            }
-            if (softmax_bar_or(!got || *abort_flag)) {
-                ok = false;
-                break;
-            }
-            if (q == 0) {
-                bool any = false;
-                for (int c = lane; c < NG; c += 32) {
-                    const float mt = fmaxf(fmaxf(red[c], red[64 + c]), fmaxf(red[128 + c], red[192 + c]));
-                    const float mu = m_sm[c];
-                    float alpha = 1.f;
-                    if (mt > mu + kTau) {
-                        alpha = fast_exp2(mu - mt);   // 0 when mu = -inf
-                        m_sm[c] = mt;
-                        any = true;
-                    }
-                    al_sm[c] = alpha;
-                }
-                any = __any_sync(0xffffffffu, any);
-                if (lane == 0)
-                    *need_sm = any ? 1 : 0;
-            }
+        const uint32_t m_addr = smem_u32(m_sm);
+        bool ok = true;
+        int gt = 0;
+        for (int s = seg_begin; s < seg_end && ok; ++s) {
+            const int local = s - seg_begin;
+            const int4 seg = a.segments[s];
+            const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
+            const int Lr = a.seq_lens[seg.x];
+            const int vis_all = Lr - (a.n_q - 1);   // tokens below this are visible to every row
+            if (local > 0)
+                softmax_bar();                       // previous epilogue is done with m_sm
+            for (int c = st; c < NG; c += 128)
+                m_sm[c] = -INFINITY;
             softmax_bar();
-            if (*need_sm != 0) {
+            float lsum[NG];
 #pragma unroll
-                for (int c = 0; c < NG; ++c)
-                    lsum[c] *= al_sm[c];
-                if (i > 0) {
-                    // O^T columns are rescaled once the previous tile's P^T V is done
-                    const bool done = wait_bounded(bar_pv, (i - 1) & 1, abort_flag, a.status, 6);
-                    if (softmax_bar_or(!done)) {
+            for (int c = 0; c < NG; ++c)
+                lsum[c] = 0.f;
+
+            for (int i = 0; i < n_tiles; ++i, ++gt) {
+                const uint32_t par = gt & 1;
+                const int t_base = seg.y + i * kTile;
+                const int t = t_base + tok;
+                const bool tile_visible = t_base + kTile <= vis_all;
+                // warp-uniform, because tcgen05.ld below is a .sync.aligned instruction
+                const bool got =
+                    __all_sync(0xffffffffu, wait_bounded(bar_s, par, abort_flag, a.status, 7));
+                float x[NG];
+                bool exceed = false;
+                if (got) {
+                    tc_fence_after();
+                    load_scores<NG>(tmem + t_lane + kTmemS, a.scale_log2, tile_visible, t, seg.z,
+                                    vis_all, row0, a.num_heads, x);
+                    exceed = shift_and_test<NG>(x, m_addr);
+                }
+                if (softmax_bar_or(exceed || !got || *abort_flag)) {
+                    // rare: a score exceeds its reference maximum (always on a segment's
+                    // first tile), or a wait gave up
+                    if (softmax_bar_or(!got || *abort_flag)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    warp_reduce_scatter<NG, true>(x, lane);
+                    scatter_to_red<NG>(x, red + 64 * q, lane);
+                    softmax_bar();
+                    if (q == 0) {
+                        bool any = false;
+                        for (int c = lane; c < NG; c += 32) {
+                            const float mu = m_sm[c];
+                            // the scores were shifted by mu (0 while unset): back to absolute
+                            const float mx = fmaxf(fmaxf(red[c], red[64 + c]),
+                                                   fmaxf(red[128 + c], red[192 + c])) +
+                                             (mu == -INFINITY ? 0.f : mu);
+                            float alpha = 1.f;
+                            if (mx != -INFINITY) {
+                                if (mu == -INFINITY) {
+                                    m_sm[c] = mx;       // first visible token of this row
+                                    alpha = 0.f;
+                                } else if (mx - mu > kTau) {
+                                    m_sm[c] = mx;
+                                    alpha = fast_exp2(mu - mx);
+                                }
+                            }
+                            al_sm[c] = alpha;
+                            any |= alpha != 1.f;
+                        }
+                        any = __any_sync(0xffffffffu, any);
+                        if (lane == 0)
+                            *need_sm = any ? 1 : 0;
+                    }
+                    softmax_bar();
+                    if (*need_sm != 0) {
+                        const uint32_t al_addr = smem_u32(al_sm);
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                        for (int c = 0; c < NG; ++c)
+                            lsum[c] *= ld_shared_f32(al_addr + 4 * c);
+                        if (i > 0) {
+                            // O^T columns are rescaled once the previous P^T V is done
+                            const bool done = wait_bounded(bar_pv, (gt - 1) & 1, abort_flag,
+                                                           a.status, 8);
+                            if (softmax_bar_or(!done)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
 #pragma unroll
-                        for (int b = 0; b < NG / 16; ++b) {
-                            uint32_t r[16];
-                            const uint32_t ta = tmem + t_lane + 64 * j + 16 * b;
-                            tmem_ld16(ta, r);
-                            tmem_wait_ld();
+                            for (int j = 0; j < 4; ++j) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                r[e] = __float_as_uint(__uint_as_float(r[e]) * al_sm[16 * b + e]);
-                            tmem_st16(ta, r);
+                                for (int b = 0; b < NG / 16; ++b) {
+                                    uint32_t r[16];
+                                    const uint32_t ta = tmem + t_lane + 64 * j + 16 * b;
+                                    tmem_ld16(ta, r);
+                                    tmem_wait_ld();
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e)
+                                        r[e] = __float_as_uint(
+                                            __uint_as_float(r[e]) *
+                                            ld_shared_f32(al_addr + 4 * (16 * b + e)));
+                                    tmem_st16(ta, r);
+                                }
+                            }
+                            tmem_wait_st();
                         }
                     }
-                    tmem_wait_st();
+                    load_scores<NG>(tmem + t_lane + kTmemS, a.scale_log2, tile_visible, t, seg.z,
+                                    vis_all, row0, a.num_heads, x);
+                    shift_and_test<NG>(x, m_addr);
                 }
-            }
-            // probabilities, running sums, and this token's P^T row (bf16, swizzled)
-            load_scores<NG>(tmem + t_lane + kTmemS, a.scale_log2, tile_visible, t, it.t1, vis_all,
-                            row0, a.num_heads, x);
-            {
-                constexpr int row_bytes = 2 * NG;
-                constexpr int swz_bits = NG == 64 ? 3 : (NG == 32 ? 2 : 1);
+                // probabilities 2^(x - m) (x is already shifted), running sums, and
+                // this token's P^T row (bf16, swizzled)
+                {
+                    constexpr int row_bytes = 2 * NG;
+                    constexpr int swz_bits = NG == 64 ? 3 : (NG == 32 ? 2 : 1);
 #pragma unroll
-                for (int ch = 0; ch < row_bytes / 16; ++ch) {
-                    uint32_t w4[4];
+                    for (int ch = 0; ch < row_bytes / 16; ++ch) {
+                        uint32_t w4[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = 8 * ch + 2 * e;
-                        const float p0 = x[c] == -INFINITY ? 0.f : fast_exp2(x[c] - m_sm[c]);
-                        const float p1 =
-                            x[c + 1] == -INFINITY ? 0.f : fast_exp2(x[c + 1] - m_sm[c + 1]);
-                        lsum[c] += p0;
-                        lsum[c + 1] += p1;
-                        w4[e] = pack_bf16x2(p0, p1);
+                        for (int e = 0; e < 4; ++e) {
+                            const int c = 8 * ch + 2 * e;
+                            const float p0 = fast_exp2(x[c]);       // 2^-inf = 0
+                            const float p1 = fast_exp2(x[c + 1]);
+                            lsum[c] += p0;
+                            lsum[c + 1] += p1;
+                            w4[e] = pack_bf16x2(p0, p1);
+                        }
+                        const uint32_t off = (uint32_t)(tok * row_bytes + 16 * ch);
+                        const uint32_t sw = off ^ (((off >> 7) & ((1u << swz_bits) - 1u)) << 4);
+                        st_shared_v4(s_p + sw, w4[0], w4[1], w4[2], w4[3]);
                     }
-                    const uint32_t off = (uint32_t)(tok * row_bytes + 16 * ch);
-                    const uint32_t sw = off ^ (((off >> 7) & ((1u << swz_bits) - 1u)) << 4);
-                    st_shared_v4(s_p + sw, w4[0], w4[1], w4[2], w4[3]);
                 }
-            }
-            if (t >= it.t1) {
-                // past the request's history: zero this token's latent row so
-                // that P = 0 never meets a stale (possibly NaN) value in the MMA
+                if (t >= seg.z) {
+                    // past the request's history: zero this token's latent row so
+                    // that P = 0 never meets a stale (possibly NaN) value in the MMA
 #pragma unroll
-                for (int k = 0; k < kSub - 1; ++k)
+                    for (int k = 0; k < kSub - 1; ++k)
 #pragma unroll
-                    for (int ch = 0; ch < 8; ++ch)
-                        st_shared_v4(s_kv + k * kSubBytes + tok * 128 + 16 * ch, 0u, 0u, 0u, 0u);
+                        for (int ch = 0; ch < 8; ++ch)
+                            st_shared_v4(s_kv + k * kSubBytes + tok * 128 + 16 * ch, 0u, 0u, 0u,
+                                         0u);
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                mbar_arrive(bar_p);
             }
-            fence_proxy_async();
-            tc_fence_before();
-            mbar_arrive(bar_p);
-        }
+            if (!ok)
+                break;
 
-        if (ok) {
-            const bool done = wait_bounded(bar_pv, (n_tiles - 1) & 1, abort_flag, a.status, 7);
-            ok = !softmax_bar_or(!done);
-        }
-        if (ok) {
+            // ---- segment epilogue: normalised partial state of the segment
+            const bool done = wait_bounded(bar_pv, (gt - 1) & 1, abort_flag, a.status, 9);
+            if (softmax_bar_or(!done)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
-            // row sums over the 128 token lanes
             warp_reduce_scatter<NG, false>(lsum, lane);
             scatter_to_red<NG>(lsum, red + 64 * q, lane);
             softmax_bar();
-            if (q == 0)
-                for (int c = lane; c < NG; c += 32)
-                    fin[c] = red[c] + red[64 + c] + red[128 + c] + red[192 + c];
+            if (q == 0) {
+                for (int c = lane; c < NG; c += 32) {
+                    const float l = red[c] + red[64 + c] + red[128 + c] + red[192 + c];
+                    fin[c] = l > 0.f ? 1.f / l : 0.f;   // 1 / row sum (0 for an empty row)
+                    a.lse_part[(int64_t)(team * seg_total + s) * NG + c] =
+                        l > 0.f ? (m_sm[c] + log2f(l)) * kLn2 : -INFINITY;
+                }
+            }
             softmax_bar();
-            // normalised partial output: thread = latent row of each O^T block
-            const int64_t out_row0 = (int64_t)it.split * a.rows_per_req + row0;
+            // normalised partial output: thread = latent row of each O^T block;
+            // for a fixed row the 128 threads store 512 contiguous bytes
+            const uint32_t inv_addr = smem_u32(fin);
+            float *out0 = a.o_part + (int64_t)(team * seg_total + s) * NG * kLatent + tok;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int b = 0; b < NG / 16; ++b) {
+                float inv[16];
 #pragma unroll
-                for (int b = 0; b < NG / 16; ++b) {
+                for (int e4 = 0; e4 < 16; e4 += 4)
+                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(inv[e4]), "=f"(inv[e4 + 1]), "=f"(inv[e4 + 2]),
+                                   "=f"(inv[e4 + 3])
+                                 : "r"(inv_addr + 4 * (16 * b + e4)));
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
                     uint32_t r[16];
                     tmem_ld16(tmem + t_lane + 64 * j + 16 * b, r);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int c = 16 * b + e;
-                        const float l = fin[c];
-                        const float o = l > 0.f ? __uint_as_float(r[e]) / l : 0.f;
-                        a.o_part[(out_row0 + c) * kLatent + 128 * j + tok] = o;
-                    }
+                    for (int e = 0; e < 16; ++e)
+                        out0[(int64_t)(16 * b + e) * kLatent + 128 * j] =
+                            __uint_as_float(r[e]) * inv[e];
                 }
             }
-            for (int c = threadIdx.x - 64; c < NG; c += 128) {
-                const float l = fin[c];
-                a.lse_part[out_row0 + c] = l > 0.f ? (m_sm[c] + log2f(l)) * kLn2 : -INFINITY;
-            }
+            tc_fence_before();
+            mbar_arrive(bar_of);
         }
     }
 
@@ -715,7 +823,7 @@ bool make_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *di
 }
 
 template <int NG>
-cudaError_t launch_ng(const DecodeArgs &a, int max_items, cudaStream_t stream)
+cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
 {
     CUtensorMap tm_kv, tm_qn, tm_qr;
     const cuuint64_t kv_dims[3] = {(cuuint64_t)kRow, (cuuint64_t)kPageTokens,
@@ -738,19 +846,19 @@ cudaError_t launch_ng(const DecodeArgs &a, int max_items, cudaStream_t stream)
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess)
         return err;
-    const unsigned grid = (unsigned)max_items * (unsigned)a.num_groups;
+    const unsigned grid = (unsigned)a.members * (unsigned)a.num_groups;
     decode_tc_kernel<NG><<<grid, kThreads, smem, stream>>>(tm_kv, tm_qn, tm_qr, a);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode_tc(const DecodeArgs &args, int max_items, cudaStream_t stream)
+cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream)
 {
     switch (args.group_rows) {
-    case 64: return launch_ng<64>(args, max_items, stream);
-    case 32: return launch_ng<32>(args, max_items, stream);
-    case 16: return launch_ng<16>(args, max_items, stream);
+    case 64: return launch_ng<64>(args, stream);
+    case 32: return launch_ng<32>(args, stream);
+    case 16: return launch_ng<16>(args, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -15,23 +15,18 @@ constexpr int kPageTokens = 1536; // token rows per MLA page
 constexpr int kTile = 128;        // KV tokens per decode tile; chunks are multiples of it
 constexpr int kMaxReqs = 1024;
 constexpr int kMaxNq = 16;
-
-// One unit of decode work: KV tokens [t0, t1) of request `req`, whose partial
-// softmax state is stored at split id `split` (the request's splits are
-// consecutive ids starting at split_indptr[req]).
-struct __align__(16) WorkItem {
-    int32_t req;
-    int32_t split;
-    int32_t t0;
-    int32_t t1;
-};
+constexpr int kMaxPlanSplits = 4096;  // chunks the device planner can schedule
+constexpr int kChunksPerMember = 16;  // default chunk budget per persistent CTA
 
 struct PlanBuffers {
-    int32_t *status;   // [1] device status word, reset to 0 by the plan kernel
-    int32_t *indptr;   // [R + 1]
-    int64_t *chunk;    // [1]
-    int32_t *count;    // [1] number of work items
-    WorkItem *items;   // [max_items], longest request first
+    int32_t *status;            // [1] device status word, reset to 0 by the plan kernel
+    int32_t *indptr;            // [R + 1] per-request chunk counts, prefix-summed
+    int64_t *chunk;             // [1] chunk length in tokens
+    // persistent schedule (all null when only the split plan is wanted)
+    int32_t *seg_count;         // [1] number of segments S
+    int4 *segments;             // [S] (request, t0, t1, member)
+    int32_t *seg_req_indptr;    // [R + 1] segments of request r: [r], [r + 1]
+    int32_t *seg_member_indptr; // [members + 1] segments of member k: [k], [k + 1]
 };
 
 struct DecodeArgs {
@@ -46,12 +41,14 @@ struct DecodeArgs {
     int32_t num_reqs, n_q, num_heads;
     int32_t rows_per_req;          // n_q * H
     int32_t group_rows;            // rows owned by one CTA: 16, 32 or 64
-    int32_t num_groups;            // rows_per_req / group_rows
+    int32_t num_groups;            // rows_per_req / group_rows (teams)
+    int32_t members;               // CTAs per team
     float scale_log2;              // softmax scale * log2(e)
-    const WorkItem *items;
-    const int32_t *item_count;
-    float *o_part;                 // [splits, rows_per_req, 512]
-    float *lse_part;               // [splits, rows_per_req], natural log
+    const int4 *segments;
+    const int32_t *seg_member_indptr;
+    const int32_t *seg_count;
+    float *o_part;                 // [groups * S, group_rows, 512]
+    float *lse_part;               // [groups * S, group_rows], natural log
     int32_t *status;               // device status word (0 = ok, else the failed wait)
 };
 
@@ -64,10 +61,16 @@ inline int group_rows_for(int rows)
     return 0;
 }
 
-cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, PlanBuffers plan,
-                        cudaStream_t stream);
-cudaError_t launch_decode_tc(const DecodeArgs &args, int max_items, cudaStream_t stream);
+size_t plan_smem_bytes();
+cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int members,
+                        PlanBuffers plan, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream);
+// Merge of chunk partials + sigmoid gate.  Row rw of request r (rw = j*H + h)
+// lives in group g = rw / group_rows at row rw % group_rows of the partials
+// of segments [g*stride + indptr[r], g*stride + indptr[r + 1]), where stride is
+// *seg_stride (or 0 when seg_stride is null).
 cudaError_t launch_combine(const float *o_part, const float *lse_part, const int32_t *indptr,
+                           const int32_t *seg_stride, int group_rows,
                            const __nv_bfloat16 *gate, int num_reqs, int n_q, int num_heads,
                            __nv_bfloat16 *out, float *lse, cudaStream_t stream);
 

@@ -1,25 +1,35 @@
-// plmla_plan.cu -- device-side per-request KV split planner.
+// plmla_plan.cu -- device-side KV split planner and the persistent-CTA schedule.
 //
-// TokenSpeed AgentX post, section "Balance MLA work with per-request KV
-// splitting" (Figure 4): a target chunk length follows from the batch's total
-// history and the parallelism budget, and each request gets as many chunks as
-// its own history needs.  The plan is computed on the device from seq_lens, so a
-// decode step never waits for the host and a captured CUDA graph stays valid
-// as histories grow (AgentX - InferenceXv3 report, SGLang section: runtime
-// lengths, no per-step device-to-host length sync).
+// Split plan (TokenSpeed AgentX post, section "Balance MLA work with per-request
+// KV splitting", Figure 4): a target chunk length follows from the batch's total
+// history and a parallelism budget, and each request gets as many chunks as its
+// own history needs.  chunk = ceil(sum L / budget) rounded up to kTile; if the
+// chunks do not fit the budget, chunk grows (the smallest multiple of kTile
+// that fits, found by binary search because the chunk count only falls as the
+// chunk grows), never beyond the longest history rounded up to kTile.
 //
-// chunk = ceil(sum L / budget) rounded up to kTile; if the chunks do not fit the
-// budget, chunk grows (smallest multiple of kTile that fits, found by binary
-// search because the chunk count only falls as the chunk grows), but never
-// beyond the longest history rounded up to kTile.  Work items are emitted
-// longest request first, so the block scheduler starts the longest chunks first.
+// Schedule (the GB300 side): the decode kernel runs one persistent CTA per SM.
+// The chunks, in request order, are dealt out as contiguous runs so that every
+// CTA ("member") gets the same cost up to half a chunk, cost counted in
+// 128-token tiles plus a fixed charge for each request's first chunk (starting
+// a segment): chunk i goes to member floor((cost before i + cost of i / 2) *
+// members / total cost).  Consecutive chunks of one request that land on one member form
+// a segment, which the CTA processes without writing an intermediate partial
+// state.  Every row group of the queries repeats the same schedule on its own
+// team of members, so teams read the same KV tiles at about the same time.
+//
+// Everything is computed on the device from seq_lens, so a decode step never
+// waits for the host and a captured CUDA graph stays valid as histories grow
+// (AgentX - InferenceXv3 report, SGLang section: runtime lengths, no per-step
+// device-to-host length sync).
 #include "plmla_internal.cuh"
 
 namespace plmla {
 namespace {
 
 constexpr int kPlanThreads = 1024;
-constexpr int kPerThread = kMaxReqs / kPlanThreads;  // elements per thread in scans
+constexpr int kSegmentCostTiles = 2;
+constexpr int kScanPerThread = kMaxPlanSplits / kPlanThreads;
 
 __device__ __forceinline__ long long ceil_div_ll(long long a, long long b)
 {
@@ -59,24 +69,23 @@ __device__ int block_max_int(int v, int *red)
     return m;
 }
 
-// Exclusive prefix sum of vals[0..n) in place (n <= kMaxReqs); returns the total.
+// Exclusive prefix sum of vals[0..n) in place (n <= kMaxPlanSplits); returns the total.
 __device__ int block_exclusive_scan(int *vals, int n, int *red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int base = threadIdx.x * kPerThread;
-    int local[kPerThread];
+    const int base = threadIdx.x * kScanPerThread;
+    int local[kScanPerThread];
     int run = 0;
 #pragma unroll
-    for (int i = 0; i < kPerThread; ++i) {
-        int v = (base + i < n) ? vals[base + i] : 0;
+    for (int i = 0; i < kScanPerThread; ++i) {
+        const int v = (base + i < n) ? vals[base + i] : 0;
         local[i] = run;
         run += v;
     }
-    // inclusive warp scan of the per-thread totals
     int incl = run;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        int up = __shfl_up_sync(0xffffffffu, incl, o);
+        const int up = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o)
             incl += up;
     }
@@ -92,35 +101,46 @@ __device__ int block_exclusive_scan(int *vals, int n, int *red)
     }
     const int thread_off = warp_off + incl - run;
 #pragma unroll
-    for (int i = 0; i < kPerThread; ++i)
+    for (int i = 0; i < kScanPerThread; ++i)
         if (base + i < n)
             vals[base + i] = thread_off + local[i];
     __syncthreads();
     return total;
 }
 
-__global__ void __launch_bounds__(kPlanThreads, 1)
-plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, PlanBuffers plan)
-{
-    __shared__ int lens[kMaxReqs];
-    __shared__ int splits[kMaxReqs];   // split count, then split id base (request order)
-    __shared__ int ranked[kMaxReqs];   // split count in rank order, then item base
-    __shared__ int rank_of[kMaxReqs];
-    __shared__ long long red64[kPlanThreads / 32];
-    __shared__ int red32[kPlanThreads / 32];
+struct PlanSmem {
+    int lens[kMaxReqs];
+    int split_base[kMaxReqs];
+    int sp_req[kMaxPlanSplits];
+    int sp_t0[kMaxPlanSplits];
+    int sp_t1[kMaxPlanSplits];
+    int sp_tiles[kMaxPlanSplits];   // tiles of each chunk, then their exclusive prefix
+    int sp_member[kMaxPlanSplits];
+    int sp_seg[kMaxPlanSplits];     // segment-start flag, then the segment id
+    long long red64[kPlanThreads / 32];
+    int red32[kPlanThreads / 32];
+};
 
+__global__ void __launch_bounds__(kPlanThreads, 1)
+plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int members,
+            PlanBuffers plan)
+{
+    extern __shared__ __align__(16) unsigned char plan_smem_raw[];
+    PlanSmem &sm = *reinterpret_cast<PlanSmem *>(plan_smem_raw);
     const int tid = threadIdx.x;
+
+    // ---- split plan (per request)
     long long local_sum = 0;
     int local_max = 0;
     for (int r = tid; r < num_reqs; r += kPlanThreads) {
-        int L = max(0, seq_lens[r]);
-        lens[r] = L;
+        const int L = max(0, seq_lens[r]);
+        sm.lens[r] = L;
         local_sum += L;
         local_max = max(local_max, L);
     }
     __syncthreads();
-    const long long total = block_sum<long long>(local_sum, red64);
-    const int longest_len = block_max_int(local_max, red32);
+    const long long total = block_sum<long long>(local_sum, sm.red64);
+    const int longest_len = block_max_int(local_max, sm.red32);
 
     long long chunk = kTile;
     if (total > 0) {
@@ -128,15 +148,14 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, Plan
         const long long longest = ceil_div_ll(longest_len, kTile) * kTile;
         chunk = c0;
         if (c0 < longest) {
-            // smallest k in [0, K] with count(c0 + k*kTile) <= budget, else K
             long long lo = 0, hi = (longest - c0) / kTile;
             while (lo < hi) {
                 const long long mid = (lo + hi) / 2;
                 const long long c = c0 + mid * kTile;
                 long long cnt = 0;
                 for (int r = tid; r < num_reqs; r += kPlanThreads)
-                    cnt += ceil_div_ll(lens[r], c);
-                cnt = block_sum<long long>(cnt, red64);
+                    cnt += ceil_div_ll(sm.lens[r], c);
+                cnt = block_sum<long long>(cnt, sm.red64);
                 if (cnt <= budget)
                     hi = mid;
                 else
@@ -145,55 +164,104 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, Plan
             chunk = c0 + lo * kTile;
         }
     }
-
-    for (int r = tid; r < num_reqs; r += kPlanThreads) {
-        const int L = lens[r];
-        splits[r] = (int)ceil_div_ll(L, chunk);
-        // rank: longer histories first, ties by request index
-        int rank = 0;
-        for (int q = 0; q < num_reqs; ++q) {
-            const int Lq = lens[q];
-            rank += (Lq > L) || (Lq == L && q < r);
-        }
-        rank_of[r] = rank;
-    }
-    __syncthreads();
     for (int r = tid; r < num_reqs; r += kPlanThreads)
-        ranked[rank_of[r]] = splits[r];
+        sm.split_base[r] = (int)ceil_div_ll(sm.lens[r], chunk);
     __syncthreads();
-    const int n_items = block_exclusive_scan(ranked, num_reqs, red32);
-    const int n_splits = block_exclusive_scan(splits, num_reqs, red32);
-
-    for (int r = tid; r < num_reqs; r += kPlanThreads) {
-        plan.indptr[r] = splits[r];
-        const int L = lens[r];
-        const int n = (int)ceil_div_ll(L, chunk);
-        const int item0 = ranked[rank_of[r]];
-        for (int s = 0; s < n && plan.items != nullptr; ++s) {
-            WorkItem it;
-            it.req = r;
-            it.split = splits[r] + s;
-            it.t0 = (int)(s * chunk);
-            it.t1 = (int)min((long long)L, (s + 1) * chunk);
-            plan.items[item0 + s] = it;
-        }
-    }
+    const int n_splits = block_exclusive_scan(sm.split_base, num_reqs, sm.red32);
+    for (int r = tid; r < num_reqs; r += kPlanThreads)
+        plan.indptr[r] = sm.split_base[r];
     if (tid == 0) {
         if (plan.status != nullptr)
             *plan.status = 0;
         plan.indptr[num_reqs] = n_splits;
         *plan.chunk = chunk;
-        if (plan.count != nullptr)
-            *plan.count = n_items;
+    }
+    if (plan.segments == nullptr)
+        return;
+    if (n_splits > kMaxPlanSplits) {   // excluded by the host-side budget limit
+        if (tid == 0 && plan.status != nullptr)
+            *plan.status = 8;
+        return;
+    }
+
+    // ---- schedule: chunks in request order, dealt to members by tile count
+    for (int r = tid; r < num_reqs; r += kPlanThreads) {
+        const int L = sm.lens[r];
+        const int n = (int)ceil_div_ll(L, chunk);
+        for (int s = 0; s < n; ++s) {
+            const int i = sm.split_base[r] + s;
+            const int t0 = (int)(s * chunk);
+            const int t1 = (int)min((long long)L, (s + 1) * chunk);
+            sm.sp_req[i] = r;
+            sm.sp_t0[i] = t0;
+            sm.sp_t1[i] = t1;
+            // cost in tiles; a request's first chunk also carries the cost of
+            // starting a segment (query load, first-tile softmax, epilogue)
+            sm.sp_tiles[i] = (t1 - t0 + kTile - 1) / kTile + (s == 0 ? kSegmentCostTiles : 0);
+            sm.sp_member[i] = sm.sp_tiles[i];   // keep the cost for the midpoint
+        }
+    }
+    __syncthreads();
+    const int total_tiles = block_exclusive_scan(sm.sp_tiles, n_splits, sm.red32);
+    for (int i = tid; i < n_splits; i += kPlanThreads) {
+        const long long mid2 = 2LL * sm.sp_tiles[i] + sm.sp_member[i];  // 2*prefix + tiles
+        const long long m = mid2 * members / (2LL * (long long)max(total_tiles, 1));
+        sm.sp_member[i] = (int)min((long long)members - 1, m);
+    }
+    __syncthreads();
+    for (int i = tid; i < n_splits; i += kPlanThreads)
+        sm.sp_seg[i] = (i == 0) || sm.sp_req[i] != sm.sp_req[i - 1] ||
+                       sm.sp_member[i] != sm.sp_member[i - 1];
+    __syncthreads();
+    const int n_segs = block_exclusive_scan(sm.sp_seg, n_splits, sm.red32);
+    for (int i = tid; i < n_splits; i += kPlanThreads) {
+        // sp_seg now holds the number of segment starts before chunk i, so a
+        // chunk that continues a segment belongs to segment sp_seg[i] - 1
+        const bool starts = (i == 0) || sm.sp_req[i] != sm.sp_req[i - 1] ||
+                            sm.sp_member[i] != sm.sp_member[i - 1];
+        const int seg = sm.sp_seg[i] - (starts ? 0 : 1);
+        const bool ends = (i == n_splits - 1) || sm.sp_req[i + 1] != sm.sp_req[i] ||
+                          sm.sp_member[i + 1] != sm.sp_member[i];
+        if (starts) {
+            plan.segments[seg].x = sm.sp_req[i];
+            plan.segments[seg].y = sm.sp_t0[i];
+            plan.segments[seg].w = sm.sp_member[i];
+            // members (previous chunk's member, this member] start at this segment
+            const int prev = (i == 0) ? -1 : sm.sp_member[i - 1];
+            for (int k = prev + 1; k <= sm.sp_member[i]; ++k)
+                plan.seg_member_indptr[k] = seg;
+        }
+        if (ends)
+            plan.segments[seg].z = sm.sp_t1[i];
+    }
+    // first segment of each request: the segment id of its first chunk (for a
+    // request without chunks, the id of the next request's first chunk)
+    for (int r = tid; r < num_reqs; r += kPlanThreads) {
+        const int i = sm.split_base[r];
+        plan.seg_req_indptr[r] = i < n_splits ? sm.sp_seg[i] : n_segs;
+    }
+    if (tid == 0) {
+        plan.seg_req_indptr[num_reqs] = n_segs;
+        const int last = n_splits > 0 ? sm.sp_member[n_splits - 1] : -1;
+        for (int k = last + 1; k <= members; ++k)
+            plan.seg_member_indptr[k] = n_segs;
+        *plan.seg_count = n_segs;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, PlanBuffers plan,
-                        cudaStream_t stream)
+size_t plan_smem_bytes() { return sizeof(PlanSmem); }
+
+cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int members,
+                        PlanBuffers plan, cudaStream_t stream)
 {
-    plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, num_reqs, budget, plan);
+    const int smem = (int)sizeof(PlanSmem);
+    cudaError_t err =
+        cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess)
+        return err;
+    plan_kernel<<<1, kPlanThreads, smem, stream>>>(seq_lens, num_reqs, budget, members, plan);
     return cudaGetLastError();
 }
 

@@ -35,20 +35,24 @@ def test_status_names(lib):
 def test_split_budget_matches_oracle_rule(lib, R, n_q, H, slots, min_splits):
     rows = n_q * H
     group = 64 if rows % 64 == 0 else 32 if rows % 32 == 0 else 16
-    expect = oracle.split_budget(R, rows // group, slots, min_splits)
+    try:
+        expect = oracle.split_budget(R, rows // group, slots, min_splits)
+    except ValueError:
+        expect = -1
     assert lib.mla_split_budget(R, n_q, H, slots, min_splits) == expect
 
 
-def test_workspace_grows_with_budget(lib):
+def test_workspace_grows_with_the_machine(lib):
     small = lib.mla_workspace_size(64, 1, 64, 152, 1)
     big = lib.mla_workspace_size(64, 1, 64, 304, 1)
     assert 0 < small < big
-    # 152 chunks x 64 rows x 512 fp32 partials dominate
-    assert small >= 152 * 64 * 512 * 4
+    # at most R + members segments of 64 rows x 512 fp32 partials
+    assert (64 + 152) * 64 * 512 * 4 <= small < (64 + 152) * 64 * 513 * 4 + (1 << 20)
 
 
 @pytest.mark.parametrize("args", [(0, 1, 64, 152, 1), (2, 0, 64, 152, 1), (2, 1, 24, 152, 1),
-                                  (2, 1, 64, -1, 1), (2, 1, 64, 152, 0), (2000, 1, 64, 152, 1)])
+                                  (2, 1, 64, -1, 1), (2, 1, 64, 152, 0), (2000, 1, 64, 152, 1),
+                                  (1024, 1, 64, 152, 8)])
 def test_bad_shapes_are_rejected_on_the_host(lib, args):
     assert lib.mla_split_budget(*args) == -1
     assert lib.mla_workspace_size(*args) == 0
