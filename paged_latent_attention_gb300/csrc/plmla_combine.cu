@@ -25,6 +25,9 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
                int group_rows, const __nv_bfloat16 *__restrict__ gate, int num_reqs, int n_q,
                int num_heads, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse)
 {
+    // launched as a programmatic dependent of the decode kernel: wait for its
+    // partial states (a no-op when launched on its own)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
@@ -98,10 +101,18 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, const int
 {
     const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
     const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
-    combine_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(o_part, lse_part, indptr,
-                                                              seg_stride, group_rows, gate,
-                                                              num_reqs, n_q, num_heads, out, lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, o_part, lse_part, indptr, seg_stride,
+                              group_rows, gate, num_reqs, n_q, num_heads, out, lse);
 }
 
 }  // namespace plmla

@@ -419,12 +419,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int team = blockIdx.x / a.members;
     const int member = blockIdx.x % a.members;
-    const int seg_begin = a.seg_member_indptr[member];
-    const int seg_end = a.seg_member_indptr[member + 1];
-    if (seg_begin >= seg_end)
-        return;
-    const int seg_total = *a.seg_count;
     const int row0 = team * NG;
+    if (threadIdx.x == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_kv)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_qn)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_qr)) : "memory");
+    }
 
     if (threadIdx.x == 0) {
         for (int k = 0; k < kSub; ++k) {
@@ -453,6 +453,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    // everything above overlaps the plan kernel (programmatic dependent launch);
+    // the schedule is read only once that grid has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int seg_begin = a.seg_member_indptr[member];
+    const int seg_end = a.seg_member_indptr[member + 1];   // empty range: no work
+    const int seg_total = *a.seg_count;
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -777,6 +784,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         }
     }
 
+    // the combine kernel may be scheduled as SMs free up; it waits for this
+    // grid's completion before reading the partial states
+    asm volatile("griddepcontrol.launch_dependents;");
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -846,9 +856,17 @@ cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess)
         return err;
-    const unsigned grid = (unsigned)a.members * (unsigned)a.num_groups;
-    decode_tc_kernel<NG><<<grid, kThreads, smem, stream>>>(tm_kv, tm_qn, tm_qr, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.members * (unsigned)a.num_groups);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NG>, tm_kv, tm_qn, tm_qr, a);
 }
 
 }  // namespace

@@ -5,7 +5,7 @@
 // history and a parallelism budget, and each request gets as many chunks as its
 // own history needs.  chunk = ceil(sum L / budget) rounded up to kTile; if the
 // chunks do not fit the budget, chunk grows (the smallest multiple of kTile
-// that fits, found by binary search because the chunk count only falls as the
+// that fits, found by a 32-way parallel search because the chunk count only falls as the
 // chunk grows), never beyond the longest history rounded up to kTile.
 //
 // Schedule (the GB300 side): the decode kernel runs one persistent CTA per SM.
@@ -119,6 +119,8 @@ struct PlanSmem {
     int sp_seg[kMaxPlanSplits];     // segment-start flag, then the segment id
     long long red64[kPlanThreads / 32];
     int red32[kPlanThreads / 32];
+    int cand_k[kPlanThreads / 32];
+    int cand_fits[kPlanThreads / 32];
 };
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
@@ -128,6 +130,9 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     extern __shared__ __align__(16) unsigned char plan_smem_raw[];
     PlanSmem &sm = *reinterpret_cast<PlanSmem *>(plan_smem_raw);
     const int tid = threadIdx.x;
+    // the decode kernel may start its prologue now; it waits for this grid's
+    // completion before reading the plan
+    asm volatile("griddepcontrol.launch_dependents;");
 
     // ---- split plan (per request)
     long long local_sum = 0;
@@ -148,20 +153,42 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
         const long long longest = ceil_div_ll(longest_len, kTile) * kTile;
         chunk = c0;
         if (c0 < longest) {
-            long long lo = 0, hi = (longest - c0) / kTile;
+            // smallest k in [0, K] with count(c0 + k*kTile) <= budget, else K;
+            // count only falls as the chunk grows, so each round splits [lo, hi]
+            // into 32 parts, one candidate per warp.  32-bit arithmetic only:
+            // histories and chunks are below 2^31, and a count is only compared
+            // with the budget, so it saturates at budget + 1.
+            int lo = 0, hi = (int)((longest - c0) / kTile);
+            const unsigned c0u = (unsigned)c0;
+            const int lane = tid & 31, warp = tid >> 5;
             while (lo < hi) {
-                const long long mid = (lo + hi) / 2;
-                const long long c = c0 + mid * kTile;
-                long long cnt = 0;
-                for (int r = tid; r < num_reqs; r += kPlanThreads)
-                    cnt += ceil_div_ll(sm.lens[r], c);
-                cnt = block_sum<long long>(cnt, sm.red64);
-                if (cnt <= budget)
-                    hi = mid;
-                else
-                    lo = mid + 1;
+                const int span = hi - lo;
+                const int k = lo + (int)(((long long)span * (warp + 1)) / 33);   // in [lo, hi)
+                const unsigned c = c0u + (unsigned)k * kTile;
+                int cnt = 0;
+                for (int r = lane; r < num_reqs; r += 32) {
+                    const unsigned L = (unsigned)sm.lens[r];
+                    cnt = min(cnt + (int)((L + c - 1u) / c), budget + 1);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    cnt = min(cnt + __shfl_xor_sync(0xffffffffu, cnt, o), budget + 1);
+                __syncthreads();
+                if (lane == 0) {
+                    sm.cand_k[warp] = k;
+                    sm.cand_fits[warp] = cnt <= budget;
+                }
+                __syncthreads();
+                // candidates ascend with the warp index: the first fitting one
+                // bounds hi, the one before it (failing) bounds lo
+                const unsigned fits = __ballot_sync(0xffffffffu, sm.cand_fits[lane] != 0);
+                const int first = fits ? __ffs(fits) - 1 : kPlanThreads / 32;
+                if (first < kPlanThreads / 32)
+                    hi = sm.cand_k[first];
+                if (first > 0)
+                    lo = max(lo, sm.cand_k[first - 1] + 1);
             }
-            chunk = c0 + lo * kTile;
+            chunk = c0 + (long long)lo * kTile;
         }
     }
     for (int r = tid; r < num_reqs; r += kPlanThreads)
@@ -184,29 +211,37 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
         return;
     }
 
-    // ---- schedule: chunks in request order, dealt to members by tile count
-    for (int r = tid; r < num_reqs; r += kPlanThreads) {
-        const int L = sm.lens[r];
-        const int n = (int)ceil_div_ll(L, chunk);
-        for (int s = 0; s < n; ++s) {
-            const int i = sm.split_base[r] + s;
-            const int t0 = (int)(s * chunk);
-            const int t1 = (int)min((long long)L, (s + 1) * chunk);
-            sm.sp_req[i] = r;
-            sm.sp_t0[i] = t0;
-            sm.sp_t1[i] = t1;
-            // cost in tiles; a request's first chunk also carries the cost of
-            // starting a segment (query load, first-tile softmax, epilogue)
-            sm.sp_tiles[i] = (t1 - t0 + kTile - 1) / kTile + (s == 0 ? kSegmentCostTiles : 0);
-            sm.sp_member[i] = sm.sp_tiles[i];   // keep the cost for the midpoint
+    // ---- schedule: chunks in request order, dealt to members by cost
+    for (int i = tid; i < n_splits; i += kPlanThreads) {
+        // request of chunk i: the last r with split_base[r] <= i
+        int lo = 0, hi = num_reqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sm.split_base[mid] <= i)
+                lo = mid;
+            else
+                hi = mid - 1;
         }
+        const int r = lo;
+        const int s = i - sm.split_base[r];
+        const int L = sm.lens[r];
+        const int t0 = (int)(s * chunk);
+        const int t1 = (int)min((long long)L, (s + 1) * chunk);
+        sm.sp_req[i] = r;
+        sm.sp_t0[i] = t0;
+        sm.sp_t1[i] = t1;
+        // cost in tiles; a request's first chunk also carries the cost of
+        // starting a segment (query load, first-tile softmax, epilogue)
+        sm.sp_tiles[i] = (t1 - t0 + kTile - 1) / kTile + (s == 0 ? kSegmentCostTiles : 0);
+        sm.sp_member[i] = sm.sp_tiles[i];   // keep the cost for the midpoint
     }
     __syncthreads();
     const int total_tiles = block_exclusive_scan(sm.sp_tiles, n_splits, sm.red32);
     for (int i = tid; i < n_splits; i += kPlanThreads) {
-        const long long mid2 = 2LL * sm.sp_tiles[i] + sm.sp_member[i];  // 2*prefix + tiles
-        const long long m = mid2 * members / (2LL * (long long)max(total_tiles, 1));
-        sm.sp_member[i] = (int)min((long long)members - 1, m);
+        // midpoint of chunk i in cost units, times members, over twice the total
+        const long long mid2 = 2LL * sm.sp_tiles[i] + sm.sp_member[i];  // 2*prefix + cost
+        const float pos = (float)mid2 * (float)members / (2.f * (float)max(total_tiles, 1));
+        sm.sp_member[i] = min(members - 1, (int)pos);
     }
     __syncthreads();
     for (int i = tid; i < n_splits; i += kPlanThreads)
