@@ -17,19 +17,26 @@
 // bytes), B = Q^T (K-major) or P^T (MN-major).  TMEM holds O^T in four 128-lane
 // blocks (columns 0..255) and S^T at columns 256..256+NG.
 //
-// KV tiles are 128 tokens (always inside one 1,536-token page), loaded by TMA as
-// nine 128 x 64 sub-tiles (16 KB, 128-byte swizzle) from a 3-D tensor map
-// [page][token][576] over the slab: page IDs come from the page table with the
-// table's row stride, and the page offset is 64-bit inside the TMA unit (pools
-// above 2 GB; AgentX - InferenceXv3 report, ROCm AITER section).  Shared memory
-// holds Q^T (9 x NG x 128 B) and exactly one tile; the probability tile P^T
-// (bf16) is written into the rope sub-tile's slot once S^T is done with it, so
-// slots are refilled for the next tile as soon as each O^T block has consumed
-// its two latent sub-tiles.
+// KV tiles are 128 tokens (always inside one 1,536-token page) read from a 3-D
+// tensor map [page][token][576] over the slab: page IDs come from the page
+// table with the table's row stride, and the page offset is 64-bit inside the
+// TMA unit (pools above 2 GB; AgentX - InferenceXv3 report, ROCm AITER section).
+// Shared memory holds Q^T (9 x NG x 128 B), the probability tile P^T, and two
+// rings of 16 KB slots through which every tile streams twice:
+//   K ring: the nine 128 x 64 column blocks of the tile, for S^T (from HBM);
+//   V ring: eight 64-token x 128-latent blocks of the same tile, for O^T
+//           (a re-read that hits L2), each covering both 64-column halves of
+//           one 128-row O^T block.
+// S^T and P^T V are issued by two threads in different warps: at M = 128,
+// N <= 64 a single issuing thread cannot keep the tensor pipe busy.  S^T is
+// double-buffered in TMEM, so S^T of tile i+1 runs while the softmax of tile i
+// does, and each ring is consumed in order by its own issuer.
 //
-// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = MMA issuer and TMEM
-// owner, warps 2..5 = softmax (one thread per token lane of S^T; the same
-// threads write the partial output, one thread per latent row of O^T).
+// Warp roles (256 threads): warp 0 = K/Q producer, warp 1 = S^T issuer and
+// TMEM owner, warps 2..5 = softmax (one thread per token lane of S^T; the same
+// threads write the partial output, one thread per latent row of O^T), warp 6
+// = V producer (it also zeroes, in the request's last partial tile, the latent
+// rows past the history before releasing the item), warp 7 = P^T V issuer.
 //
 // Online softmax in fp32 with a lagged maximum: the reference maximum m of a
 // row moves only when a score exceeds it by more than kTau (log2 units).  Each
@@ -40,12 +47,12 @@
 // <= 2^kTau stays finite in bf16.
 //
 // Tokens at or past the chunk end (the request's last, partial tile) are
-// masked in the scores and their latent rows are zeroed in shared memory before
+// masked in the scores and their latent rows are zeroed in the V items before
 // P^T V, so stale or NaN page contents never reach the output.
 //
 // Every mbarrier wait is bounded: after kWaitLimitNs the waiting thread sets
 // the workspace status word and a CTA-wide abort flag, the producer waits (with
-// its own bound) for the copies it issued, the MMA thread waits for its MMAs,
+// its own bound) for the copies it issued, each MMA thread waits for its MMAs,
 // and TMEM is freed before the CTA exits.
 #include <cuda.h>
 #include <math.h>
@@ -55,30 +62,54 @@
 namespace plmla {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kSub = 9;                         // 8 latent sub-tiles + 1 rope sub-tile
-constexpr int kSubBytes = kTile * 64 * 2;       // 128 tokens x 64 columns bf16
-constexpr int kKvBytes = kSub * kSubBytes;
+constexpr int kThreads = 256;
+constexpr int kSub = 9;                         // 8 latent column blocks + 1 rope block
+constexpr int kVItems = 8;                      // V items per tile (4 O^T blocks x 2 token halves)
+constexpr int kSubBytes = kTile * 64 * 2;       // one ring slot: 16 KB
+constexpr int kVHalf = 64 * 64 * 2;             // one 64 x 64 half of a V item
 constexpr int kTmemCols = 512;
-constexpr int kTmemS = 256;
+constexpr int kTmemS = 256;                     // S^T buffers at columns 256 and 320
 constexpr float kTau = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
+constexpr int kMaxDynSmem = 232448;
+constexpr int kMaxK = 8, kMaxV = 8;             // ring slots (K, V) at most
 
 template <int NG>
 struct Smem {
     static constexpr int q_chunk = NG * 128;                // one 64-column chunk of Q^T
-    static constexpr int q_off = kKvBytes;
-    static constexpr int bar_off = q_off + kSub * q_chunk;  // 1024-aligned
-    static constexpr int red_off = bar_off + 256;           // float red[4][64] (25 mbarriers before)
-    static constexpr int fin_off = red_off + 4 * 64 * 4;    // float fin[64]
-    static constexpr int m_off = fin_off + 64 * 4;          // float m[64]   (log2 units)
-    static constexpr int al_off = m_off + 64 * 4;           // float alpha[64]
-    static constexpr int misc_off = al_off + 64 * 4;        // tmem addr, abort, need
+    static constexpr int p_bytes = kTile * 2 * NG;          // P^T, bf16
+    static constexpr int bar_bytes = 512;
+    static constexpr int misc_bytes = bar_bytes + 4 * 64 * 4 + 3 * 64 * 4 + 16;
+    static constexpr int fixed = p_bytes + kSub * q_chunk + misc_bytes + 1024;
+    static constexpr int slots_fit = (kMaxDynSmem - fixed) / kSubBytes;
+    // half of the slots for each ring
+    static constexpr int v_slots = slots_fit / 2 < kMaxV ? slots_fit / 2 : kMaxV;
+    static constexpr int k_slots = slots_fit - v_slots < kMaxK ? slots_fit - v_slots : kMaxK;
+    static constexpr int v_off = k_slots * kSubBytes;
+    static constexpr int p_off = v_off + v_slots * kSubBytes;
+    static constexpr int q_off = p_off + p_bytes;            // 1024-aligned
+    static constexpr int bar_off = q_off + kSub * q_chunk;   // 1024-aligned
+    static constexpr int red_off = bar_off + bar_bytes;      // float red[4][64]
+    static constexpr int fin_off = red_off + 4 * 64 * 4;     // float fin[64]
+    static constexpr int m_off = fin_off + 64 * 4;           // float m[64]   (log2 units)
+    static constexpr int al_off = m_off + 64 * 4;            // float alpha[64]
+    static constexpr int misc_off = al_off + 64 * 4;         // tmem addr, abort, need
     static constexpr int bytes = misc_off + 16;
-    static constexpr int alloc = bytes + 1024;              // slack for 1024-B alignment
+    static constexpr int alloc = bytes + 1024;               // slack for 1024-B alignment
+    static_assert(k_slots >= 2 && v_slots >= 2, "ring depth");
+    static_assert(alloc <= kMaxDynSmem, "shared memory budget");
 };
+
+// barrier offsets inside the barrier area (8 bytes each)
+constexpr int kBarFullK = 0, kBarEmptyK = 64, kBarFullV = 128, kBarEmptyV = 192;
+constexpr int kBarVtmp = 256, kBarQ = 264, kBarQe = 272, kBarS = 280, kBarSfree = 296;
+constexpr int kBarP = 312, kBarPv = 320, kBarOf = 328, kBarDrainS = 336, kBarDrainPv = 344;
+constexpr int kBarPvIssued = 352;                // [4] P^T V of tile g issued, on barrier g % 4
+// S^T of tile g waits until P^T V of tile g - kLead has been issued (kLead <= 3,
+// so that the next phase of that barrier, tile g - kLead + 4, cannot complete first)
+constexpr int kLead = 2;
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -173,6 +204,31 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
+}
+
+// The same load with an L2 eviction-priority policy (from createpolicy).
+__device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                                 int c2, uint32_t bar, uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
@@ -389,25 +445,32 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
 
 template <int NG>
 __global__ void __launch_bounds__(kThreads, 1)
-decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_qn,
-                 const __grid_constant__ CUtensorMap tm_qr, const DecodeArgs a)
+decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
+                 const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
+                 const DecodeArgs a)
 {
     using L = Smem<NG>;
+    constexpr int NK = L::k_slots, NV = L::v_slots;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t s_kv = smem_u32(smem);
-    const uint32_t s_q = s_kv + L::q_off;
-    const uint32_t bars = s_kv + L::bar_off;
-    const uint32_t bar_full = bars;                 // [9] sub-tile landed
-    const uint32_t bar_empty = bars + 8 * kSub;     // [9] sub-tile slot free
-    const uint32_t bar_q = bars + 16 * kSub;        // Q^T landed
-    const uint32_t bar_qe = bar_q + 8;              // Q^T no longer read (segment's last S^T done)
-    const uint32_t bar_s = bar_q + 16;              // S^T of a tile complete
-    const uint32_t bar_p = bar_q + 24;              // P^T of a tile written (128 arrivals)
-    const uint32_t bar_pv = bar_q + 32;             // P^T V of a tile complete
-    const uint32_t bar_of = bar_q + 40;             // O^T read out by the epilogue (128 arrivals)
-    const uint32_t bar_drain = bar_q + 48;
+    const uint32_t s_k = smem_u32(smem);             // K ring
+    const uint32_t s_v = s_k + L::v_off;             // V ring
+    const uint32_t s_p = s_k + L::p_off;             // P^T
+    const uint32_t s_q = s_k + L::q_off;             // Q^T
+    const uint32_t bars = s_k + L::bar_off;
+    const uint32_t bar_full_k = bars + kBarFullK;    // [NK] K item landed
+    const uint32_t bar_empty_k = bars + kBarEmptyK;  // [NK] K slot free
+    const uint32_t bar_full_v = bars + kBarFullV;    // [NV] V item ready
+    const uint32_t bar_empty_v = bars + kBarEmptyV;  // [NV] V slot free
+    const uint32_t bar_vtmp = bars + kBarVtmp;       // V item of a partial tile landed (pre-mask)
+    const uint32_t bar_q = bars + kBarQ;             // Q^T landed
+    const uint32_t bar_qe = bars + kBarQe;           // Q^T no longer read (segment's last S^T done)
+    const uint32_t bar_s = bars + kBarS;             // [2] S^T of a tile complete, per buffer
+    const uint32_t bar_sfree = bars + kBarSfree;     // [2] S^T buffer read by the softmax (128)
+    const uint32_t bar_p = bars + kBarP;             // P^T of a tile written (128 arrivals)
+    const uint32_t bar_pv = bars + kBarPv;           // P^T V of a tile complete
+    const uint32_t bar_of = bars + kBarOf;           // O^T read out by the epilogue (128 arrivals)
     float *red = reinterpret_cast<float *>(smem + L::red_off);
     float *fin = reinterpret_cast<float *>(smem + L::fin_off);
     float *m_sm = reinterpret_cast<float *>(smem + L::m_off);
@@ -422,22 +485,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     const int row0 = team * NG;
     if (threadIdx.x == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_kv)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_qn)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_qr)) : "memory");
     }
 
     if (threadIdx.x == 0) {
-        for (int k = 0; k < kSub; ++k) {
-            mbar_init(bar_full + 8 * k, 1);
-            mbar_init(bar_empty + 8 * k, 1);
+        for (int k = 0; k < NK; ++k) {
+            mbar_init(bar_full_k + 8 * k, 1);
+            mbar_init(bar_empty_k + 8 * k, 1);
         }
+        for (int k = 0; k < NV; ++k) {
+            mbar_init(bar_full_v + 8 * k, 1);
+            mbar_init(bar_empty_v + 8 * k, 1);
+        }
+        mbar_init(bar_vtmp, 1);
         mbar_init(bar_q, 1);
         mbar_init(bar_qe, 1);
         mbar_init(bar_s, 1);
+        mbar_init(bar_s + 8, 1);
+        mbar_init(bar_sfree, 128);
+        mbar_init(bar_sfree + 8, 128);
         mbar_init(bar_p, 128);
         mbar_init(bar_pv, 1);
         mbar_init(bar_of, 128);
-        mbar_init(bar_drain, 1);
+        mbar_init(bars + kBarDrainS, 1);
+        mbar_init(bars + kBarDrainPv, 1);
+        for (int k = 0; k < 4; ++k)
+            mbar_init(bars + kBarPvIssued + 8 * k, 1);
         *abort_flag = 0;
         *need_sm = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -462,10 +537,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     const int seg_total = *a.seg_count;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ producer
+        // ---------------------------------------------------------- K producer
         if (lane == 0) {
-            int gt = 0;                              // tiles issued so far (all segments)
-            int li_gt = -1, li_k = kSub - 1;         // last issued (tile, sub-tile)
+            // the latent blocks are read again (as V items) shortly: keep them in
+            // L2 until then; the rope block is not
+            const uint64_t pol_keep = l2_policy_evict_last();
+            const uint64_t pol_once = l2_policy_evict_first();
+            int slot = 0;
+            uint32_t phase = 0;
+            int issued = 0;                          // K items issued (all segments)
             int q_loads = 0;
             bool ok = true;
             for (int s = seg_begin; s < seg_end && ok; ++s) {
@@ -484,42 +564,130 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 ++q_loads;
                 const int32_t *trow = a.page_table + (int64_t)seg.x * a.table_ld;
                 const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
-                for (int i = 0; i < n_tiles && ok; ++i, ++gt) {
+                for (int i = 0; i < n_tiles && ok; ++i) {
                     const int t = seg.y + i * kTile;
                     const int page = trow[t / kPageTokens];
                     const int tok = t % kPageTokens;
                     for (int k = 0; k < kSub; ++k) {
-                        if (!wait_bounded(bar_empty + 8 * k, (gt & 1) ^ 1, abort_flag, a.status,
+                        if (!wait_bounded(bar_empty_k + 8 * slot, phase ^ 1, abort_flag, a.status,
                                           2)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(bar_full + 8 * k, kSubBytes);
-                        tma_load_3d(s_kv + k * kSubBytes, &tm_kv, 64 * k, tok, page,
-                                    bar_full + 8 * k);
-                        li_gt = gt;
-                        li_k = k;
+                        mbar_arrive_expect_tx(bar_full_k + 8 * slot, kSubBytes);
+                        tma_load_3d_hint(s_k + slot * kSubBytes, &tm_kv, 64 * k, tok, page,
+                                         bar_full_k + 8 * slot, k < kSub - 1 ? pol_keep : pol_once);
+                        ++issued;
+                        if (++slot == NK) {
+                            slot = 0;
+                            phase ^= 1;
+                        }
                     }
                 }
             }
-            // every issued copy must land before the CTA can exit
+            // every issued copy must land before the CTA can exit: the last NK
+            // items may still be in flight, earlier ones were consumed
             if (q_loads > 0)
                 wait_drain(bar_q, (q_loads - 1) & 1);
-            for (int k = 0; k < kSub; ++k) {
-                const int tile_k = k <= li_k ? li_gt : li_gt - 1;
-                if (tile_k >= 0)
-                    wait_drain(bar_full + 8 * k, tile_k & 1);
+            for (int it = issued > NK ? issued - NK : 0; it < issued; ++it)
+                wait_drain(bar_full_k + 8 * (it % NK), (uint32_t)(it / NK) & 1u);
+        }
+    } else if (warp == 6) {
+        // ---------------------------------------------------------- V producer
+        // V item v of a tile = latent block v / 2 (128 columns), token half v % 2.
+        // Items of a partial tile land on bar_vtmp first; the warp zeroes the
+        // rows past the history and then releases the item to the issuer.
+        const uint64_t pol_once = l2_policy_evict_first();   // the tile's last read
+        int slot = 0;
+        uint32_t phase = 0, vtmp_phase = 0;
+        int issued = 0;
+        uint32_t partial_bits = 0;                   // bit b: the item issued b items ago was partial
+        bool vtmp_pending = false;                   // a partial item's copy was never seen landing
+        bool ok = true;
+        for (int s = seg_begin; s < seg_end && ok; ++s) {
+            const int4 seg = a.segments[s];
+            const int32_t *trow = a.page_table + (int64_t)seg.x * a.table_ld;
+            const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
+            for (int i = 0; i < n_tiles && ok; ++i) {
+                const int t = seg.y + i * kTile;
+                const int page = trow[t / kPageTokens];
+                const int tok = t % kPageTokens;
+                for (int v = 0; v < kVItems; ++v) {
+                    // this item's 64 tokens reach past the history: mask it
+                    const bool partial = t + 64 * (v & 1) + 64 > seg.z;
+                    bool got = true;
+                    if (lane == 0)
+                        got = wait_bounded(bar_empty_v + 8 * slot, phase ^ 1, abort_flag, a.status,
+                                           11);
+                    if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = s_v + slot * kSubBytes;
+                    const int col = 128 * (v >> 1), tk = tok + 64 * (v & 1);
+                    const uint32_t done_bar = partial ? bar_vtmp : bar_full_v + 8 * slot;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(done_bar, kSubBytes);
+                        tma_load_3d_hint(dst, &tm_v, col, tk, page, done_bar, pol_once);
+                        tma_load_3d_hint(dst + kVHalf, &tm_v, col + 64, tk, page, done_bar,
+                                         pol_once);
+                    }
+                    ++issued;
+                    partial_bits = (partial_bits << 1) | (partial ? 1u : 0u);
+                    if (partial) {
+                        // rows r of this item hold token t + 64 * (v % 2) + r
+                        const bool landed =
+                            wait_bounded(bar_vtmp, vtmp_phase, abort_flag, a.status, 12);
+                        if (!__all_sync(0xffffffffu, landed)) {
+                            vtmp_pending = true;
+                            ok = false;
+                            break;
+                        }
+                        vtmp_phase ^= 1;
+                        const int first_dead = seg.z - (t + 64 * (v & 1));   // may be <= 0
+                        for (int r = lane; r < 64; r += 32) {
+                            if (r >= first_dead) {
+#pragma unroll
+                                for (int half = 0; half < 2; ++half)
+#pragma unroll
+                                    for (int ch = 0; ch < 8; ++ch)
+                                        st_shared_v4(dst + half * kVHalf + r * 128 + 16 * ch, 0u,
+                                                     0u, 0u, 0u);
+                            }
+                        }
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(bar_full_v + 8 * slot);
+                    }
+                    if (++slot == NV) {
+                        slot = 0;
+                        phase ^= 1;
+                    }
+                }
             }
         }
+        if (lane == 0) {
+            // copies still in flight: the last NV items that complete on their
+            // slot's barrier, and a partial item whose landing was never seen
+            for (int back = 0; back < NV && back < issued; ++back) {
+                const int it = issued - 1 - back;
+                if (((partial_bits >> back) & 1u) == 0u)
+                    wait_drain(bar_full_v + 8 * (it % NV), (uint32_t)(it / NV) & 1u);
+            }
+            if (vtmp_pending)
+                wait_drain(bar_vtmp, vtmp_phase);
+        }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+        // -------------------------------------------------------- S^T issuer
         if (lane == 0) {
             bool issued = false, ok = true;
             constexpr uint32_t idesc_s = idesc_bf16(128, NG, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, NG, true, true);
-            constexpr uint32_t p_layout = NG == 64 ? kSw128 : (NG == 32 ? kSw64 : kSw32);
-            const uint32_t s_p = s_kv + (kSub - 1) * kSubBytes;  // P^T lives in the rope slot
-            int gt = 0;
+            const uint64_t dk0 = sdesc(s_k, 16, 1024, kSw128);
+            const uint64_t dq0 = sdesc(s_q, 16, 1024, kSw128);
+            int slot = 0;
+            uint32_t phase = 0;
+            int g = 0;                               // tiles so far (all segments)
             for (int s = seg_begin; s < seg_end && ok; ++s) {
                 const int local = s - seg_begin;
                 const int4 seg = a.segments[s];
@@ -528,58 +696,113 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     ok = false;
                     break;
                 }
-                for (int i = 0; i < n_tiles; ++i, ++gt) {
-                    const uint32_t par = gt & 1;
-                    // S^T = K_tile . Q^T over the 576 columns
-                    for (int k = 0; k < kSub && ok; ++k) {
-                        if (!wait_bounded(bar_full + 8 * k, par, abort_flag, a.status, 4)) {
+                for (int i = 0; i < n_tiles; ++i, ++g) {
+                    const uint32_t b = g & 1;
+                    // the softmax of tile g - 2 must be done with this S^T buffer, and
+                    // S^T runs at most kLead tiles ahead of P^T V, so that a tile's
+                    // latent blocks are still in L2 when they are read again as V items
+                    if (g >= 2 && !wait_bounded(bar_sfree + 8 * b, ((g - 2) >> 1) & 1, abort_flag,
+                                                a.status, 13)) {
+                        ok = false;
+                        break;
+                    }
+                    if (g >= kLead &&
+                        !wait_bounded(bars + kBarPvIssued + 8 * ((g - kLead) & 3),
+                                      ((g - kLead) >> 2) & 1, abort_flag, a.status, 10)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d_s = tmem + kTmemS + 64 * b;
+#pragma unroll
+                    for (int k = 0; k < kSub; ++k) {
+                        if (!wait_bounded(bar_full_k + 8 * slot, phase, abort_flag, a.status, 4)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
+                        const uint64_t da = dk0 + (uint64_t)(slot * (kSubBytes >> 4));
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t da = sdesc(s_kv + k * kSubBytes + 32 * kk, 16, 1024, kSw128);
-                            const uint64_t db = sdesc(s_q + k * L::q_chunk + 32 * kk, 16, 1024, kSw128);
-                            mma_bf16(tmem + kTmemS, da, db, idesc_s, (k | kk) != 0);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16(d_s, da + 2 * kk,
+                                     dq0 + (uint64_t)(k * (L::q_chunk >> 4) + 2 * kk), idesc_s,
+                                     (k | kk) != 0);
+                        mma_commit(bar_empty_k + 8 * slot);
                         issued = true;
+                        if (++slot == NK) {
+                            slot = 0;
+                            phase ^= 1;
+                        }
                     }
                     if (!ok)
                         break;
-                    mma_commit(bar_s);
+                    mma_commit(bar_s + 8 * b);
                     if (i == n_tiles - 1)
                         mma_commit(bar_qe);
+                }
+            }
+            if (issued) {
+                mma_commit(bars + kBarDrainS);
+                wait_drain(bars + kBarDrainS, 0);
+            }
+        }
+    } else if (warp == 7) {
+        // ----------------------------------------------------- P^T V issuer
+        if (lane == 0) {
+            bool issued = false, ok = true;
+            constexpr uint32_t idesc_pv = idesc_bf16(128, NG, true, true);
+            constexpr uint32_t p_layout = NG == 64 ? kSw128 : (NG == 32 ? kSw64 : kSw32);
+            const uint64_t dv0 = sdesc(s_v, kVHalf, 1024, kSw128);
+            const uint64_t dp0 = sdesc(s_p, 8192, 16 * NG, p_layout);
+            int slot = 0;
+            uint32_t phase = 0;
+            int g = 0;
+            for (int s = seg_begin; s < seg_end && ok; ++s) {
+                const int local = s - seg_begin;
+                const int4 seg = a.segments[s];
+                const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
+                for (int i = 0; i < n_tiles; ++i, ++g) {
+                    // O^T of the previous segment must have been read out
                     if (i == 0 && local > 0 &&
                         !wait_bounded(bar_of, (local - 1) & 1, abort_flag, a.status, 5)) {
                         ok = false;
                         break;
                     }
-                    // O^T += V^T . P^T, four 128-row latent blocks over the 128 tokens
-                    if (!wait_bounded(bar_p, par, abort_flag, a.status, 6)) {
+                    if (!wait_bounded(bar_p, g & 1, abort_flag, a.status, 6)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t da = sdesc(s_kv + 2 * j * kSubBytes + 2048 * kk,
-                                                      kSubBytes, 1024, kSw128);
-                            const uint64_t db = sdesc(s_p + kk * 32 * NG, 8192, 16 * NG, p_layout);
-                            mma_bf16(tmem + 64 * j, da, db, idesc_pv, (i | kk) != 0);
+                    for (int v = 0; v < kVItems; ++v) {
+                        if (!wait_bounded(bar_full_v + 8 * slot, phase, abort_flag, a.status, 14)) {
+                            ok = false;
+                            break;
                         }
-                        mma_commit(bar_empty + 8 * (2 * j));
-                        mma_commit(bar_empty + 8 * (2 * j + 1));
+                        tc_fence_after();
+                        const uint64_t da = dv0 + (uint64_t)(slot * (kSubBytes >> 4));
+                        const int j = v >> 1, h = v & 1;
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16(tmem + 64 * j, da + (uint64_t)(128 * kk),
+                                     dp0 + (uint64_t)((4 * h + kk) * 2 * NG), idesc_pv,
+                                     (i | h | kk) != 0);
+                        mma_commit(bar_empty_v + 8 * slot);
+                        issued = true;
+                        if (++slot == NV) {
+                            slot = 0;
+                            phase ^= 1;
+                        }
                     }
-                    mma_commit(bar_empty + 8 * (kSub - 1));
+                    if (!ok)
+                        break;
                     mma_commit(bar_pv);
+                    mbar_arrive(bars + kBarPvIssued + 8 * (g & 3));
                 }
             }
             if (issued) {
-                mma_commit(bar_drain);
-                wait_drain(bar_drain, 0);
+                mma_commit(bars + kBarDrainPv);
+                wait_drain(bars + kBarDrainPv, 0);
             }
         }
     } else {
@@ -588,7 +811,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         const int tok = 32 * q + lane;          // token lane of S^T / latent row of O^T
         const int st = threadIdx.x - 64;        // 0..127
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
-        const uint32_t s_p = s_kv + (kSub - 1) * kSubBytes;
         const uint32_t m_addr = smem_u32(m_sm);
         bool ok = true;
         int gt = 0;
@@ -609,18 +831,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 lsum[c] = 0.f;
 
             for (int i = 0; i < n_tiles; ++i, ++gt) {
-                const uint32_t par = gt & 1;
                 const int t_base = seg.y + i * kTile;
                 const int t = t_base + tok;
                 const bool tile_visible = t_base + kTile <= vis_all;
+                const uint32_t b = gt & 1;
+                const uint32_t s_col = kTmemS + 64 * b;
                 // warp-uniform, because tcgen05.ld below is a .sync.aligned instruction
-                const bool got =
-                    __all_sync(0xffffffffu, wait_bounded(bar_s, par, abort_flag, a.status, 7));
+                const bool got = __all_sync(
+                    0xffffffffu, wait_bounded(bar_s + 8 * b, (gt >> 1) & 1, abort_flag, a.status, 7));
                 float x[NG];
                 bool exceed = false;
                 if (got) {
                     tc_fence_after();
-                    load_scores<NG>(tmem + t_lane + kTmemS, a.scale_log2, tile_visible, t, seg.z,
+                    load_scores<NG>(tmem + t_lane + s_col, a.scale_log2, tile_visible, t, seg.z,
                                     vis_all, row0, a.num_heads, x);
                     exceed = shift_and_test<NG>(x, m_addr);
                 }
@@ -677,57 +900,58 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
 #pragma unroll
-                                for (int b = 0; b < NG / 16; ++b) {
+                                for (int bb = 0; bb < NG / 16; ++bb) {
                                     uint32_t r[16];
-                                    const uint32_t ta = tmem + t_lane + 64 * j + 16 * b;
+                                    const uint32_t ta = tmem + t_lane + 64 * j + 16 * bb;
                                     tmem_ld16(ta, r);
                                     tmem_wait_ld();
 #pragma unroll
                                     for (int e = 0; e < 16; ++e)
                                         r[e] = __float_as_uint(
                                             __uint_as_float(r[e]) *
-                                            ld_shared_f32(al_addr + 4 * (16 * b + e)));
+                                            ld_shared_f32(al_addr + 4 * (16 * bb + e)));
                                     tmem_st16(ta, r);
                                 }
                             }
                             tmem_wait_st();
                         }
                     }
-                    load_scores<NG>(tmem + t_lane + kTmemS, a.scale_log2, tile_visible, t, seg.z,
+                    load_scores<NG>(tmem + t_lane + s_col, a.scale_log2, tile_visible, t, seg.z,
                                     vis_all, row0, a.num_heads, x);
                     shift_and_test<NG>(x, m_addr);
                 }
-                // probabilities 2^(x - m) (x is already shifted), running sums, and
-                // this token's P^T row (bf16, swizzled)
+                // this S^T buffer may now be overwritten by the tile after next
+                tc_fence_before();
+                mbar_arrive(bar_sfree + 8 * b);
+                // probabilities 2^(x - m) (x is already shifted) and running sums
+                uint32_t pk[NG / 2];
+#pragma unroll
+                for (int c = 0; c < NG; c += 2) {
+                    const float p0 = fast_exp2(x[c]);        // 2^-inf = 0
+                    const float p1 = fast_exp2(x[c + 1]);
+                    lsum[c] += p0;
+                    lsum[c + 1] += p1;
+                    pk[c / 2] = pack_bf16x2(p0, p1);
+                }
+                // P^T is free once the previous tile's P^T V has completed
+                if (gt > 0) {
+                    const bool done =
+                        wait_bounded(bar_pv, (gt - 1) & 1, abort_flag, a.status, 8);
+                    if (softmax_bar_or(!done)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 {
                     constexpr int row_bytes = 2 * NG;
                     constexpr int swz_bits = NG == 64 ? 3 : (NG == 32 ? 2 : 1);
 #pragma unroll
                     for (int ch = 0; ch < row_bytes / 16; ++ch) {
-                        uint32_t w4[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int c = 8 * ch + 2 * e;
-                            const float p0 = fast_exp2(x[c]);       // 2^-inf = 0
-                            const float p1 = fast_exp2(x[c + 1]);
-                            lsum[c] += p0;
-                            lsum[c + 1] += p1;
-                            w4[e] = pack_bf16x2(p0, p1);
-                        }
                         const uint32_t off = (uint32_t)(tok * row_bytes + 16 * ch);
                         const uint32_t sw = off ^ (((off >> 7) & ((1u << swz_bits) - 1u)) << 4);
-                        st_shared_v4(s_p + sw, w4[0], w4[1], w4[2], w4[3]);
+                        st_shared_v4(s_p + sw, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
+                                     pk[4 * ch + 3]);
                     }
-                }
-                if (t >= seg.z) {
-                    // past the request's history: zero this token's latent row so
-                    // that P = 0 never meets a stale (possibly NaN) value in the MMA
-#pragma unroll
-                    for (int k = 0; k < kSub - 1; ++k)
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch)
-                            st_shared_v4(s_kv + k * kSubBytes + tok * 128 + 16 * ch, 0u, 0u, 0u,
-                                         0u);
                 }
                 fence_proxy_async();
                 tc_fence_before();
@@ -760,22 +984,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             const uint32_t inv_addr = smem_u32(fin);
             float *out0 = a.o_part + (int64_t)(team * seg_total + s) * NG * kLatent + tok;
 #pragma unroll
-            for (int b = 0; b < NG / 16; ++b) {
+            for (int bb = 0; bb < NG / 16; ++bb) {
                 float inv[16];
 #pragma unroll
                 for (int e4 = 0; e4 < 16; e4 += 4)
                     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
                                  : "=f"(inv[e4]), "=f"(inv[e4 + 1]), "=f"(inv[e4 + 2]),
                                    "=f"(inv[e4 + 3])
-                                 : "r"(inv_addr + 4 * (16 * b + e4)));
+                                 : "r"(inv_addr + 4 * (16 * bb + e4)));
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint32_t r[16];
-                    tmem_ld16(tmem + t_lane + 64 * j + 16 * b, r);
+                    tmem_ld16(tmem + t_lane + 64 * j + 16 * bb, r);
                     tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
-                        out0[(int64_t)(16 * b + e) * kLatent + 128 * j] =
+                        out0[(int64_t)(16 * bb + e) * kLatent + 128 * j] =
                             __uint_as_float(r[e]) * inv[e];
                 }
             }
@@ -835,11 +1059,12 @@ bool make_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *di
 template <int NG>
 cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
 {
-    CUtensorMap tm_kv, tm_qn, tm_qr;
+    CUtensorMap tm_kv, tm_v, tm_qn, tm_qr;
     const cuuint64_t kv_dims[3] = {(cuuint64_t)kRow, (cuuint64_t)kPageTokens,
                                    (cuuint64_t)a.num_pages};
     const cuuint64_t kv_strides[2] = {(cuuint64_t)kRow * 2, (cuuint64_t)a.page_stride * 2};
     const cuuint32_t kv_box[3] = {64, (cuuint32_t)kTile, 1};
+    const cuuint32_t v_box[3] = {64, 64, 1};
     const cuuint64_t rows = (cuuint64_t)a.num_reqs * a.rows_per_req;
     const cuuint64_t qn_dims[2] = {(cuuint64_t)kLatent, rows};
     const cuuint64_t qn_strides[1] = {(cuuint64_t)kLatent * 2};
@@ -847,11 +1072,11 @@ cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
     const cuuint64_t qr_strides[1] = {(cuuint64_t)kRope * 2};
     const cuuint32_t q_box[2] = {64, (cuuint32_t)NG};
     if (!make_map(&tm_kv, a.slab, 3, kv_dims, kv_strides, kv_box) ||
+        !make_map(&tm_v, a.slab, 3, kv_dims, kv_strides, v_box) ||
         !make_map(&tm_qn, a.q_nope, 2, qn_dims, qn_strides, q_box) ||
         !make_map(&tm_qr, a.q_rope, 2, qr_dims, qr_strides, q_box))
         return cudaErrorInvalidValue;
     constexpr int smem = Smem<NG>::alloc;
-    static_assert(Smem<NG>::alloc <= 232448, "shared memory budget");
     cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<NG>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess)
@@ -866,7 +1091,7 @@ cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NG>, tm_kv, tm_qn, tm_qr, a);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NG>, tm_kv, tm_v, tm_qn, tm_qr, a);
 }
 
 }  // namespace
