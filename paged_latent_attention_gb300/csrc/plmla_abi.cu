@@ -42,8 +42,8 @@ bool shape_ok(int32_t num_reqs, int32_t n_q, int32_t num_heads)
 }
 
 struct WorkspaceLayout {
-    size_t status, indptr, chunk, seg_count, segments, seg_req, seg_member, o_part, lse_part,
-        total;
+    size_t status, indptr, chunk, seg_count, segments, seg_req, seg_member, done, o_part,
+        lse_part, total;
     int32_t max_segments;
 };
 
@@ -103,6 +103,8 @@ WorkspaceLayout layout_for(int32_t num_reqs, const Shape &sh)
     off = align_up(off + sizeof(int32_t) * (size_t)(num_reqs + 1));
     w.seg_member = off;
     off = align_up(off + sizeof(int32_t) * (size_t)(sh.members + 1));
+    w.done = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)sh.groups * num_reqs);
     const size_t part_rows = (size_t)sh.groups * w.max_segments * sh.group_rows;
     w.o_part = off;
     off = align_up(off + sizeof(float) * part_rows * kLatent);
@@ -181,7 +183,7 @@ extern "C" plmla_status mla_split_combine(const float *o_part, const float *lse_
                                      n_q_per_req * num_heads,
                                      static_cast<const __nv_bfloat16 *>(gate), num_reqs,
                                      n_q_per_req, num_heads, static_cast<__nv_bfloat16 *>(out),
-                                     lse, static_cast<cudaStream_t>(stream));
+                                     lse, nullptr, nullptr, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
 }
 
@@ -239,6 +241,8 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
     plan.segments = reinterpret_cast<int4 *>(ws + w.segments);
     plan.seg_req_indptr = reinterpret_cast<int32_t *>(ws + w.seg_req);
     plan.seg_member_indptr = reinterpret_cast<int32_t *>(ws + w.seg_member);
+    plan.done = reinterpret_cast<int32_t *>(ws + w.done);
+    plan.n_done = sh.groups * num_reqs;
     float *o_part = reinterpret_cast<float *>(ws + w.o_part);
     float *lse_part = reinterpret_cast<float *>(ws + w.lse_part);
 
@@ -273,13 +277,15 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
     a.o_part = o_part;
     a.lse_part = lse_part;
     a.status = plan.status;
+    a.done = plan.done;
     err = launch_decode_tc(a, s);
     if (err != cudaSuccess || record(ev.combine_begin, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
 
     err = launch_combine(o_part, lse_part, plan.seg_req_indptr, plan.seg_count, sh.group_rows,
                          static_cast<const __nv_bfloat16 *>(gate), num_reqs, n_q_per_req,
-                         num_heads, static_cast<__nv_bfloat16 *>(out), lse, s);
+                         num_heads, static_cast<__nv_bfloat16 *>(out), lse, plan.done,
+                         plan.status, s);
     if (err != cudaSuccess || record(ev.combine_end, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
     return PLMLA_OK;

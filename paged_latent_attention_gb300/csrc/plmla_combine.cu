@@ -18,16 +18,62 @@ namespace plmla {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr int32_t kStatusCombineWait = 16;
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Lane 0 waits (bounded) until `need` segments of the row's request have been
+// published by the decode kernel; false if the wait gave up or the decode
+// reported an error.
+__device__ bool wait_segments(const int32_t *counter, int need, int32_t *status)
+{
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) {
+        const unsigned long long t0 = global_ns();
+        while (ld_acquire(counter) < need) {
+            if (*reinterpret_cast<volatile int32_t *>(status) != 0) {
+                ok = false;
+                break;
+            }
+            if (global_ns() - t0 > kWaitLimitNs) {
+                atomicExch(status, kStatusCombineWait);
+                ok = false;
+                break;
+            }
+            __nanosleep(256);
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    // every lane takes its own acquire of the (final) count before reading
+    if (ok)
+        (void)ld_acquire(counter);
+    return ok;
+}
 
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
                const int32_t *__restrict__ indptr, const int32_t *__restrict__ seg_stride,
                int group_rows, const __nv_bfloat16 *__restrict__ gate, int num_reqs, int n_q,
-               int num_heads, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse)
+               int num_heads, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
+               const int32_t *__restrict__ done, int32_t *status)
 {
-    // launched as a programmatic dependent of the decode kernel: wait for its
-    // partial states (a no-op when launched on its own)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Without counters: launched as a programmatic dependent of the decode
+    // kernel (or on its own), wait for the previous grid's partial states.
+    if (done == nullptr)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
@@ -38,12 +84,16 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     const int rw = (int)(row % rows_per_req);   // j * H + h within the request
     const int g = rw / group_rows;               // row group (team) of this row
     const int gi = rw % group_rows;              // row inside the group's partials
-    const int base = seg_stride != nullptr ? g * (*seg_stride) : 0;
-    const int s0 = base + indptr[r], s1 = base + indptr[r + 1];
+    const int base = seg_stride != nullptr ? g * __ldcg(seg_stride) : 0;
+    const int s0 = base + __ldcg(indptr + r), s1 = base + __ldcg(indptr + r + 1);
+    // With counters: this request's partial states are complete once all its
+    // segments of this team are published (other requests may still run).
+    if (done != nullptr && !wait_segments(done + g * num_reqs + r, s1 - s0, status))
+        return;
 
     float m = -INFINITY;
     for (int s = s0; s < s1; ++s)
-        m = fmaxf(m, lse_part[(int64_t)s * group_rows + gi]);
+        m = fmaxf(m, __ldcg(lse_part + (int64_t)s * group_rows + gi));
 
     float4 acc[4];
 #pragma unroll
@@ -52,7 +102,7 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     float wsum = 0.f;
     if (m != -INFINITY) {
         for (int s = s0; s < s1; ++s) {
-            const float l = lse_part[(int64_t)s * group_rows + gi];
+            const float l = __ldcg(lse_part + (int64_t)s * group_rows + gi);
             if (l == -INFINITY)
                 continue;
             const float w = expf(l - m);
@@ -61,7 +111,7 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
                 o_part + ((int64_t)s * group_rows + gi) * kLatent);
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const float4 v = src[lane + 32 * k];
+                const float4 v = __ldcg(src + lane + 32 * k);
                 acc[k].x = fmaf(w, v.x, acc[k].x);
                 acc[k].y = fmaf(w, v.y, acc[k].y);
                 acc[k].z = fmaf(w, v.z, acc[k].z);
@@ -97,7 +147,8 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
 cudaError_t launch_combine(const float *o_part, const float *lse_part, const int32_t *indptr,
                            const int32_t *seg_stride, int group_rows,
                            const __nv_bfloat16 *gate, int num_reqs, int n_q, int num_heads,
-                           __nv_bfloat16 *out, float *lse, cudaStream_t stream)
+                           __nv_bfloat16 *out, float *lse, const int32_t *done,
+                           int32_t *status, cudaStream_t stream)
 {
     const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
     const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
@@ -111,8 +162,10 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, const int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if ((done == nullptr) != (status == nullptr))
+        return cudaErrorInvalidValue;
     return cudaLaunchKernelEx(&cfg, combine_kernel, o_part, lse_part, indptr, seg_stride,
-                              group_rows, gate, num_reqs, n_q, num_heads, out, lse);
+                              group_rows, gate, num_reqs, n_q, num_heads, out, lse, done, status);
 }
 
 }  // namespace plmla

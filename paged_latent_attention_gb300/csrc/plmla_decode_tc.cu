@@ -535,6 +535,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     const int seg_begin = a.seg_member_indptr[member];
     const int seg_end = a.seg_member_indptr[member + 1];   // empty range: no work
     const int seg_total = *a.seg_count;
+    // the combine kernel may launch now: it occupies SMs only as CTAs of this
+    // grid exit, and waits per request on the finished-segment counters
+    asm volatile("griddepcontrol.launch_dependents;");
 
     if (warp == 0) {
         // ---------------------------------------------------------- K producer
@@ -1005,12 +1008,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             }
             tc_fence_before();
             mbar_arrive(bar_of);
+            // publish the segment: every thread's stores, then one counter update
+            __threadfence();
+            softmax_bar();
+            if (st == 0)
+                atomicAdd(a.done + team * a.num_reqs + seg.x, 1);
         }
     }
 
-    // the combine kernel may be scheduled as SMs free up; it waits for this
-    // grid's completion before reading the partial states
-    asm volatile("griddepcontrol.launch_dependents;");
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {

@@ -27,6 +27,8 @@ struct PlanBuffers {
     int4 *segments;             // [S] (request, t0, t1, member)
     int32_t *seg_req_indptr;    // [R + 1] segments of request r: [r], [r + 1]
     int32_t *seg_member_indptr; // [members + 1] segments of member k: [k], [k + 1]
+    int32_t *done;              // [n_done] finished-segment counters, zeroed by the plan kernel
+    int32_t n_done;
 };
 
 struct DecodeArgs {
@@ -50,6 +52,7 @@ struct DecodeArgs {
     float *o_part;                 // [groups * S, group_rows, 512]
     float *lse_part;               // [groups * S, group_rows], natural log
     int32_t *status;               // device status word (0 = ok, else the failed wait)
+    int32_t *done;                 // [groups * R] segments of (team, request) written
 };
 
 // Largest of 64, 32, 16 that divides `rows`, or 0.
@@ -69,10 +72,14 @@ cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream);
 // lives in group g = rw / group_rows at row rw % group_rows of the partials
 // of segments [g*stride + indptr[r], g*stride + indptr[r + 1]), where stride is
 // *seg_stride (or 0 when seg_stride is null).
+// With `done` (and `status`) set, the combine is launched while the decode is
+// still running and waits, per request, until done[team * R + r] counts all of
+// the request's segments; without it, it waits for the previous grid to finish.
 cudaError_t launch_combine(const float *o_part, const float *lse_part, const int32_t *indptr,
                            const int32_t *seg_stride, int group_rows,
                            const __nv_bfloat16 *gate, int num_reqs, int n_q, int num_heads,
-                           __nv_bfloat16 *out, float *lse, cudaStream_t stream);
+                           __nv_bfloat16 *out, float *lse, const int32_t *done,
+                           int32_t *status, cudaStream_t stream);
 
 __device__ __forceinline__ float fast_exp2(float x)
 {

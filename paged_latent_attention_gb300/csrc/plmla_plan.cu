@@ -134,6 +134,11 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     // completion before reading the plan
     asm volatile("griddepcontrol.launch_dependents;");
 
+    // finished-segment counters of this call's decode start from zero
+    if (plan.done != nullptr)
+        for (int i = tid; i < plan.n_done; i += kPlanThreads)
+            plan.done[i] = 0;
+
     // ---- split plan (per request)
     long long local_sum = 0;
     int local_max = 0;
