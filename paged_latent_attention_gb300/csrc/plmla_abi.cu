@@ -6,6 +6,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "plmla.h"
 #include "plmla_internal.cuh"
 
@@ -41,9 +43,33 @@ bool shape_ok(int32_t num_reqs, int32_t n_q, int32_t num_heads)
            num_heads >= 16 && num_heads <= 128 && num_heads % 16 == 0;
 }
 
+// The per-device SM speed record (zero-initialised when the module loads).
+__device__ SmCalib g_sm_calib;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_calib_mutex;
+SmCalib *g_calib_ptr[kMaxDevices] = {nullptr};
+
+// Device address of g_sm_calib on the current device, looked up once; null if
+// the lookup fails (the planner then gives every CTA an equal share).
+SmCalib *calib_for_current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(g_calib_mutex);
+    if (g_calib_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_sm_calib) != cudaSuccess)
+            return nullptr;
+        g_calib_ptr[dev] = static_cast<SmCalib *>(ptr);
+    }
+    return g_calib_ptr[dev];
+}
+
 struct WorkspaceLayout {
-    size_t status, indptr, chunk, seg_count, segments, seg_req, seg_member, done, o_part,
-        lse_part, total;
+    size_t status, indptr, chunk, seg_count, segments, seg_req, seg_member, done, claim,
+        o_part, lse_part, total;
     int32_t max_segments;
 };
 
@@ -105,6 +131,8 @@ WorkspaceLayout layout_for(int32_t num_reqs, const Shape &sh)
     off = align_up(off + sizeof(int32_t) * (size_t)(sh.members + 1));
     w.done = off;
     off = align_up(off + sizeof(int32_t) * (size_t)sh.groups * num_reqs);
+    w.claim = off;
+    off = align_up(off + sizeof(int32_t) * (size_t)sh.groups * sh.members);
     const size_t part_rows = (size_t)sh.groups * w.max_segments * sh.group_rows;
     w.o_part = off;
     off = align_up(off + sizeof(float) * part_rows * kLatent);
@@ -243,6 +271,9 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
     plan.seg_member_indptr = reinterpret_cast<int32_t *>(ws + w.seg_member);
     plan.done = reinterpret_cast<int32_t *>(ws + w.done);
     plan.n_done = sh.groups * num_reqs;
+    plan.claim = reinterpret_cast<int32_t *>(ws + w.claim);
+    plan.n_claim = sh.groups * sh.members;
+    plan.calib = calib_for_current_device();
     float *o_part = reinterpret_cast<float *>(ws + w.o_part);
     float *lse_part = reinterpret_cast<float *>(ws + w.lse_part);
 
@@ -278,6 +309,8 @@ extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q
     a.lse_part = lse_part;
     a.status = plan.status;
     a.done = plan.done;
+    a.claim = plan.claim;
+    a.calib = plan.calib;
     err = launch_decode_tc(a, s);
     if (err != cudaSuccess || record(ev.combine_begin, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;

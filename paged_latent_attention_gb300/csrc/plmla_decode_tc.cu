@@ -32,11 +32,14 @@
 // double-buffered in TMEM, so S^T of tile i+1 runs while the softmax of tile i
 // does, and each ring is consumed in order by its own issuer.
 //
-// Warp roles (256 threads): warp 0 = K/Q producer, warp 1 = S^T issuer and
-// TMEM owner, warps 2..5 = softmax (one thread per token lane of S^T; the same
-// threads write the partial output, one thread per latent row of O^T), warp 6
-// = V producer (it also zeroes, in the request's last partial tile, the latent
-// rows past the history before releasing the item), warp 7 = P^T V issuer.
+// Warp roles (384 threads): warp 0 = K/Q producer, warp 1 = S^T issuer and
+// TMEM owner, warps 2..9 = softmax (two warps per TMEM lane quadrant, each with
+// half of a token's query-row columns; the same threads write the partial
+// output, one thread per latent row of O^T and column half), warp 10 = V
+// producer (it also zeroes, in the request's last partial tile, the latent
+// rows past the history before releasing the item), warp 11 = P^T V issuer.
+// Two softmax warps per SM sub-partition keep the dependent softmax arithmetic
+// from exposing its full latency.
 //
 // Online softmax in fp32 with a lagged maximum: the reference maximum m of a
 // row moves only when a score exceeds it by more than kTau (log2 units).  Each
@@ -62,7 +65,10 @@
 namespace plmla {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxWarps = 8;                // warps 2..9: two per TMEM lane quadrant
+constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
+constexpr int kWarpVProducer = 10, kWarpPvIssuer = 11;
 constexpr int kSub = 9;                         // 8 latent column blocks + 1 rope block
 constexpr int kVItems = 8;                      // V items per tile (4 O^T blocks x 2 token halves)
 constexpr int kSubBytes = kTile * 64 * 2;       // one ring slot: 16 KB
@@ -81,7 +87,7 @@ struct Smem {
     static constexpr int q_chunk = NG * 128;                // one 64-column chunk of Q^T
     static constexpr int p_bytes = kTile * 2 * NG;          // P^T, bf16
     static constexpr int bar_bytes = 512;
-    static constexpr int misc_bytes = bar_bytes + 4 * 64 * 4 + 3 * 64 * 4 + 16;
+    static constexpr int misc_bytes = bar_bytes + 4 * 64 * 4 + 3 * 64 * 4 + 32;
     static constexpr int fixed = p_bytes + kSub * q_chunk + misc_bytes + 1024;
     static constexpr int slots_fit = (kMaxDynSmem - fixed) / kSubBytes;
     // half of the slots for each ring
@@ -95,8 +101,8 @@ struct Smem {
     static constexpr int fin_off = red_off + 4 * 64 * 4;     // float fin[64]
     static constexpr int m_off = fin_off + 64 * 4;           // float m[64]   (log2 units)
     static constexpr int al_off = m_off + 64 * 4;            // float alpha[64]
-    static constexpr int misc_off = al_off + 64 * 4;         // tmem addr, abort, need
-    static constexpr int bytes = misc_off + 16;
+    static constexpr int misc_off = al_off + 64 * 4;         // tmem addr, abort, need[2], cta
+    static constexpr int bytes = misc_off + 32;
     static constexpr int alloc = bytes + 1024;               // slack for 1024-B alignment
     static_assert(k_slots >= 2 && v_slots >= 2, "ring depth");
     static_assert(alloc <= kMaxDynSmem, "shared memory budget");
@@ -297,6 +303,22 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]));
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
 {
     asm volatile(
@@ -309,7 +331,66 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Load C consecutive fp32 TMEM columns of this thread's lane (C = 8, 16 or 32).
+template <int C>
+__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float (&v)[C])
+{
+    if constexpr (C % 16 == 0) {
+#pragma unroll
+        for (int b = 0; b < C / 16; ++b) {
+            uint32_t r[16];
+            tmem_ld16(taddr + 16 * b, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                v[16 * b + e] = __uint_as_float(r[e]);
+        }
+    } else {
+        static_assert(C == 8, "column count");
+        uint32_t r[8];
+        tmem_ld8(taddr, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            v[e] = __uint_as_float(r[e]);
+    }
+}
+
+// Multiply C consecutive fp32 TMEM columns of this thread's lane by alpha[col].
+template <int C>
+__device__ __forceinline__ void tmem_scale_cols(uint32_t taddr, uint32_t alpha_addr)
+{
+    if constexpr (C % 16 == 0) {
+#pragma unroll
+        for (int b = 0; b < C / 16; ++b) {
+            uint32_t r[16];
+            tmem_ld16(taddr + 16 * b, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                float al;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(al) : "r"(alpha_addr + 4 * (16 * b + e)));
+                r[e] = __float_as_uint(__uint_as_float(r[e]) * al);
+            }
+            tmem_st16(taddr + 16 * b, r);
+        }
+    } else {
+        static_assert(C == 8, "column count");
+        uint32_t r[8];
+        tmem_ld8(taddr, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            float al;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(al) : "r"(alpha_addr + 4 * e));
+            r[e] = __float_as_uint(__uint_as_float(r[e]) * al);
+        }
+        tmem_st8(taddr, r);
+    }
+}
+
+
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Named barrier over the 128 softmax threads that also ORs a predicate: every
 // thread gets the same answer, so an abort decided here is taken uniformly.
@@ -319,7 +400,7 @@ __device__ __forceinline__ bool softmax_bar_or(bool pred)
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.b32 q, %1, 0;\n\t"
-        "bar.red.or.pred p, 1, 128, q;\n\t"
+        "bar.red.or.pred p, 1, 256, q;\n\t"
         "selp.b32 %0, 1, 0, p;\n\t}"
         : "=r"(res)
         : "r"(pred ? 1u : 0u)
@@ -344,7 +425,7 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // Butterfly reduce-scatter of NG per-lane values across a warp.  Afterwards
 // lane l holds the warp-wide result for columns [l*NG/32, (l+1)*NG/32) when
-// NG >= 32, or for column l/2 when NG == 16.
+// NG >= 32, or for column l / (32/NG) when NG < 32.
 template <int NG, bool kMax>
 __device__ __forceinline__ void warp_reduce_scatter(float (&v)[NG], int lane)
 {
@@ -372,12 +453,15 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[NG], int lane)
 template <int NG>
 __device__ __forceinline__ void scatter_to_red(const float (&v)[NG], float *red_q, int lane)
 {
-    if (NG >= 32) {
+    if constexpr (NG >= 32) {
 #pragma unroll
-        for (int e = 0; e < (NG >= 32 ? NG / 32 : 1); ++e)
+        for (int e = 0; e < NG / 32; ++e)
             red_q[lane * (NG / 32) + e] = v[e];
-    } else if ((lane & 1) == 0) {
-        red_q[lane >> 1] = v[0];
+    } else {
+        // each column's result sits on 32 / NG neighbouring lanes
+        constexpr int rep = 32 / NG;
+        if (lane % rep == 0)
+            red_q[lane / rep] = v[0];
     }
 }
 
@@ -390,15 +474,10 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, float scale_log2, bo
                                             int t, int t_end, int vis_all, int row0, int heads,
                                             float (&x)[NG])
 {
+    tmem_load_cols<NG>(taddr, x);
 #pragma unroll
-    for (int b = 0; b < NG / 16; ++b) {
-        uint32_t r[16];
-        tmem_ld16(taddr + 16 * b, r);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            x[16 * b + e] = __uint_as_float(r[e]) * scale_log2;
-    }
+    for (int c = 0; c < NG; ++c)
+        x[c] *= scale_log2;
     if (!tile_visible) {
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
@@ -477,12 +556,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     float *al_sm = reinterpret_cast<float *>(smem + L::al_off);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
-    volatile int *need_sm = reinterpret_cast<volatile int *>(smem + L::misc_off + 8);
+    volatile int *need_sm = reinterpret_cast<volatile int *>(smem + L::misc_off + 16);   // [2]
+
+    volatile int *cta_index = reinterpret_cast<volatile int *>(smem + L::misc_off + 12);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int team = blockIdx.x / a.members;
-    const int member = blockIdx.x % a.members;
-    const int row0 = team * NG;
     if (threadIdx.x == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_kv)) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_v)) : "memory");
@@ -504,17 +582,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         mbar_init(bar_qe, 1);
         mbar_init(bar_s, 1);
         mbar_init(bar_s + 8, 1);
-        mbar_init(bar_sfree, 128);
-        mbar_init(bar_sfree + 8, 128);
-        mbar_init(bar_p, 128);
+        mbar_init(bar_sfree, kSoftmaxWarps);       // one arrival per softmax warp
+        mbar_init(bar_sfree + 8, kSoftmaxWarps);
+        mbar_init(bar_p, kSoftmaxWarps);
         mbar_init(bar_pv, 1);
-        mbar_init(bar_of, 128);
+        mbar_init(bar_of, kSoftmaxWarps);
         mbar_init(bars + kBarDrainS, 1);
         mbar_init(bars + kBarDrainPv, 1);
         for (int k = 0; k < 4; ++k)
             mbar_init(bars + kBarPvIssued + 8 * k, 1);
         *abort_flag = 0;
-        *need_sm = 0;
+        need_sm[0] = 0;
+        need_sm[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         fence_proxy_async();
     }
@@ -532,6 +611,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     // everything above overlaps the plan kernel (programmatic dependent launch);
     // the schedule is read only once that grid has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Take the CTA index equal to this SM's id when it is free, so that the
+    // planner's speed-scaled share for that SM is the one this CTA runs; else
+    // the first free index (each of the grid's CTAs ends up with a distinct one).
+    uint32_t sm_id;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_id));
+    const unsigned long long t_start = global_ns();
+    if (threadIdx.x == 0) {
+        const int total = a.members * a.num_groups;
+        int c = -1;
+        if ((int)sm_id < total && atomicCAS(a.claim + sm_id, 0, 1) == 0)
+            c = (int)sm_id;
+        for (int k = 0; c < 0 && k < total; ++k)
+            if (atomicCAS(a.claim + k, 0, 1) == 0)
+                c = k;
+        *cta_index = c;
+    }
+    __syncthreads();
+    const int cta = *cta_index;
+    const int team = cta / a.members;
+    const int member = cta % a.members;
+    const int row0 = team * NG;
     const int seg_begin = a.seg_member_indptr[member];
     const int seg_end = a.seg_member_indptr[member + 1];   // empty range: no work
     const int seg_total = *a.seg_count;
@@ -595,7 +695,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             for (int it = issued > NK ? issued - NK : 0; it < issued; ++it)
                 wait_drain(bar_full_k + 8 * (it % NK), (uint32_t)(it / NK) & 1u);
         }
-    } else if (warp == 6) {
+    } else if (warp == kWarpVProducer) {
         // ---------------------------------------------------------- V producer
         // V item v of a tile = latent block v / 2 (128 columns), token half v % 2.
         // Items of a partial tile land on bar_vtmp first; the warp zeroes the
@@ -749,7 +849,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 wait_drain(bars + kBarDrainS, 0);
             }
         }
-    } else if (warp == 7) {
+    } else if (warp == kWarpPvIssuer) {
         // ----------------------------------------------------- P^T V issuer
         if (lane == 0) {
             bool issued = false, ok = true;
@@ -810,11 +910,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         }
     } else {
         // ------------------------------------------------------------- softmax
-        const int q = warp & 3;                 // TMEM lane quadrant of this warp
+        // warp w in 2..9: TMEM lane quadrant w % 4 (tokens of S^T, latent rows of
+        // O^T), columns [h*CH, (h+1)*CH) of the NG query rows, h = (w - 2) / 4
+        constexpr int CH = NG / 2;
+        const int q = warp & 3;
+        const int h = (warp - 2) >> 2;
+        const int col0 = h * CH;
         const int tok = 32 * q + lane;          // token lane of S^T / latent row of O^T
-        const int st = threadIdx.x - 64;        // 0..127
+        const int st = threadIdx.x - 64;        // 0..255
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
-        const uint32_t m_addr = smem_u32(m_sm);
+        const uint32_t m_addr = smem_u32(m_sm) + 4 * col0;
+        const uint32_t al_addr = smem_u32(al_sm) + 4 * col0;
         bool ok = true;
         int gt = 0;
         for (int s = seg_begin; s < seg_end && ok; ++s) {
@@ -825,12 +931,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             const int vis_all = Lr - (a.n_q - 1);   // tokens below this are visible to every row
             if (local > 0)
                 softmax_bar();                       // previous epilogue is done with m_sm
-            for (int c = st; c < NG; c += 128)
+            for (int c = st; c < NG; c += kSoftmaxThreads)
                 m_sm[c] = -INFINITY;
             softmax_bar();
-            float lsum[NG];
+            float lsum[CH];
 #pragma unroll
-            for (int c = 0; c < NG; ++c)
+            for (int c = 0; c < CH; ++c)
                 lsum[c] = 0.f;
 
             for (int i = 0; i < n_tiles; ++i, ++gt) {
@@ -838,17 +944,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 const int t = t_base + tok;
                 const bool tile_visible = t_base + kTile <= vis_all;
                 const uint32_t b = gt & 1;
-                const uint32_t s_col = kTmemS + 64 * b;
+                const uint32_t s_col = kTmemS + 64 * b + col0;
                 // warp-uniform, because tcgen05.ld below is a .sync.aligned instruction
                 const bool got = __all_sync(
                     0xffffffffu, wait_bounded(bar_s + 8 * b, (gt >> 1) & 1, abort_flag, a.status, 7));
-                float x[NG];
+                float x[CH];
                 bool exceed = false;
                 if (got) {
                     tc_fence_after();
-                    load_scores<NG>(tmem + t_lane + s_col, a.scale_log2, tile_visible, t, seg.z,
-                                    vis_all, row0, a.num_heads, x);
-                    exceed = shift_and_test<NG>(x, m_addr);
+                    load_scores<CH>(tmem + t_lane + s_col, a.scale_log2, tile_visible, t, seg.z,
+                                    vis_all, row0 + col0, a.num_heads, x);
+                    exceed = shift_and_test<CH>(x, m_addr);
                 }
                 if (softmax_bar_or(exceed || !got || *abort_flag)) {
                     // rare: a score exceeds its reference maximum (always on a segment's
@@ -857,12 +963,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                         ok = false;
                         break;
                     }
-                    warp_reduce_scatter<NG, true>(x, lane);
-                    scatter_to_red<NG>(x, red + 64 * q, lane);
+                    warp_reduce_scatter<CH, true>(x, lane);
+                    scatter_to_red<CH>(x, red + 64 * q + col0, lane);
                     softmax_bar();
                     if (q == 0) {
+                        // one warp per column half: new reference maxima and factors
                         bool any = false;
-                        for (int c = lane; c < NG; c += 32) {
+                        if (lane < CH) {
+                            const int c = col0 + lane;
                             const float mu = m_sm[c];
                             // the scores were shifted by mu (0 while unset): back to absolute
                             const float mx = fmaxf(fmaxf(red[c], red[64 + c]),
@@ -879,57 +987,47 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                                 }
                             }
                             al_sm[c] = alpha;
-                            any |= alpha != 1.f;
+                            any = alpha != 1.f;
                         }
                         any = __any_sync(0xffffffffu, any);
                         if (lane == 0)
-                            *need_sm = any ? 1 : 0;
+                            need_sm[h] = any ? 1 : 0;
                     }
                     softmax_bar();
-                    if (*need_sm != 0) {
-                        const uint32_t al_addr = smem_u32(al_sm);
+                    if (need_sm[h] != 0) {
 #pragma unroll
-                        for (int c = 0; c < NG; ++c)
+                        for (int c = 0; c < CH; ++c)
                             lsum[c] *= ld_shared_f32(al_addr + 4 * c);
-                        if (i > 0) {
-                            // O^T columns are rescaled once the previous P^T V is done
-                            const bool done = wait_bounded(bar_pv, (gt - 1) & 1, abort_flag,
-                                                           a.status, 8);
-                            if (softmax_bar_or(!done)) {
-                                ok = false;
-                                break;
-                            }
+                    }
+                    if (i > 0 && (need_sm[0] | need_sm[1]) != 0) {
+                        // O^T columns are rescaled once the previous P^T V is done
+                        const bool done =
+                            wait_bounded(bar_pv, (gt - 1) & 1, abort_flag, a.status, 8);
+                        if (softmax_bar_or(!done)) {
+                            ok = false;
+                            break;
+                        }
+                        if (need_sm[h] != 0) {
                             tc_fence_after();
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-#pragma unroll
-                                for (int bb = 0; bb < NG / 16; ++bb) {
-                                    uint32_t r[16];
-                                    const uint32_t ta = tmem + t_lane + 64 * j + 16 * bb;
-                                    tmem_ld16(ta, r);
-                                    tmem_wait_ld();
-#pragma unroll
-                                    for (int e = 0; e < 16; ++e)
-                                        r[e] = __float_as_uint(
-                                            __uint_as_float(r[e]) *
-                                            ld_shared_f32(al_addr + 4 * (16 * bb + e)));
-                                    tmem_st16(ta, r);
-                                }
-                            }
+                            for (int j = 0; j < 4; ++j)
+                                tmem_scale_cols<CH>(tmem + t_lane + 64 * j + col0, al_addr);
                             tmem_wait_st();
                         }
                     }
-                    load_scores<NG>(tmem + t_lane + s_col, a.scale_log2, tile_visible, t, seg.z,
-                                    vis_all, row0, a.num_heads, x);
-                    shift_and_test<NG>(x, m_addr);
+                    load_scores<CH>(tmem + t_lane + s_col, a.scale_log2, tile_visible, t, seg.z,
+                                    vis_all, row0 + col0, a.num_heads, x);
+                    shift_and_test<CH>(x, m_addr);
                 }
                 // this S^T buffer may now be overwritten by the tile after next
                 tc_fence_before();
-                mbar_arrive(bar_sfree + 8 * b);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar_sfree + 8 * b);
                 // probabilities 2^(x - m) (x is already shifted) and running sums
-                uint32_t pk[NG / 2];
+                uint32_t pk[CH / 2];
 #pragma unroll
-                for (int c = 0; c < NG; c += 2) {
+                for (int c = 0; c < CH; c += 2) {
                     const float p0 = fast_exp2(x[c]);        // 2^-inf = 0
                     const float p1 = fast_exp2(x[c + 1]);
                     lsum[c] += p0;
@@ -946,11 +1044,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     }
                 }
                 {
+                    // this token's row of P^T (2*NG bytes, 16-byte chunks swizzled
+                    // like the MMA operand); this thread writes its column half
                     constexpr int row_bytes = 2 * NG;
                     constexpr int swz_bits = NG == 64 ? 3 : (NG == 32 ? 2 : 1);
+                    constexpr int chunks = CH * 2 / 16;
 #pragma unroll
-                    for (int ch = 0; ch < row_bytes / 16; ++ch) {
-                        const uint32_t off = (uint32_t)(tok * row_bytes + 16 * ch);
+                    for (int ch = 0; ch < chunks; ++ch) {
+                        const uint32_t off = (uint32_t)(tok * row_bytes + h * CH * 2 + 16 * ch);
                         const uint32_t sw = off ^ (((off >> 7) & ((1u << swz_bits) - 1u)) << 4);
                         st_shared_v4(s_p + sw, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
                                      pk[4 * ch + 3]);
@@ -958,7 +1059,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 }
                 fence_proxy_async();
                 tc_fence_before();
-                mbar_arrive(bar_p);
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(bar_p);
             }
             if (!ok)
                 break;
@@ -970,44 +1073,38 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 break;
             }
             tc_fence_after();
-            warp_reduce_scatter<NG, false>(lsum, lane);
-            scatter_to_red<NG>(lsum, red + 64 * q, lane);
+            warp_reduce_scatter<CH, false>(lsum, lane);
+            scatter_to_red<CH>(lsum, red + 64 * q + col0, lane);
             softmax_bar();
-            if (q == 0) {
-                for (int c = lane; c < NG; c += 32) {
-                    const float l = red[c] + red[64 + c] + red[128 + c] + red[192 + c];
-                    fin[c] = l > 0.f ? 1.f / l : 0.f;   // 1 / row sum (0 for an empty row)
-                    a.lse_part[(int64_t)(team * seg_total + s) * NG + c] =
-                        l > 0.f ? (m_sm[c] + log2f(l)) * kLn2 : -INFINITY;
-                }
+            if (q == 0 && lane < CH) {
+                const int c = col0 + lane;
+                const float l = red[c] + red[64 + c] + red[128 + c] + red[192 + c];
+                fin[c] = l > 0.f ? 1.f / l : 0.f;   // 1 / row sum (0 for an empty row)
+                a.lse_part[(int64_t)(team * seg_total + s) * NG + c] =
+                    l > 0.f ? (m_sm[c] + log2f(l)) * kLn2 : -INFINITY;
             }
             softmax_bar();
             // normalised partial output: thread = latent row of each O^T block;
-            // for a fixed row the 128 threads store 512 contiguous bytes
-            const uint32_t inv_addr = smem_u32(fin);
-            float *out0 = a.o_part + (int64_t)(team * seg_total + s) * NG * kLatent + tok;
+            // for a fixed row the 128 threads of a column half store 512
+            // contiguous bytes
+            const uint32_t inv_addr = smem_u32(fin) + 4 * col0;
+            float *out0 = a.o_part + ((int64_t)(team * seg_total + s) * NG + col0) * kLatent + tok;
+            float inv[CH];
 #pragma unroll
-            for (int bb = 0; bb < NG / 16; ++bb) {
-                float inv[16];
+            for (int c = 0; c < CH; ++c)
+                inv[c] = ld_shared_f32(inv_addr + 4 * c);
 #pragma unroll
-                for (int e4 = 0; e4 < 16; e4 += 4)
-                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                                 : "=f"(inv[e4]), "=f"(inv[e4 + 1]), "=f"(inv[e4 + 2]),
-                                   "=f"(inv[e4 + 3])
-                                 : "r"(inv_addr + 4 * (16 * bb + e4)));
+            for (int j = 0; j < 4; ++j) {
+                float o[CH];
+                tmem_load_cols<CH>(tmem + t_lane + 64 * j + col0, o);
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t r[16];
-                    tmem_ld16(tmem + t_lane + 64 * j + 16 * bb, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        out0[(int64_t)(16 * bb + e) * kLatent + 128 * j] =
-                            __uint_as_float(r[e]) * inv[e];
-                }
+                for (int c = 0; c < CH; ++c)
+                    out0[(int64_t)c * kLatent + 128 * j] = o[c] * inv[c];
             }
             tc_fence_before();
-            mbar_arrive(bar_of);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar_of);
             // publish the segment: every thread's stores, then one counter update
             __threadfence();
             softmax_bar();
@@ -1022,6 +1119,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols));
+    }
+    if (threadIdx.x == 0 && a.calib != nullptr && (int)sm_id < kMaxSms && *abort_flag == 0 &&
+        a.calib->cost[sm_id] < kCalibCost) {
+        // this SM's speed in the planner's cost units, from calls with real work
+        float cost = 0.f;
+        for (int s = seg_begin; s < seg_end; ++s) {
+            const int4 seg = a.segments[s];
+            cost += (float)((seg.z - seg.y + kTile - 1) / kTile + (seg.y == 0 ? 2 : 0));
+        }
+        if (cost >= kCalibMinCost) {
+            atomicAdd(&a.calib->time_ns[sm_id], (float)(global_ns() - t_start));
+            atomicAdd(&a.calib->cost[sm_id], cost);
+        }
     }
 }
 

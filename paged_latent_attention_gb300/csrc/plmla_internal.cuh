@@ -18,6 +18,23 @@ constexpr int kMaxNq = 16;
 constexpr int kMaxPlanSplits = 4096;  // chunks the device planner can schedule
 constexpr int kChunksPerMember = 16;  // default chunk budget per persistent CTA
 
+constexpr int kMaxSms = 256;            // SM ids the speed record covers
+constexpr float kCalibCost = 192.f;     // cost units an SM measures before its speed is used
+constexpr float kCalibMinCost = 16.f;   // a call adds to the record only with this much work
+
+// Per-device record of how fast each SM works through the decode: cost units
+// (tiles plus a charge per request start, the planner's unit) and active time,
+// summed over calls in which the SM's CTA had at least kCalibMinCost of work,
+// until kCalibCost units are measured.  SMs of one chip run the same code at
+// repeatably different speeds (some TPCs sit closer to their GPC's crossbar
+// port, some GPCs have fewer TPCs), so once every SM of the grid is measured
+// the planner gives each CTA a share of the work proportional to its SM's
+// speed; until then, and for ever after, the shares are fixed.
+struct SmCalib {
+    float cost[kMaxSms];
+    float time_ns[kMaxSms];
+};
+
 struct PlanBuffers {
     int32_t *status;            // [1] device status word, reset to 0 by the plan kernel
     int32_t *indptr;            // [R + 1] per-request chunk counts, prefix-summed
@@ -29,6 +46,9 @@ struct PlanBuffers {
     int32_t *seg_member_indptr; // [members + 1] segments of member k: [k], [k + 1]
     int32_t *done;              // [n_done] finished-segment counters, zeroed by the plan kernel
     int32_t n_done;
+    int32_t *claim;             // [n_claim] CTA-index claims of the decode grid, zeroed here
+    int32_t n_claim;
+    SmCalib *calib;             // per-device speed record (null: equal shares)
 };
 
 struct DecodeArgs {
@@ -53,6 +73,8 @@ struct DecodeArgs {
     float *lse_part;               // [groups * S, group_rows], natural log
     int32_t *status;               // device status word (0 = ok, else the failed wait)
     int32_t *done;                 // [groups * R] segments of (team, request) written
+    int32_t *claim;                // [groups * members] CTA indices taken (zeroed by the plan)
+    SmCalib *calib;                // per-device speed record, or null
 };
 
 // Largest of 64, 32, 16 that divides `rows`, or 0.

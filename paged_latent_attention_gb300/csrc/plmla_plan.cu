@@ -10,10 +10,11 @@
 //
 // Schedule (the GB300 side): the decode kernel runs one persistent CTA per SM.
 // The chunks, in request order, are dealt out as contiguous runs so that every
-// CTA ("member") gets the same cost up to half a chunk, cost counted in
+// CTA ("member") gets its share of the cost up to half a chunk, cost counted in
 // 128-token tiles plus a fixed charge for each request's first chunk (starting
-// a segment): chunk i goes to member floor((cost before i + cost of i / 2) *
-// members / total cost).  Consecutive chunks of one request that land on one member form
+// a segment): chunk i goes to the member whose share holds the chunk's cost
+// midpoint (cost before i + cost of i / 2).  Shares are equal until the decode
+// has measured each SM's speed (SmCalib), then proportional to it.  Consecutive chunks of one request that land on one member form
 // a segment, which the CTA processes without writing an intermediate partial
 // state.  Every row group of the queries repeats the same schedule on its own
 // team of members, so teams read the same KV tiles at about the same time.
@@ -121,6 +122,9 @@ struct PlanSmem {
     int red32[kPlanThreads / 32];
     int cand_k[kPlanThreads / 32];
     int cand_fits[kPlanThreads / 32];
+    float wprefix[kMaxSms + 1];     // inclusive prefix of member weights (speed-scaled shares)
+    float wrun[kMaxSms];
+    int weighted;                   // 1 when wprefix holds measured weights
 };
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
@@ -134,10 +138,13 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     // completion before reading the plan
     asm volatile("griddepcontrol.launch_dependents;");
 
-    // finished-segment counters of this call's decode start from zero
+    // finished-segment counters and CTA claims of this call's decode start from zero
     if (plan.done != nullptr)
         for (int i = tid; i < plan.n_done; i += kPlanThreads)
             plan.done[i] = 0;
+    if (plan.claim != nullptr)
+        for (int i = tid; i < plan.n_claim; i += kPlanThreads)
+            plan.claim[i] = 0;
 
     // ---- split plan (per request)
     long long local_sum = 0;
@@ -216,6 +223,67 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
         return;
     }
 
+    // ---- member shares: CTA c of the decode grid runs on the SM with id c when
+    // it can (it claims that index), so once every such SM's speed is measured,
+    // member m of every team gets a share of the cost proportional to the mean
+    // speed of SMs team*members + m; until then the shares are equal
+    {
+        const SmCalib *cal = plan.calib;
+        const int n_cta = plan.n_claim;
+        const int teams = n_cta / max(members, 1);
+        const bool usable = cal != nullptr && teams >= 1 && n_cta <= kMaxSms;
+        float rate = 0.f;
+        bool measured = true;
+        if (usable && tid < n_cta) {
+            const float c = cal->cost[tid], t = cal->time_ns[tid];
+            measured = c >= kCalibCost && t > 0.f;
+            rate = measured ? c / t : 0.f;
+            sm.wprefix[tid + 1] = rate;              // per-CTA rate, reduced below
+        }
+        const int ready = __syncthreads_and(usable && measured);
+        if (ready) {
+            // member rate (mean over teams), then an inclusive prefix in warp 0:
+            // lane l owns members [8l, 8l + 8)
+            if (tid < members) {
+                float r = 0.f;
+                for (int g = 0; g < teams; ++g)
+                    r += sm.wprefix[g * members + tid + 1];
+                sm.wrun[tid] = r / teams;
+            }
+            __syncthreads();
+            if (tid < 32) {
+                constexpr int per = kMaxSms / 32;
+                float loc[per];
+                float run = 0.f;
+#pragma unroll
+                for (int i = 0; i < per; ++i) {
+                    const int m = tid * per + i;
+                    run += m < members ? sm.wrun[m] : 0.f;
+                    loc[i] = run;
+                }
+                float incl = run;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float up = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (tid >= o)
+                        incl += up;
+                }
+                const float off = incl - run;
+#pragma unroll
+                for (int i = 0; i < per; ++i) {
+                    const int m = tid * per + i;
+                    if (m < members)
+                        sm.wprefix[m + 1] = off + loc[i];
+                }
+                if (tid == 0)
+                    sm.wprefix[0] = 0.f;
+            }
+        }
+        if (tid == 0)
+            sm.weighted = ready ? 1 : 0;
+        __syncthreads();
+    }
+
     // ---- schedule: chunks in request order, dealt to members by cost
     for (int i = tid; i < n_splits; i += kPlanThreads) {
         // request of chunk i: the last r with split_base[r] <= i
@@ -243,10 +311,26 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     __syncthreads();
     const int total_tiles = block_exclusive_scan(sm.sp_tiles, n_splits, sm.red32);
     for (int i = tid; i < n_splits; i += kPlanThreads) {
-        // midpoint of chunk i in cost units, times members, over twice the total
+        // midpoint of chunk i as a fraction of the total cost
         const long long mid2 = 2LL * sm.sp_tiles[i] + sm.sp_member[i];  // 2*prefix + cost
-        const float pos = (float)mid2 * (float)members / (2.f * (float)max(total_tiles, 1));
-        sm.sp_member[i] = min(members - 1, (int)pos);
+        const float frac = (float)mid2 / (2.f * (float)max(total_tiles, 1));
+        int m;
+        if (sm.weighted) {
+            // the member whose share [wprefix[m], wprefix[m + 1]) holds the midpoint
+            const float target = frac * sm.wprefix[members];
+            int lo = 0, hi = members - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (sm.wprefix[mid] <= target)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            m = lo;
+        } else {
+            m = (int)(frac * (float)members);
+        }
+        sm.sp_member[i] = min(members - 1, max(0, m));
     }
     __syncthreads();
     for (int i = tid; i < n_splits; i += kPlanThreads)
