@@ -78,8 +78,11 @@ const char *mla_strerror(plmla_status status);
  *   budget     = max(16 * members, num_reqs * min_splits_per_req), at most 4096
  *
  * mla_decode runs row_groups x members persistent CTAs; each takes a contiguous,
- * tile-balanced run of the chunks.  Returns the budget, or -1 for invalid
- * arguments, a budget above 4096, or no CUDA device when cta_budget == 0.
+ * cost-balanced run of the chunks (equal shares until the library has measured
+ * the speed of each SM over a few calls with real work, then shares in
+ * proportion to it, fixed from then on).  Returns the budget, or -1 for invalid
+ * arguments, members above 256, a budget above 4096, or no CUDA device when
+ * cta_budget == 0.
  */
 int32_t mla_split_budget(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_budget,
                          int32_t min_splits_per_req);

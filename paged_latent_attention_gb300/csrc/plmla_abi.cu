@@ -93,6 +93,8 @@ bool shape_for(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_bud
     if (slots <= 0)
         return false;
     sh.members = (int32_t)(slots / sh.groups > 0 ? slots / sh.groups : 1);
+    if (sh.members > kMaxSms)   // the schedule keeps per-member tables of kMaxSms entries
+        return false;
     int64_t budget = (int64_t)kChunksPerMember * sh.members;
     const int64_t wanted = (int64_t)num_reqs * min_splits;
     if (wanted > budget)

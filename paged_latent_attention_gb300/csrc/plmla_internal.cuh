@@ -33,6 +33,10 @@ constexpr float kCalibMinCost = 16.f;   // a call adds to the record only with t
 struct SmCalib {
     float cost[kMaxSms];
     float time_ns[kMaxSms];
+    // the planner's member weight prefix for one grid shape, computed once all
+    // of that grid's SMs are measured (their records no longer change)
+    int32_t cache_members, cache_teams;
+    float cache_wprefix[kMaxSms + 1];
 };
 
 struct PlanBuffers {

@@ -5,19 +5,24 @@
 // history and a parallelism budget, and each request gets as many chunks as its
 // own history needs.  chunk = ceil(sum L / budget) rounded up to kTile; if the
 // chunks do not fit the budget, chunk grows (the smallest multiple of kTile
-// that fits, found by a 32-way parallel search because the chunk count only falls as the
-// chunk grows), never beyond the longest history rounded up to kTile.
+// that fits, found by a parallel search because the chunk count only falls as
+// the chunk grows), never beyond the longest history rounded up to kTile.
 //
 // Schedule (the GB300 side): the decode kernel runs one persistent CTA per SM.
 // The chunks, in request order, are dealt out as contiguous runs so that every
 // CTA ("member") gets its share of the cost up to half a chunk, cost counted in
 // 128-token tiles plus a fixed charge for each request's first chunk (starting
-// a segment): chunk i goes to the member whose share holds the chunk's cost
-// midpoint (cost before i + cost of i / 2).  Shares are equal until the decode
-// has measured each SM's speed (SmCalib), then proportional to it.  Consecutive chunks of one request that land on one member form
-// a segment, which the CTA processes without writing an intermediate partial
-// state.  Every row group of the queries repeats the same schedule on its own
-// team of members, so teams read the same KV tiles at about the same time.
+// a segment): a chunk goes to the member whose share holds the chunk's cost
+// midpoint (cost before it + half its cost).  Shares are equal until the decode
+// has measured each SM's speed (SmCalib), then proportional to it.  The chunks
+// of one request all have the same length (the last may be shorter), so the
+// cost before any chunk has a closed form from a per-request prefix, and each
+// member's chunk range comes from a binary search over requests, without a
+// per-chunk table.  Consecutive chunks of one request that land on one member
+// form a segment, which the CTA processes without writing an intermediate
+// partial state.  Every row group of the queries repeats the same schedule on
+// its own team of members, so teams read the same KV tiles at about the same
+// time.
 //
 // Everything is computed on the device from seq_lens, so a decode step never
 // waits for the host and a captured CUDA graph stays valid as histories grow
@@ -28,104 +33,136 @@
 namespace plmla {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 256;
+constexpr int kPlanWarps = kPlanThreads / 32;
+constexpr int kReqPerThread = kMaxReqs / kPlanThreads;   // thread t owns requests [4t, 4t + 4)
 constexpr int kSegmentCostTiles = 2;
-constexpr int kScanPerThread = kMaxPlanSplits / kPlanThreads;
 
-__device__ __forceinline__ long long ceil_div_ll(long long a, long long b)
-{
-    return (a + b - 1) / b;
-}
+struct PlanSmem {
+    int lens[kMaxReqs];
+    int sb[kMaxReqs + 1];        // exclusive prefix of chunks per request (split base)
+    int cost0[kMaxReqs + 1];     // exclusive prefix of request cost (tiles + start charge)
+    int lastm[kMaxReqs];         // running max of each request's last-chunk doubled midpoint
+    int nonempty[kMaxReqs + 1];  // exclusive prefix of requests with at least one chunk
+    int first[kMaxSms + 1];      // first chunk of each member (members + 1 entries)
+    int nseg[kMaxSms + 1];       // exclusive prefix of segments per member
+    float wprefix[kMaxSms + 1];  // inclusive prefix of member weights
+    float wrate[kMaxSms];        // measured rate of each CTA index
+    long long red64[kPlanWarps];
+    int red32[kPlanWarps];
+    int cand_k[kPlanWarps];
+    int cand_fits[kPlanWarps];
+    int weighted;
+};
 
-template <typename T>
-__device__ T block_sum(T v, T *red)
+// Block-wide sum / max of one value per thread; every thread gets the result.
+__device__ long long block_sum64(long long v, long long *red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         v += __shfl_xor_sync(0xffffffffu, v, o);
-    __syncthreads();
     if (lane == 0)
         red[warp] = v;
     __syncthreads();
-    T total = 0;
-    for (int w = 0; w < kPlanThreads / 32; ++w)
-        total += red[w];
-    return total;
+    long long t = 0;
+#pragma unroll
+    for (int w = 0; w < kPlanWarps; ++w)
+        t += red[w];
+    __syncthreads();
+    return t;
 }
 
-__device__ int block_max_int(int v, int *red)
+__device__ int block_max32(int v, int *red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncthreads();
     if (lane == 0)
         red[warp] = v;
     __syncthreads();
     int m = 0;
-    for (int w = 0; w < kPlanThreads / 32; ++w)
+#pragma unroll
+    for (int w = 0; w < kPlanWarps; ++w)
         m = max(m, red[w]);
+    __syncthreads();
     return m;
 }
 
-// Exclusive prefix sum of vals[0..n) in place (n <= kMaxPlanSplits); returns the total.
-__device__ int block_exclusive_scan(int *vals, int n, int *red)
+// Exclusive block scan (sum) of one value per thread, in thread order; the
+// block total goes to *total.
+__device__ int block_scan_excl(int v, int *red, int *total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int base = threadIdx.x * kScanPerThread;
-    int local[kScanPerThread];
-    int run = 0;
-#pragma unroll
-    for (int i = 0; i < kScanPerThread; ++i) {
-        const int v = (base + i < n) ? vals[base + i] : 0;
-        local[i] = run;
-        run += v;
-    }
-    int incl = run;
+    int incl = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int up = __shfl_up_sync(0xffffffffu, incl, o);
         if (lane >= o)
             incl += up;
     }
-    __syncthreads();
     if (lane == 31)
         red[warp] = incl;
     __syncthreads();
-    int warp_off = 0, total = 0;
-    for (int w = 0; w < kPlanThreads / 32; ++w) {
-        if (w < warp)
-            warp_off += red[w];
-        total += red[w];
-    }
-    const int thread_off = warp_off + incl - run;
+    int off = 0, t = 0;
 #pragma unroll
-    for (int i = 0; i < kScanPerThread; ++i)
-        if (base + i < n)
-            vals[base + i] = thread_off + local[i];
+    for (int w = 0; w < kPlanWarps; ++w) {
+        off += w < warp ? red[w] : 0;
+        t += red[w];
+    }
     __syncthreads();
-    return total;
+    *total = t;
+    return off + incl - v;
 }
 
-struct PlanSmem {
-    int lens[kMaxReqs];
-    int split_base[kMaxReqs];
-    int sp_req[kMaxPlanSplits];
-    int sp_t0[kMaxPlanSplits];
-    int sp_t1[kMaxPlanSplits];
-    int sp_tiles[kMaxPlanSplits];   // tiles of each chunk, then their exclusive prefix
-    int sp_member[kMaxPlanSplits];
-    int sp_seg[kMaxPlanSplits];     // segment-start flag, then the segment id
-    long long red64[kPlanThreads / 32];
-    int red32[kPlanThreads / 32];
-    int cand_k[kPlanThreads / 32];
-    int cand_fits[kPlanThreads / 32];
-    float wprefix[kMaxSms + 1];     // inclusive prefix of member weights (speed-scaled shares)
-    float wrun[kMaxSms];
-    int weighted;                   // 1 when wprefix holds measured weights
-};
+// Exclusive block scan (max, identity -1) of one value per thread.
+__device__ int block_scan_max_excl(int v, int *red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int up = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl = max(incl, up);
+    }
+    int excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0)
+        excl = -1;
+    if (lane == 31)
+        red[warp] = incl;
+    __syncthreads();
+    int off = -1;
+#pragma unroll
+    for (int w = 0; w < kPlanWarps; ++w)
+        off = w < warp ? max(off, red[w]) : off;
+    __syncthreads();
+    return max(off, excl);
+}
+
+// Number of chunks of length c (a multiple of kTile, below 2^31) the requests
+// need, counted by one warp and saturated at cap + 1.
+__device__ int warp_chunk_count(const int *lens, int num_reqs, unsigned c, int cap)
+{
+    const int lane = threadIdx.x & 31;
+    int cnt = 0;
+    for (int r = lane; r < num_reqs; r += 32)
+        cnt = min(cnt + (int)(((unsigned)lens[r] + c - 1u) / c), cap + 1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        cnt = min(cnt + __shfl_xor_sync(0xffffffffu, cnt, o), cap + 1);
+    return cnt;
+}
+
+// Doubled cost midpoint of chunk s of a request whose cost prefix is `cost0`
+// and which has `tiles` tiles: the first chunk carries the segment charge.
+__device__ __forceinline__ int chunk_mid2(int cost0, int tiles, int chunk_tiles, int s)
+{
+    const int t = min(chunk_tiles, tiles - s * chunk_tiles);
+    return s == 0 ? 2 * cost0 + t + kSegmentCostTiles
+                  : 2 * cost0 + 2 * kSegmentCostTiles + 2 * s * chunk_tiles + t;
+}
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int members,
@@ -133,11 +170,36 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
 {
     extern __shared__ __align__(16) unsigned char plan_smem_raw[];
     PlanSmem &sm = *reinterpret_cast<PlanSmem *>(plan_smem_raw);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // the decode kernel may start its prologue now; it waits for this grid's
     // completion before reading the plan
     asm volatile("griddepcontrol.launch_dependents;");
 
+    // ---- histories
+    const int r0 = tid * kReqPerThread;
+    int L[kReqPerThread];
+    long long local_sum = 0;
+    int local_max = 0;
+#pragma unroll
+    for (int k = 0; k < kReqPerThread; ++k) {
+        const int r = r0 + k;
+        L[k] = r < num_reqs ? max(0, seq_lens[r]) : 0;
+        if (r < num_reqs)
+            sm.lens[r] = L[k];
+        local_sum += L[k];
+        local_max = max(local_max, L[k]);
+    }
+    // cached member weights for this grid shape (loaded early, used later)
+    const SmCalib *cal = plan.segments != nullptr ? plan.calib : nullptr;
+    const int n_cta = plan.n_claim;
+    const int teams = n_cta / max(members, 1);
+    int cache_hit = 0;
+    float cached_w = 0.f;
+    if (cal != nullptr) {
+        cache_hit = cal->cache_members == members && cal->cache_teams == teams;
+        if (tid <= kMaxSms)
+            cached_w = cal->cache_wprefix[tid];
+    }
     // finished-segment counters and CTA claims of this call's decode start from zero
     if (plan.done != nullptr)
         for (int i = tid; i < plan.n_done; i += kPlanThreads)
@@ -145,47 +207,29 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     if (plan.claim != nullptr)
         for (int i = tid; i < plan.n_claim; i += kPlanThreads)
             plan.claim[i] = 0;
+    const long long total = block_sum64(local_sum, sm.red64);   // also publishes sm.lens
+    const int longest_len = block_max32(local_max, sm.red32);
 
-    // ---- split plan (per request)
-    long long local_sum = 0;
-    int local_max = 0;
-    for (int r = tid; r < num_reqs; r += kPlanThreads) {
-        const int L = max(0, seq_lens[r]);
-        sm.lens[r] = L;
-        local_sum += L;
-        local_max = max(local_max, L);
-    }
-    __syncthreads();
-    const long long total = block_sum<long long>(local_sum, sm.red64);
-    const int longest_len = block_max_int(local_max, sm.red32);
-
+    // ---- chunk length
     long long chunk = kTile;
     if (total > 0) {
-        const long long c0 = ceil_div_ll(ceil_div_ll(total, budget), kTile) * kTile;
-        const long long longest = ceil_div_ll(longest_len, kTile) * kTile;
+        const long long c0 = (((total + budget - 1) / budget + kTile - 1) / kTile) * kTile;
+        const long long longest = ((longest_len + kTile - 1) / (long long)kTile) * kTile;
         chunk = c0;
-        if (c0 < longest) {
-            // smallest k in [0, K] with count(c0 + k*kTile) <= budget, else K;
-            // count only falls as the chunk grows, so each round splits [lo, hi]
-            // into 32 parts, one candidate per warp.  32-bit arithmetic only:
-            // histories and chunks are below 2^31, and a count is only compared
-            // with the budget, so it saturates at budget + 1.
-            int lo = 0, hi = (int)((longest - c0) / kTile);
+        // c0 usually fits the budget already; otherwise the smallest k in
+        // [1, K] with count(c0 + k*kTile) <= budget (K if none): the count only
+        // falls as the chunk grows, so each round splits [lo, hi] into
+        // kPlanWarps + 1 parts, one candidate per warp.  Histories and chunks
+        // are below 2^31, and a count is only compared with the budget, so it
+        // saturates at budget + 1.
+        if (c0 < longest && warp_chunk_count(sm.lens, num_reqs, (unsigned)c0, budget) > budget) {
+            int lo = 1, hi = (int)((longest - c0) / kTile);
             const unsigned c0u = (unsigned)c0;
-            const int lane = tid & 31, warp = tid >> 5;
             while (lo < hi) {
                 const int span = hi - lo;
-                const int k = lo + (int)(((long long)span * (warp + 1)) / 33);   // in [lo, hi)
-                const unsigned c = c0u + (unsigned)k * kTile;
-                int cnt = 0;
-                for (int r = lane; r < num_reqs; r += 32) {
-                    const unsigned L = (unsigned)sm.lens[r];
-                    cnt = min(cnt + (int)((L + c - 1u) / c), budget + 1);
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    cnt = min(cnt + __shfl_xor_sync(0xffffffffu, cnt, o), budget + 1);
-                __syncthreads();
+                const int k = lo + (int)(((long long)span * (warp + 1)) / (kPlanWarps + 1));
+                const int cnt = warp_chunk_count(sm.lens, num_reqs, c0u + (unsigned)k * kTile,
+                                                 budget);
                 if (lane == 0) {
                     sm.cand_k[warp] = k;
                     sm.cand_fits[warp] = cnt <= budget;
@@ -193,31 +237,80 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
                 __syncthreads();
                 // candidates ascend with the warp index: the first fitting one
                 // bounds hi, the one before it (failing) bounds lo
-                const unsigned fits = __ballot_sync(0xffffffffu, sm.cand_fits[lane] != 0);
-                const int first = fits ? __ffs(fits) - 1 : kPlanThreads / 32;
-                if (first < kPlanThreads / 32)
+                int first = kPlanWarps;
+                for (int w = kPlanWarps - 1; w >= 0; --w)
+                    if (sm.cand_fits[w])
+                        first = w;
+                if (first < kPlanWarps)
                     hi = sm.cand_k[first];
                 if (first > 0)
                     lo = max(lo, sm.cand_k[first - 1] + 1);
+                __syncthreads();
             }
             chunk = c0 + (long long)lo * kTile;
         }
     }
-    for (int r = tid; r < num_reqs; r += kPlanThreads)
-        sm.split_base[r] = (int)ceil_div_ll(sm.lens[r], chunk);
+    const int chunk_tiles = (int)(chunk / kTile);
+
+    // ---- per request: chunks, tiles, cost (tiles plus the start charge); prefixes
+    int ns[kReqPerThread], nt[kReqPerThread];
+    int my_chunks = 0, my_cost = 0, my_nonempty = 0;
+#pragma unroll
+    for (int k = 0; k < kReqPerThread; ++k) {
+        ns[k] = (int)((L[k] + chunk - 1) / chunk);
+        nt[k] = (L[k] + kTile - 1) / kTile;
+        my_chunks += ns[k];
+        my_cost += nt[k] + (ns[k] > 0 ? kSegmentCostTiles : 0);
+        my_nonempty += ns[k] > 0 ? 1 : 0;
+    }
+    int n_splits, total_cost, n_nonempty;
+    int sb_run = block_scan_excl(my_chunks, sm.red32, &n_splits);
+    int cost_run = block_scan_excl(my_cost, sm.red32, &total_cost);
+    int ne_run = block_scan_excl(my_nonempty, sm.red32, &n_nonempty);
+    int lm[kReqPerThread];
+    int my_lm = -1;
+    {
+        int c = cost_run;
+#pragma unroll
+        for (int k = 0; k < kReqPerThread; ++k) {
+            lm[k] = ns[k] > 0 ? chunk_mid2(c, nt[k], chunk_tiles, ns[k] - 1) : -1;
+            my_lm = max(my_lm, lm[k]);
+            c += nt[k] + (ns[k] > 0 ? kSegmentCostTiles : 0);
+        }
+    }
+    int lm_run = block_scan_max_excl(my_lm, sm.red32);
+#pragma unroll
+    for (int k = 0; k < kReqPerThread; ++k) {
+        const int r = r0 + k;
+        lm_run = max(lm_run, lm[k]);
+        if (r < num_reqs) {
+            sm.sb[r] = sb_run;
+            sm.cost0[r] = cost_run;
+            sm.nonempty[r] = ne_run;
+            sm.lastm[r] = lm_run;
+        }
+        sb_run += ns[k];
+        cost_run += nt[k] + (ns[k] > 0 ? kSegmentCostTiles : 0);
+        ne_run += ns[k] > 0 ? 1 : 0;
+    }
+    if (tid == 0) {
+        sm.sb[num_reqs] = n_splits;
+        sm.cost0[num_reqs] = total_cost;
+        sm.nonempty[num_reqs] = n_nonempty;
+    }
     __syncthreads();
-    const int n_splits = block_exclusive_scan(sm.split_base, num_reqs, sm.red32);
-    for (int r = tid; r < num_reqs; r += kPlanThreads)
-        plan.indptr[r] = sm.split_base[r];
+
+    // ---- the split plan itself
+    for (int r = tid; r <= num_reqs; r += kPlanThreads)
+        plan.indptr[r] = sm.sb[r];
     if (tid == 0) {
         if (plan.status != nullptr)
             *plan.status = 0;
-        plan.indptr[num_reqs] = n_splits;
         *plan.chunk = chunk;
     }
     if (plan.segments == nullptr)
         return;
-    if (n_splits > kMaxPlanSplits) {   // excluded by the host-side budget limit
+    if (members > kMaxSms || n_splits > kMaxPlanSplits) {   // excluded on the host
         if (tid == 0 && plan.status != nullptr)
             *plan.status = 8;
         return;
@@ -227,149 +320,210 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     // it can (it claims that index), so once every such SM's speed is measured,
     // member m of every team gets a share of the cost proportional to the mean
     // speed of SMs team*members + m; until then the shares are equal
-    {
-        const SmCalib *cal = plan.calib;
-        const int n_cta = plan.n_claim;
-        const int teams = n_cta / max(members, 1);
+    if (cache_hit) {
+        if (tid <= members)
+            sm.wprefix[tid] = cached_w;
+        if (tid == 0)
+            sm.weighted = 1;
+        __syncthreads();
+    } else {
         const bool usable = cal != nullptr && teams >= 1 && n_cta <= kMaxSms;
-        float rate = 0.f;
         bool measured = true;
         if (usable && tid < n_cta) {
             const float c = cal->cost[tid], t = cal->time_ns[tid];
             measured = c >= kCalibCost && t > 0.f;
-            rate = measured ? c / t : 0.f;
-            sm.wprefix[tid + 1] = rate;              // per-CTA rate, reduced below
+            sm.wrate[tid] = measured ? c / t : 0.f;
         }
         const int ready = __syncthreads_and(usable && measured);
-        if (ready) {
+        if (ready && tid < 32) {
             // member rate (mean over teams), then an inclusive prefix in warp 0:
             // lane l owns members [8l, 8l + 8)
-            if (tid < members) {
+            constexpr int per = kMaxSms / 32;
+            float loc[per];
+            float run = 0.f;
+#pragma unroll
+            for (int i = 0; i < per; ++i) {
+                const int m = tid * per + i;
                 float r = 0.f;
-                for (int g = 0; g < teams; ++g)
-                    r += sm.wprefix[g * members + tid + 1];
-                sm.wrun[tid] = r / teams;
+                if (m < members) {
+                    for (int g = 0; g < teams; ++g)
+                        r += sm.wrate[g * members + m];
+                    r /= teams;
+                }
+                run += r;
+                loc[i] = run;
             }
-            __syncthreads();
-            if (tid < 32) {
-                constexpr int per = kMaxSms / 32;
-                float loc[per];
-                float run = 0.f;
+            float incl = run;
 #pragma unroll
-                for (int i = 0; i < per; ++i) {
-                    const int m = tid * per + i;
-                    run += m < members ? sm.wrun[m] : 0.f;
-                    loc[i] = run;
-                }
-                float incl = run;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float up = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (tid >= o)
-                        incl += up;
-                }
-                const float off = incl - run;
-#pragma unroll
-                for (int i = 0; i < per; ++i) {
-                    const int m = tid * per + i;
-                    if (m < members)
-                        sm.wprefix[m + 1] = off + loc[i];
-                }
-                if (tid == 0)
-                    sm.wprefix[0] = 0.f;
+            for (int o = 1; o < 32; o <<= 1) {
+                const float up = __shfl_up_sync(0xffffffffu, incl, o);
+                if (tid >= o)
+                    incl += up;
             }
+            const float off = incl - run;
+#pragma unroll
+            for (int i = 0; i < per; ++i) {
+                const int m = tid * per + i;
+                if (m < members)
+                    sm.wprefix[m + 1] = off + loc[i];
+            }
+            if (tid == 0)
+                sm.wprefix[0] = 0.f;
         }
         if (tid == 0)
             sm.weighted = ready ? 1 : 0;
         __syncthreads();
+        if (ready) {
+            // the records of this grid's SMs are final: keep the prefix for later calls
+            SmCalib *wcal = plan.calib;
+            if (tid <= members)
+                wcal->cache_wprefix[tid] = sm.wprefix[tid];
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) {
+                wcal->cache_teams = teams;
+                wcal->cache_members = members;
+            }
+        }
     }
 
-    // ---- schedule: chunks in request order, dealt to members by cost
-    for (int i = tid; i < n_splits; i += kPlanThreads) {
-        // request of chunk i: the last r with split_base[r] <= i
+    // ---- first chunk of every member: the first chunk whose doubled cost
+    // midpoint reaches the member's doubled share boundary
+    const bool weighted = sm.weighted != 0;
+    for (int m = tid; m <= members; m += kPlanThreads) {
+        int firstc = n_splits;
+        if (m == 0) {
+            firstc = 0;
+        } else if (m < members) {
+            // a doubled midpoint v reaches member m's boundary when
+            // v >= 2 * total_cost * share(m): an integer threshold
+            const long long thr =
+                weighted ? (long long)ceil(2.0 * total_cost * (double)sm.wprefix[m] /
+                                           (double)sm.wprefix[members])
+                         : (2LL * total_cost * m + members - 1) / members;
+            auto reaches = [&](int v) -> bool { return (long long)v >= thr; };
+            // the first request whose last chunk reaches it (lastm is a running
+            // maximum, so this request has chunks)
+            int lo = 0, hi = num_reqs;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (reaches(sm.lastm[mid]))
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            if (lo < num_reqs) {
+                const int r = lo;
+                const int tiles = (sm.lens[r] + kTile - 1) / kTile;
+                const int nsr = sm.sb[r + 1] - sm.sb[r];
+                const int c = sm.cost0[r];
+                int s = 0;
+                if (!reaches(chunk_mid2(c, tiles, chunk_tiles, 0))) {
+                    int a = 1, b = nsr - 1;   // the last chunk reaches
+                    while (a < b) {
+                        const int mid = (a + b) >> 1;
+                        if (reaches(chunk_mid2(c, tiles, chunk_tiles, mid)))
+                            b = mid;
+                        else
+                            a = mid + 1;
+                    }
+                    s = a;
+                }
+                firstc = sm.sb[r] + s;
+            }
+        }
+        sm.first[m] = firstc;
+    }
+    __syncthreads();
+
+    // request of chunk i: the last r with sb[r] <= i (a request with chunks)
+    auto req_of = [&](int chunk_i) -> int {
         int lo = 0, hi = num_reqs - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (sm.split_base[mid] <= i)
+            if (sm.sb[mid] <= chunk_i)
                 lo = mid;
             else
                 hi = mid - 1;
         }
-        const int r = lo;
-        const int s = i - sm.split_base[r];
-        const int L = sm.lens[r];
-        const int t0 = (int)(s * chunk);
-        const int t1 = (int)min((long long)L, (s + 1) * chunk);
-        sm.sp_req[i] = r;
-        sm.sp_t0[i] = t0;
-        sm.sp_t1[i] = t1;
-        // cost in tiles; a request's first chunk also carries the cost of
-        // starting a segment (query load, first-tile softmax, epilogue)
-        sm.sp_tiles[i] = (t1 - t0 + kTile - 1) / kTile + (s == 0 ? kSegmentCostTiles : 0);
-        sm.sp_member[i] = sm.sp_tiles[i];   // keep the cost for the midpoint
-    }
-    __syncthreads();
-    const int total_tiles = block_exclusive_scan(sm.sp_tiles, n_splits, sm.red32);
-    for (int i = tid; i < n_splits; i += kPlanThreads) {
-        // midpoint of chunk i as a fraction of the total cost
-        const long long mid2 = 2LL * sm.sp_tiles[i] + sm.sp_member[i];  // 2*prefix + cost
-        const float frac = (float)mid2 / (2.f * (float)max(total_tiles, 1));
-        int m;
-        if (sm.weighted) {
-            // the member whose share [wprefix[m], wprefix[m + 1]) holds the midpoint
-            const float target = frac * sm.wprefix[members];
-            int lo = 0, hi = members - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (sm.wprefix[mid] <= target)
-                    lo = mid;
-                else
-                    hi = mid - 1;
-            }
-            m = lo;
-        } else {
-            m = (int)(frac * (float)members);
+        return lo;
+    };
+
+    // ---- segments per member: one per request with chunks in the member's range
+    int my_nseg = 0, my_rfirst = 0;
+    if (tid < members) {
+        const int c0i = sm.first[tid], c1i = sm.first[tid + 1];
+        if (c1i > c0i) {
+            my_rfirst = req_of(c0i);
+            const int rlast = req_of(c1i - 1);
+            my_nseg = sm.nonempty[rlast + 1] - sm.nonempty[my_rfirst];
         }
-        sm.sp_member[i] = min(members - 1, max(0, m));
     }
-    __syncthreads();
-    for (int i = tid; i < n_splits; i += kPlanThreads)
-        sm.sp_seg[i] = (i == 0) || sm.sp_req[i] != sm.sp_req[i - 1] ||
-                       sm.sp_member[i] != sm.sp_member[i - 1];
-    __syncthreads();
-    const int n_segs = block_exclusive_scan(sm.sp_seg, n_splits, sm.red32);
-    for (int i = tid; i < n_splits; i += kPlanThreads) {
-        // sp_seg now holds the number of segment starts before chunk i, so a
-        // chunk that continues a segment belongs to segment sp_seg[i] - 1
-        const bool starts = (i == 0) || sm.sp_req[i] != sm.sp_req[i - 1] ||
-                            sm.sp_member[i] != sm.sp_member[i - 1];
-        const int seg = sm.sp_seg[i] - (starts ? 0 : 1);
-        const bool ends = (i == n_splits - 1) || sm.sp_req[i + 1] != sm.sp_req[i] ||
-                          sm.sp_member[i + 1] != sm.sp_member[i];
-        if (starts) {
-            plan.segments[seg].x = sm.sp_req[i];
-            plan.segments[seg].y = sm.sp_t0[i];
-            plan.segments[seg].w = sm.sp_member[i];
-            // members (previous chunk's member, this member] start at this segment
-            const int prev = (i == 0) ? -1 : sm.sp_member[i - 1];
-            for (int k = prev + 1; k <= sm.sp_member[i]; ++k)
-                plan.seg_member_indptr[k] = seg;
-        }
-        if (ends)
-            plan.segments[seg].z = sm.sp_t1[i];
-    }
-    // first segment of each request: the segment id of its first chunk (for a
-    // request without chunks, the id of the next request's first chunk)
-    for (int r = tid; r < num_reqs; r += kPlanThreads) {
-        const int i = sm.split_base[r];
-        plan.seg_req_indptr[r] = i < n_splits ? sm.sp_seg[i] : n_segs;
+    int n_segs;
+    const int seg0 = block_scan_excl(tid < members ? my_nseg : 0, sm.red32, &n_segs);
+    if (tid < members) {
+        sm.nseg[tid] = seg0;
+        plan.seg_member_indptr[tid] = seg0;
     }
     if (tid == 0) {
-        plan.seg_req_indptr[num_reqs] = n_segs;
-        const int last = n_splits > 0 ? sm.sp_member[n_splits - 1] : -1;
-        for (int k = last + 1; k <= members; ++k)
-            plan.seg_member_indptr[k] = n_segs;
+        sm.nseg[members] = n_segs;
+        plan.seg_member_indptr[members] = n_segs;
         *plan.seg_count = n_segs;
+        plan.seg_req_indptr[num_reqs] = n_segs;
+    }
+    if (tid < members && my_nseg > 0) {
+        const int c0i = sm.first[tid], c1i = sm.first[tid + 1];
+        int id = seg0;
+        for (int r = my_rfirst; id < seg0 + my_nseg; ++r) {
+            if (sm.sb[r + 1] == sm.sb[r])
+                continue;                            // a request without chunks
+            const int a = max(c0i, sm.sb[r]) - sm.sb[r];
+            const int b = min(c1i, sm.sb[r + 1]) - sm.sb[r];
+            int4 seg;
+            seg.x = r;
+            seg.y = (int)(a * chunk);
+            seg.z = (int)min((long long)sm.lens[r], b * chunk);
+            seg.w = tid;
+            plan.segments[id] = seg;
+            ++id;
+        }
+    }
+    __syncthreads();
+
+    // ---- first segment of each request (for a request without chunks, that of
+    // the next request with chunks, or the total)
+    for (int r = tid; r < num_reqs; r += kPlanThreads) {
+        int rr = r;
+        if (sm.sb[r + 1] == sm.sb[r]) {
+            const int want = sm.nonempty[r];          // that request's rank among them
+            if (want >= n_nonempty) {
+                plan.seg_req_indptr[r] = n_segs;
+                continue;
+            }
+            int lo = r + 1, hi = num_reqs - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (sm.nonempty[mid + 1] > want)
+                    hi = mid;
+                else
+                    lo = mid + 1;
+            }
+            rr = lo;
+        }
+        // the member holding the request's first chunk (the last member whose
+        // range starts at or before it), and the request's place among that
+        // member's requests
+        const int c = sm.sb[rr];
+        int lo = 0, hi = members - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (sm.first[mid] <= c)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int rf = req_of(sm.first[lo]);
+        plan.seg_req_indptr[r] = sm.nseg[lo] + (sm.nonempty[rr] - sm.nonempty[rf]);
     }
 }
 

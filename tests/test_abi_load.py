@@ -44,7 +44,7 @@ def test_split_budget_matches_oracle_rule(lib, R, n_q, H, slots, min_splits):
 
 def test_workspace_grows_with_the_machine(lib):
     small = lib.mla_workspace_size(64, 1, 64, 152, 1)
-    big = lib.mla_workspace_size(64, 1, 64, 304, 1)
+    big = lib.mla_workspace_size(64, 1, 64, 256, 1)
     assert 0 < small < big
     # at most R + members segments of 64 rows x 512 fp32 partials
     assert (64 + 152) * 64 * 512 * 4 <= small < (64 + 152) * 64 * 513 * 4 + (1 << 20)
@@ -85,3 +85,12 @@ def test_misaligned_and_out_of_range_arguments(lib):
     assert call(pages=0) == 1
     assert call(H=24) == 1
     assert call(ws=fake + 128) == 1              # workspace not 256-byte aligned
+
+
+def test_more_than_256_ctas_per_row_group_is_rejected(lib):
+    # the persistent schedule keeps per-CTA tables of 256 entries
+    assert lib.mla_split_budget(64, 1, 64, 256, 1) > 0
+    assert lib.mla_split_budget(64, 1, 64, 257, 1) == -1
+    assert lib.mla_workspace_size(64, 1, 64, 257, 1) == 0
+    # four row groups: 1024 slots give 256 CTAs per group
+    assert lib.mla_split_budget(8, 4, 64, 1024, 1) > 0
