@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "paged MLA decode: achieved HBM GB/s (% of GB300 peak), request-steps/s"
 UNIT = "GB/s"
+FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
 KERNELS_PER_STEP = 3          # plan, split decode, combine+gate
@@ -178,6 +179,18 @@ def hbm_peak():
         return v, "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense bf16 tensor peak (TFLOP/s): the burst figure, for a kernel timed in
+    a short step."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["bf16_tflops"])
+        return v, "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def decode_source_hash():
@@ -360,6 +373,26 @@ def run_gpu(args):
     dec_avg = statistics.mean(decode_ms)
     achieved = kv_bytes_layer / (dec_avg / 1e3) / 1e9
     traffic = profiled_traffic(args.workload, kv_bytes_layer)
+    # Which roofline bounds the decode: 2 * (576 + 512) flop per (query row, KV
+    # token) against 1,152 bytes per KV token, compared with the measured ridge.
+    tpeak, tpeak_src = tensor_peak()
+    flops_layer = 2.0 * (w.dc + w.dr + w.dc) * w.n_q * w.num_heads * w.kv_tokens
+    intensity = flops_layer / kv_bytes_layer
+    ridge = tpeak * 1e12 / (peak * 1e9)
+    if intensity > ridge:
+        achieved_t = flops_layer / (dec_avg / 1e3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "split decode", "achieved": achieved_t,
+                    "peak": tpeak, "peak_source": tpeak_src, "unit": "TFLOP/s",
+                    "frac": achieved_t / tpeak, "traffic": traffic,
+                    "algorithmic_flops_per_launch": flops_layer,
+                    "flop_per_byte": intensity, "ridge_flop_per_byte": ridge,
+                    "hbm_achieved_gbs": achieved, "hbm_frac": achieved / peak}
+    else:
+        roofline = {"bound": "hbm", "kernel": "split decode", "achieved": achieved,
+                    "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                    "frac": achieved / peak, "traffic": traffic,
+                    "algorithmic_bytes_per_launch": kv_bytes_layer,
+                    "flop_per_byte": intensity, "ridge_flop_per_byte": ridge}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -378,10 +411,7 @@ def run_gpu(args):
                       "note": "from a second timed pass of the same K calls with CUDA events "
                               "recorded between the kernels (which stops them overlapping); "
                               "the reported value comes from the first pass, without them"},
-        "roofline": {"bound": "hbm", "kernel": "split decode", "achieved": achieved,
-                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": kv_bytes_layer},
+        "roofline": roofline,
         "gpu_launches": KERNELS_PER_STEP * K * layers,
         "clocks": clocks,
     }
