@@ -75,14 +75,14 @@ const char *mla_strerror(plmla_status status);
  *                one CTA owns); row_groups = n_q * num_heads / group_rows
  *   slots      = cta_budget, or the current device's SM count when 0
  *   members    = max(1, floor(slots / row_groups))   (persistent CTAs per group)
- *   budget     = max(16 * members, num_reqs * min_splits_per_req), at most 4096
+ *   budget     = max(26 * members, num_reqs * min_splits_per_req), at most 4096
  *
  * mla_decode runs row_groups x members persistent CTAs; each takes a contiguous,
  * cost-balanced run of the chunks (equal shares until the library has measured
  * the speed of each SM over a few calls with real work, then shares in
  * proportion to it, fixed from then on).  Returns the budget, or -1 for invalid
- * arguments, members above 256, a budget above 4096, or no CUDA device when
- * cta_budget == 0.
+ * arguments, members above 256, num_reqs * min_splits_per_req above 4096, or no
+ * CUDA device when cta_budget == 0.
  */
 int32_t mla_split_budget(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_budget,
                          int32_t min_splits_per_req);

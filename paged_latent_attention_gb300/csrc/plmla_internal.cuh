@@ -16,7 +16,7 @@ constexpr int kTile = 128;        // KV tokens per decode tile; chunks are multi
 constexpr int kMaxReqs = 1024;
 constexpr int kMaxNq = 16;
 constexpr int kMaxPlanSplits = 4096;  // chunks the device planner can schedule
-constexpr int kChunksPerMember = 16;  // default chunk budget per persistent CTA
+constexpr int kChunksPerMember = 26;  // default chunk budget per persistent CTA
 
 constexpr int kMaxSms = 256;            // SM ids the speed record covers
 constexpr float kCalibCost = 192.f;     // cost units an SM measures before its speed is used
