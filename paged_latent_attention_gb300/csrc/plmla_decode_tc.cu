@@ -698,8 +698,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     } else if (warp == kWarpVProducer) {
         // ---------------------------------------------------------- V producer
         // V item v of a tile = latent block v / 2 (128 columns), token half v % 2.
-        // Items of a partial tile land on bar_vtmp first; the warp zeroes the
-        // rows past the history and then releases the item to the issuer.
+        // Items of a request's last tile that reach past the history land on
+        // bar_vtmp first; the warp zeroes the rows past the history and then
+        // releases the item to the issuer.  An item entirely past the history is
+        // not loaded at all: its slot is zeroed.
         const uint64_t pol_once = l2_policy_evict_first();   // the tile's last read
         int slot = 0;
         uint32_t phase = 0, vtmp_phase = 0;
@@ -728,8 +730,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     }
                     const uint32_t dst = s_v + slot * kSubBytes;
                     const int col = 128 * (v >> 1), tk = tok + 64 * (v & 1);
+                    // all 64 tokens of the item past the history: nothing to load
+                    const bool dead = t + 64 * (v & 1) >= seg.z;
                     const uint32_t done_bar = partial ? bar_vtmp : bar_full_v + 8 * slot;
-                    if (lane == 0) {
+                    if (lane == 0 && !dead) {
                         mbar_arrive_expect_tx(done_bar, kSubBytes);
                         tma_load_3d_hint(dst, &tm_v, col, tk, page, done_bar, pol_once);
                         tma_load_3d_hint(dst + kVHalf, &tm_v, col + 64, tk, page, done_bar,
@@ -740,13 +744,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     if (partial) {
                         // rows r of this item hold token t + 64 * (v % 2) + r
                         const bool landed =
-                            wait_bounded(bar_vtmp, vtmp_phase, abort_flag, a.status, 12);
+                            dead || wait_bounded(bar_vtmp, vtmp_phase, abort_flag, a.status, 12);
                         if (!__all_sync(0xffffffffu, landed)) {
                             vtmp_pending = true;
                             ok = false;
                             break;
                         }
-                        vtmp_phase ^= 1;
+                        if (!dead)
+                            vtmp_phase ^= 1;
                         const int first_dead = seg.z - (t + 64 * (v & 1));   // may be <= 0
                         for (int r = lane; r < 64; r += 32) {
                             if (r >= first_dead) {
