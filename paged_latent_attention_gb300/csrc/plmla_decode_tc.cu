@@ -1131,7 +1131,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         float cost = 0.f;
         for (int s = seg_begin; s < seg_end; ++s) {
             const int4 seg = a.segments[s];
-            cost += (float)((seg.z - seg.y + kTile - 1) / kTile + (seg.y == 0 ? 2 : 0));
+            cost += (float)((seg.z - seg.y + kTile - 1) / kTile +
+                            (seg.y == 0 ? kSegmentCostTiles : 0));
         }
         if (cost >= kCalibMinCost) {
             atomicAdd(&a.calib->time_ns[sm_id], (float)(global_ns() - t_start));

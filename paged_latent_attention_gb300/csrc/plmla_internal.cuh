@@ -17,6 +17,10 @@ constexpr int kMaxReqs = 1024;
 constexpr int kMaxNq = 16;
 constexpr int kMaxPlanSplits = 4096;  // chunks the device planner can schedule
 constexpr int kChunksPerMember = 26;  // default chunk budget per persistent CTA
+// Planner cost of starting a segment, in 128-token tiles: a request's first
+// chunk carries it (query load, first-tile softmax, the previous segment's
+// partial-state epilogue).
+constexpr int kSegmentCostTiles = 2;
 
 constexpr int kMaxSms = 256;            // SM ids the speed record covers
 constexpr float kCalibCost = 192.f;     // cost units an SM measures before its speed is used

@@ -36,7 +36,6 @@ namespace {
 constexpr int kPlanThreads = 256;
 constexpr int kPlanWarps = kPlanThreads / 32;
 constexpr int kReqPerThread = kMaxReqs / kPlanThreads;   // thread t owns requests [4t, 4t + 4)
-constexpr int kSegmentCostTiles = 2;
 
 struct PlanSmem {
     int lens[kMaxReqs];
