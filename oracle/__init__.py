@@ -7,6 +7,7 @@ does.  It shares no code with the CUDA path.
 from .oracle import (  # noqa: F401
     attend_rows,
     gate_sigmoid,
+    kv_append,
     lse_merge,
     mla_decode_reference,
     plan_splits,

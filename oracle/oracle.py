@@ -217,3 +217,49 @@ def split_budget(num_reqs: int, row_groups: int, cta_slots: int, min_splits: int
         raise ValueError("budget above the planner's limit")
     budget = min(max(chunks_per_member * members, wanted), limit)
     return budget
+
+
+# --------------------------------------------------------------------------
+# KV append (vLLM blog "Kimi K3 Inference Backend Evolution", section "State
+# Overwrite: How KDA Breaks Traditional KV Cache", the append-only contract of
+# MLA: a new token's latent and rope rows are written after the request's
+# existing history and no earlier row changes), into the flat page pool
+# (TokenSpeed Kimi K3 post, "A Generic, Unified Flat KV Layout for Cache
+# Management": one global page ID per 1,536-token page).
+# --------------------------------------------------------------------------
+
+def kv_append(slab, page_table, seq_lens, latent_new, rope_new, n_new, *,
+              page_tokens=PAGE_TOKENS, page_stride=None, dc=DC, dr=DR):
+    """Return a copy of the slab with each request's n_new new rows written.
+
+    seq_lens counts the history after the append, so new token j of request r
+    goes to position p = seq_lens[r] - n_new + j: page page_table[r, p //
+    page_tokens], row p % page_tokens.  latent_new is [R*n_new, dc] and rope_new
+    [R*n_new, dr] (bf16, row r*n_new + j); the stored row is latent then rope.
+    Raises IndexError for a position below zero or a page ID outside the pool.
+    """
+    sl = _u16(slab).copy()
+    shape = sl.shape
+    flat = sl.reshape(-1)
+    pt, lens = _i32(page_table), _i32(seq_lens)
+    R = lens.shape[0]
+    if pt.ndim == 1:
+        pt = pt.reshape(R, -1)
+    row_elems = dc + dr
+    if page_stride is None:
+        page_stride = page_tokens * row_elems
+    num_pages = flat.size // page_stride
+    lat = _u16(latent_new).reshape(R * n_new, dc)
+    rope = _u16(rope_new).reshape(R * n_new, dr)
+    for r in range(R):
+        for j in range(n_new):
+            p = int(lens[r]) - n_new + j
+            if p < 0:
+                raise IndexError("new token before the start of the history")
+            page = int(pt[r, p // page_tokens])
+            if page < 0 or page >= num_pages:
+                raise IndexError("page table entry outside the pool")
+            base = page * page_stride + (p % page_tokens) * row_elems
+            flat[base:base + dc] = lat[r * n_new + j]
+            flat[base + dc:base + row_elems] = rope[r * n_new + j]
+    return flat.reshape(shape)
