@@ -46,6 +46,11 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["plmla", "reference"], default="plmla")
+    ap.add_argument("--op", choices=["decode", "append"], default="decode",
+                    help="decode: the hot path (default); append: the KV append kernel "
+                         "writing a block of new rows per request into the same pool")
+    ap.add_argument("--append-tokens", type=int, default=4096,
+                    help="new tokens per request for --op append")
     ap.add_argument("--workload", default="steady",
                     choices=["tiny", "steady", "agentic", "spec", "long"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -477,6 +482,177 @@ def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist):
 
 
 # --------------------------------------------------------------------------
+# KV append (the step before the hot path): n_new rows per request written into
+# the steady workload's pool
+# --------------------------------------------------------------------------
+
+APPEND_METRIC = "paged KV append: achieved HBM GB/s on row bytes read + written"
+
+
+def append_rows(w, n_new, device, seed=11):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    lat = torch.empty(w.num_reqs * n_new, w.dc, dtype=torch.bfloat16,
+                      device=device).normal_(generator=g)
+    rope = torch.empty(w.num_reqs * n_new, w.dr, dtype=torch.bfloat16,
+                       device=device).normal_(generator=g)
+    return lat, rope
+
+
+def time_appends(plmla, lat, rope, slab, table, lens, n_new, K, W, stream):
+    import torch
+    for _ in range(W):
+        plmla.mla_kv_append(lat, rope, slab, table, lens, n_new)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(K):
+        plmla.mla_kv_append(lat, rope, slab, table, lens, n_new)
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / K
+
+
+def run_append(args):
+    import torch
+    import paged_latent_attention_gb300 as plmla
+    from paged_latent_attention_gb300 import inputs
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+    w = inputs.make_workload("steady")
+    n_new = args.append_tokens
+    if n_new < 1 or n_new > int(w.seq_lens.min()):
+        raise SystemExit(f"--append-tokens must lie in [1, {int(w.seq_lens.min())}]")
+    slab = inputs.make_slab(w, device)
+    table = torch.as_tensor(w.page_table, device=device)
+    lens = torch.as_tensor(w.seq_lens, device=device)
+    lat, rope = append_rows(w, n_new, device)
+    rows = w.num_reqs * n_new
+    row_bytes = (w.dc + w.dr) * 2
+    # algorithmic bytes: each new row read once and written once, plus the
+    # lengths and one table entry per row
+    bytes_step = 2 * rows * row_bytes + w.num_reqs * 4 + rows * 4
+    stream = torch.cuda.current_stream(device)
+    K, W = args.steps, max(3, args.warmup)
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid).start()
+    time.sleep(0.3)
+    barrier(dist, device)
+    host_t0 = time.time()
+    ms = time_appends(plmla, lat, rope, slab, table, lens, n_new, K, W, stream)
+    host_t1 = time.time()
+    # the decode step's own append: one new row per request
+    lat1, rope1 = append_rows(w, 1, device, seed=12)
+    ms_one = time_appends(plmla, lat1, rope1, slab, table, lens, 1, K, W, stream)
+    barrier(dist, device)
+    max_ms, units = aggregate(dist, ms, bytes_step, device)
+
+    e2e = None
+    if not args.no_e2e:
+        host_lat, host_rope = lat.cpu().pin_memory(), rope.cpu().pin_memory()
+        host_lens = lens.cpu().pin_memory()
+        dev_lat, dev_rope, dev_lens = (torch.empty_like(lat), torch.empty_like(rope),
+                                       torch.empty_like(lens))
+        host_status = torch.zeros(1, dtype=torch.int32).pin_memory()
+        status = torch.zeros(1, dtype=torch.int32, device=device)
+
+        def e2e_step():
+            dev_lat.copy_(host_lat, non_blocking=True)
+            dev_rope.copy_(host_rope, non_blocking=True)
+            dev_lens.copy_(host_lens, non_blocking=True)
+            plmla.mla_kv_append(dev_lat, dev_rope, slab, table, dev_lens, n_new, status=status)
+            host_status.copy_(status, non_blocking=True)
+
+        for _ in range(W):
+            e2e_step()
+        torch.cuda.synchronize(device)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(K):
+            e2e_step()
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        e_ms, e_units = aggregate(dist, start.elapsed_time(end) / K, bytes_step, device)
+        e2e = {"value": e_units / (e_ms / 1e3) / 1e9, "unit": UNIT,
+               "h2d_bytes_per_step": host_lat.numel() * 2 + host_rope.numel() * 2 + 4 * w.num_reqs,
+               "d2h_bytes_per_step": 4, "ms_per_step": e_ms,
+               "note": "new rows and lengths copied in from pinned host memory, the status "
+                       "word copied out; the pool stays resident"}
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(host_t0, host_t1)
+    if rank != 0:
+        return None
+    peak, peak_src = hbm_peak()
+    achieved = bytes_step / (ms / 1e3) / 1e9
+    line = {
+        "metric": APPEND_METRIC, "value": units / (max_ms / 1e3) / 1e9, "unit": UNIT,
+        "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": max_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"KV append: {w.num_reqs} requests x {n_new} new tokens "
+                               f"({rows} rows of 512 latent + 64 rope bf16) into the steady "
+                               f"decode pool ({w.num_pages} pages of 1536 tokens), positions "
+                               f"seq_lens - {n_new} .. seq_lens - 1",
+                   "rows": rows, "bytes_per_step": bytes_step,
+                   "l2": "rows read + written per step exceed the 129 MB L2"
+                         if 2 * rows * row_bytes > 129e6 else "fits in L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "kv append", "achieved": achieved,
+                     "peak": peak, "peak_source": peak_src, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": bytes_step},
+        "decode_step_append_us": 1e3 * ms_one,
+        "gpu_launches": 2 * K + (K if e2e is not None else 0),
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = append_cpu_baseline(w, slab, lat, rope, n_new, args.cpu_seconds)
+    return line
+
+
+def append_cpu_baseline(w, slab_dev, lat, rope, n_new, target_s):
+    """The oracle's kv_append on the pages of the first few requests (remapped
+    into a small host pool), timed on the host."""
+    import numpy as np
+    import torch
+    import oracle
+    ids = list(range(min(8, w.num_reqs)))
+    per = [-(-int(w.seq_lens[r]) // w.page_tokens) for r in ids]
+    phys = [int(p) for r, n in zip(ids, per) for p in w.page_table[r, :n]]
+    host = slab_dev.index_select(0, torch.as_tensor(phys, device=slab_dev.device)).cpu()
+    table = np.zeros((len(ids), max(per)), dtype=np.int32)
+    pos = 0
+    for i, n in enumerate(per):
+        table[i, :n] = np.arange(pos, pos + n)
+        pos += n
+    lens = w.seq_lens[ids].astype(np.int32)
+    lat_h, rope_h = lat[:len(ids) * n_new].cpu(), rope[:len(ids) * n_new].cpu()
+    elapsed, reps = 0.0, 0
+    while elapsed < 0.5 * target_s or reps == 0:
+        t = time.perf_counter()
+        oracle.kv_append(host, table, lens, lat_h, rope_h, n_new, page_stride=w.page_stride)
+        elapsed += time.perf_counter() - t
+        reps += 1
+    rows = len(ids) * n_new
+    gbs = 2 * rows * (w.dc + w.dr) * 2 * reps / elapsed / 1e9
+    return {"value": gbs, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(ids)} of {w.num_reqs} requests x {n_new} new rows, {reps} pass(es) "
+                      f"over a {len(phys)}-page host pool, {elapsed:.1f} s"}
+
+
+# --------------------------------------------------------------------------
 # reference arm: the oracle as it stands, on host cores
 # --------------------------------------------------------------------------
 
@@ -528,6 +704,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         line = run_reference(args)
+    elif args.op == "append":
+        line = run_append(args)
     else:
         line = run_gpu(args)
     if line is not None:

@@ -255,6 +255,39 @@ plmla_status mla_split_combine(const float *o_part, const float *lse_part,
                                int32_t n_q_per_req, int32_t num_heads, void *out, float *lse,
                                void *stream);
 
+/*
+ * mla_kv_append -- write each request's new latent and rope rows into the flat
+ * page pool, the step before attention: under MLA a new token's rows are
+ * appended after the request's history and no earlier row changes (vLLM blog
+ * "Kimi K3 Inference Backend Evolution", section "State Overwrite: How KDA
+ * Breaks Traditional KV Cache"); pages as in mla_decode (TokenSpeed Kimi K3
+ * post, "A Generic, Unified Flat KV Layout for Cache Management").
+ *
+ * latent_new   [num_reqs * n_new, 512] bf16, row r * n_new + j = request r's
+ *              new token j, contiguous rows, 16-byte aligned
+ * rope_new     [num_reqs * n_new, 64] bf16, same rows, 16-byte aligned
+ * slab_base, num_pages, page_stride_elems, page_table, page_table_ld
+ *              the pool and table exactly as for mla_decode
+ * seq_lens     [num_reqs] int32 histories AFTER the append (mla_decode's
+ *              convention): new token j of request r goes to position
+ *              seq_lens[r] - n_new + j, i.e. page page_table[r, p / 1536],
+ *              row p % 1536, as 512 latent then 64 rope values
+ * n_new        new tokens per request (0: nothing to do)
+ * status       optional device int32: set to 32 if some seq_lens[r] < n_new and
+ *              to 33 if a position's page column p / 1536 is >= page_table_ld or
+ *              its page ID lies outside [0, num_pages); such rows are skipped,
+ *              no table entry past a row's page_table_ld columns is read and
+ *              nothing is written outside the pool
+ *
+ * Ownership: caller owns every buffer.  Asynchronous on `stream`.  Returns
+ * PLMLA_INVALID_ARGUMENT for null or misaligned pointers and bad sizes,
+ * PLMLA_CUDA_ERROR if the launch fails.
+ */
+plmla_status mla_kv_append(const void *latent_new, const void *rope_new, void *slab_base,
+                           int64_t num_pages, int64_t page_stride_elems, const int32_t *page_table,
+                           int64_t page_table_ld, const int32_t *seq_lens, int32_t num_reqs,
+                           int32_t n_new, int32_t *status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

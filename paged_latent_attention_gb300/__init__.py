@@ -8,6 +8,7 @@ from .api import (  # noqa: F401
     allocate_workspace,
     device_status,
     mla_decode,
+    mla_kv_append,
     mla_plan_splits,
     mla_split_budget,
     mla_split_combine,

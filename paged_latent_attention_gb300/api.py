@@ -174,3 +174,36 @@ def mla_split_combine(o_part, lse_part, split_indptr, gate, *, n_q=1, out=None, 
         _stream_ptr(stream, gate.device))
     _native.check(status, "mla_split_combine")
     return out, lse
+
+
+def mla_kv_append(latent_new, rope_new, slab, page_table, seq_lens, n_new, *, status=None,
+                  stream=None):
+    """Write each request's n_new new latent / rope rows into the page pool.
+
+    latent_new [R*n_new, 512] and rope_new [R*n_new, 64] bf16 (row r*n_new + j is
+    request r's new token j); slab, page_table as for mla_decode; seq_lens [R]
+    int32 histories after the append, so token j lands at position
+    seq_lens[r] - n_new + j.  ``status``: optional CUDA int32 tensor of one
+    element that the kernel sets to 32 (a history shorter than n_new) or 33 (a
+    page ID outside the pool); such rows are skipped.  Asynchronous.
+    """
+    R = int(seq_lens.shape[0]) if hasattr(seq_lens, "shape") else 0
+    _require(seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+             and seq_lens.dim() == 1, "seq_lens must be a contiguous CUDA int32 vector")
+    _check_bf16(latent_new, "latent_new", (R * n_new, 512))
+    _check_bf16(rope_new, "rope_new", (R * n_new, 64))
+    _require(slab.is_cuda and slab.dtype == torch.bfloat16 and slab.dim() == 2
+             and slab.stride(1) == 1, "slab must be a CUDA bf16 [num_pages, page_stride] view")
+    _require(slab.shape[1] >= PAGE_TOKENS * ROW, "slab page too small")
+    _require(page_table.is_cuda and page_table.dtype == torch.int32 and page_table.dim() == 2
+             and page_table.shape[0] == R and page_table.stride(1) == 1,
+             "page_table must be a CUDA int32 [R, >= pages] view with unit column stride")
+    if status is not None:
+        _require(status.is_cuda and status.dtype == torch.int32 and status.numel() >= 1,
+                 "status must be a CUDA int32 tensor")
+    rc = _native.lib().mla_kv_append(
+        latent_new.data_ptr(), rope_new.data_ptr(), slab.data_ptr(), slab.shape[0],
+        slab.stride(0), page_table.data_ptr(), page_table.stride(0), seq_lens.data_ptr(), R,
+        int(n_new), None if status is None else status.data_ptr(),
+        _stream_ptr(stream, slab.device))
+    _native.check(rc, "mla_kv_append")

@@ -27,6 +27,7 @@ SOURCES = [
     "plmla_combine.cu",
     "plmla_decode_tc.cu",
     "plmla_static_scratch.cu",
+    "plmla_append.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -340,3 +340,31 @@ extern "C" plmla_status mla_decode(const void *q_nope_absorbed, const void *q_ro
                          scale, out, lse, workspace, workspace_bytes, cta_budget,
                          min_splits_per_req, stream, nullptr);
 }
+
+extern "C" plmla_status mla_kv_append(const void *latent_new, const void *rope_new,
+                                      void *slab_base, int64_t num_pages,
+                                      int64_t page_stride_elems, const int32_t *page_table,
+                                      int64_t page_table_ld, const int32_t *seq_lens,
+                                      int32_t num_reqs, int32_t n_new, int32_t *status,
+                                      void *stream)
+{
+    if (num_reqs < 1 || n_new < 0)
+        return PLMLA_INVALID_ARGUMENT;
+    if (n_new == 0)
+        return PLMLA_OK;
+    if (latent_new == nullptr || rope_new == nullptr || slab_base == nullptr ||
+        page_table == nullptr || seq_lens == nullptr)
+        return PLMLA_INVALID_ARGUMENT;
+    if (!aligned(latent_new, 16) || !aligned(rope_new, 16) || !aligned(slab_base, 16) ||
+        !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
+        (status != nullptr && !aligned(status, 4)))
+        return PLMLA_INVALID_ARGUMENT;
+    if (num_pages < 1 || page_table_ld < 1 || page_stride_elems < (int64_t)kPageTokens * kRow ||
+        page_stride_elems % 8 != 0)
+        return PLMLA_INVALID_ARGUMENT;
+    const cudaError_t err = launch_append(latent_new, rope_new, slab_base, num_pages,
+                                          page_stride_elems, page_table, page_table_ld, seq_lens,
+                                          num_reqs, n_new, status,
+                                          static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
+}

@@ -102,6 +102,14 @@ cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream);
 // lives in group g = rw / group_rows at row rw % group_rows of the partials
 // of segments [g*stride + indptr[r], g*stride + indptr[r + 1]), where stride is
 // *seg_stride (or 0 when seg_stride is null).
+// KV append (plmla_append.cu): status codes it writes for a bad row.
+constexpr int32_t kStatusAppendPosition = 32;   // seq_lens[r] < n_new
+constexpr int32_t kStatusAppendPage = 33;       // page ID outside [0, num_pages)
+cudaError_t launch_append(const void *latent, const void *rope, void *slab, int64_t num_pages,
+                          int64_t page_stride, const int32_t *table, int64_t table_ld,
+                          const int32_t *seq_lens, int num_reqs, int n_new, int32_t *status,
+                          cudaStream_t stream);
+
 // With `done` (and `status`) set, the combine is launched while the decode is
 // still running and waits, per request, until done[team * R + r] counts all of
 // the request's segments; without it, it waits for the previous grid to finish.
