@@ -45,10 +45,10 @@ def _load():
         build_oracle()
     lib = ctypes.CDLL(_LIB_PATH)
     i64, p = ctypes.c_int64, ctypes.c_void_p
-    lib.oracle_attend_rows.restype = ctypes.c_int
-    lib.oracle_attend_rows.argtypes = [p, p, p, i64, i64, i64, i64, p, i64, p, i64, i64, i64,
-                                       i64, i64, ctypes.c_double, p, i64, i64, i64, p, p,
-                                       ctypes.c_int]
+    dbl, c_int = ctypes.c_double, ctypes.c_int
+    lib.oracle_attend_rows.restype = c_int
+    lib.oracle_attend_rows.argtypes = [p, p, p, c_int, dbl, i64, i64, i64, i64, p, i64, p, i64,
+                                       i64, i64, i64, i64, dbl, p, i64, i64, i64, p, p, p, c_int]
     _lib = lib
     return lib
 
@@ -64,6 +64,34 @@ def _u16(a) -> np.ndarray:
     return a
 
 
+def _u8(a) -> np.ndarray:
+    """Byte data (E4M3 codes) as a contiguous uint8 numpy array (accepts torch
+    uint8 / float8 tensors)."""
+    if hasattr(a, "detach"):
+        import torch
+        a = a.detach().contiguous().cpu()
+        if a.dtype != torch.uint8:
+            a = a.view(torch.uint8)
+        a = a.numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint8:
+        a = a.view(np.uint8)
+    return a
+
+
+def _as_f64(a) -> np.ndarray:
+    """Query values as contiguous float64: bf16 (torch tensor or uint16 bit
+    patterns) widened exactly, any float array converted."""
+    if hasattr(a, "dtype") and str(a.dtype) == "torch.bfloat16":
+        return np.ascontiguousarray(_bf16_to_f64(a))
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return np.ascontiguousarray(_bf16_to_f64(a))
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
 def _i32(a) -> np.ndarray:
     if hasattr(a, "cpu"):
         a = a.detach().cpu().numpy()
@@ -74,19 +102,35 @@ def default_threads() -> int:
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
 
 
+def _bf16_to_f64(a) -> np.ndarray:
+    """bf16 bit patterns (or a torch bf16 tensor) widened exactly to float64."""
+    u = _u16(a).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
 def attend_rows(q_nope, q_rope, slab, page_table, seq_lens, n_q, num_heads, scale, *,
                 num_pages, page_stride=None, page_tokens=PAGE_TOKENS, dc=DC, dr=DR,
-                rows=None, t_lo=0, t_hi=None, threads=None):
+                rows=None, t_lo=0, t_hi=None, threads=None, kv_format="bf16", kv_scale=1.0,
+                with_abs=False):
     """Ungated softmax attention over the paged latent history.
 
-    Returns (o, lse): o is [n_rows, dc] float64, lse is [n_rows] float64
-    (natural log; -inf where the row sees no token).  ``rows`` lists flat row
-    ids (r*n_q + j)*H + h; None means every row in that order.  ``[t_lo, t_hi)``
-    restricts the tokens (a KV chunk); the causal limit of draft token j is
-    seq_lens[r] - (n_q - 1 - j).
+    Returns (o, lse), or (o, lse, o_abs) with ``with_abs``: o is [n_rows, dc]
+    float64, lse is [n_rows] float64 (natural log; -inf where the row sees no
+    token), o_abs the probability-weighted absolute latent sum_t w_t |c_t|.
+    ``rows`` lists flat row ids (r*n_q + j)*H + h; None means every row in that
+    order.  ``[t_lo, t_hi)`` restricts the tokens (a KV chunk); the causal limit
+    of draft token j is seq_lens[r] - (n_q - 1 - j).  The queries are bf16 (or
+    any float array, taken as float64).  ``kv_format`` "e4m3": the slab holds
+    E4M3 bytes and an element's value is kv_scale times the decoded byte.
     """
     lib = _load()
-    qn, qr, sl = _u16(q_nope), _u16(q_rope), _u16(slab)
+    qn, qr = _as_f64(q_nope), _as_f64(q_rope)
+    if kv_format == "bf16":
+        sl, fp8 = _u16(slab), 0
+    elif kv_format == "e4m3":
+        sl, fp8 = _u8(slab), 1
+    else:
+        raise ValueError(kv_format)
     pt, lens = _i32(page_table), _i32(seq_lens)
     R = lens.shape[0]
     if pt.ndim == 1:
@@ -102,19 +146,22 @@ def attend_rows(q_nope, q_rope, slab, page_table, seq_lens, n_q, num_heads, scal
         rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         n_rows = rows_arr.shape[0]
     o = np.zeros((n_rows, dc), dtype=np.float64)
+    o_abs = np.zeros((n_rows, dc), dtype=np.float64) if with_abs else None
     lse = np.zeros((n_rows,), dtype=np.float64)
     if t_hi is None:
         t_hi = np.iinfo(np.int64).max
     rc = lib.oracle_attend_rows(
-        qn.ctypes.data, qr.ctypes.data, sl.ctypes.data, num_pages, page_stride, page_tokens,
-        row_elems, pt.ctypes.data, table_ld, lens.ctypes.data, R, n_q, num_heads, dc, dr,
-        float(scale), rows_arr.ctypes.data if rows_arr is not None else None, n_rows,
-        int(t_lo), int(t_hi), o.ctypes.data, lse.ctypes.data, int(threads or default_threads()))
+        qn.ctypes.data, qr.ctypes.data, sl.ctypes.data, fp8, float(kv_scale), num_pages,
+        page_stride, page_tokens, row_elems, pt.ctypes.data, table_ld, lens.ctypes.data, R, n_q,
+        num_heads, dc, dr, float(scale), rows_arr.ctypes.data if rows_arr is not None else None,
+        n_rows, int(t_lo), int(t_hi), o.ctypes.data,
+        o_abs.ctypes.data if o_abs is not None else None, lse.ctypes.data,
+        int(threads or default_threads()))
     if rc == -1:
         raise IndexError("page table entry outside the pool")
     if rc != 0:
         raise MemoryError("oracle allocation failed")
-    return o, lse
+    return (o, lse, o_abs) if with_abs else (o, lse)
 
 
 def gate_sigmoid(o, gate_logits):
@@ -262,4 +309,148 @@ def kv_append(slab, page_table, seq_lens, latent_new, rope_new, n_new, *,
             base = page * page_stride + (p % page_tokens) * row_elems
             flat[base:base + dc] = lat[r * n_new + j]
             flat[base + dc:base + row_elems] = rope[r * n_new + j]
+    return flat.reshape(shape)
+
+
+# --------------------------------------------------------------------------
+# FP8 pages.  The deployment keeps its MLA cache in FP8 (TokenSpeed AgentX post,
+# memory-budget paragraph: FP8 target/drafter KV cache), and the AMD notes of
+# the AgentX - InferenceXv3 report name the encoding (float8_e4m3fn, as opposed
+# to gfx942's e4m3fnuz).  The pages give no scale granularity; the reading here
+# is one float scale per cache tensor: element value = kv_scale * decoded byte.
+# The FP8 tensor-core path multiplies FP8 by FP8, so the decode also quantises
+# each query row to E4M3 with a power-of-two scale; that step is part of what
+# the FP8 decode computes and the oracle takes it exactly.
+# --------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """E4M3 bytes -> float64: sign bit, 4 exponent bits (bias 7), 3 mantissa
+    bits; exponent 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN."""
+    c = _u8(codes).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    v = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    v = np.where((e == 15) & ((c & 7) == 7), np.nan, v)
+    return sign * v
+
+
+_E4M3_POS = None
+
+
+def _e4m3_table() -> np.ndarray:
+    global _E4M3_POS
+    if _E4M3_POS is None:
+        _E4M3_POS = e4m3_decode(np.arange(127, dtype=np.uint8))   # 0 .. 448, increasing
+    return _E4M3_POS
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round float values to E4M3 bytes: nearest representable magnitude, ties
+    to the even code, magnitudes above 448 saturated to 448, NaN -> 0x7F, the
+    sign kept (also for a zero result)."""
+    x = np.asarray(x, dtype=np.float64)
+    ax = np.abs(x)
+    tab = _e4m3_table()
+    hi = np.clip(np.searchsorted(tab, np.minimum(ax, E4M3_MAX), side="left"), 0, 126)
+    lo = np.clip(hi - 1, 0, 126)
+    d_lo = np.minimum(ax, E4M3_MAX) - tab[lo]
+    d_hi = tab[hi] - np.minimum(ax, E4M3_MAX)
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def query_scale_exponent(amax) -> np.ndarray:
+    """Per-row power-of-two scale 2^e of the FP8 query: the smallest e with
+    amax * 2^-e <= 448 (E4M3's largest finite value), e >= -126; e = 0 for an
+    all-zero row."""
+    amax = np.asarray(amax, dtype=np.float64)
+    f, E = np.frexp(amax)                    # amax = f * 2^E, f in [0.5, 1)
+    k = E - 1                                # amax = (2f) * 2^k, 2f in [1, 2)
+    e = np.where(2.0 * f <= 1.75, k - 8, k - 7)
+    e = np.maximum(e, -126)
+    return np.where(amax == 0, 0, e).astype(np.int32)
+
+
+def quantize_query_rows(q_nope, q_rope):
+    """FP8 queries: rows of [q_nope | q_rope] (dc + dr values) as E4M3 codes of
+    q * 2^-e, with e = query_scale_exponent(max |q| over the row).  Returns
+    (codes [rows, dc + dr] uint8, exps [rows] int32)."""
+    qn, qr = _as_f64(q_nope), _as_f64(q_rope)
+    qn = qn.reshape(-1, qn.shape[-1])
+    qr = qr.reshape(-1, qr.shape[-1])
+    q = np.concatenate([qn, qr], axis=1)
+    e = query_scale_exponent(np.max(np.abs(q), axis=1))
+    codes = e4m3_encode(np.ldexp(q, -e[:, None].astype(np.int64)))
+    return codes, e
+
+
+def dequantize_query_rows(codes, exps) -> np.ndarray:
+    """float64 values of FP8 query rows: decoded byte * 2^e (exact)."""
+    return np.ldexp(e4m3_decode(codes), np.asarray(exps, dtype=np.int64)[:, None])
+
+
+def mla_decode_e4m3_reference(q_nope, q_rope, gate, slab8, kv_scale, page_table, seq_lens, n_q,
+                              num_heads, scale, *, num_pages, page_stride=None,
+                              page_tokens=PAGE_TOKENS, dc=DC, dr=DR, rows=None, threads=None,
+                              with_abs=False):
+    """Gated MLA decode over E4M3 pages with FP8 queries.
+
+    Every query row is quantised as quantize_query_rows does; the scores, the
+    softmax and the latent sum then follow the bf16 definition on the
+    dequantised values (kv_scale * decoded byte for the cache).  Returns (out,
+    lse), or (out, lse, bound) with ``with_abs``, bound = sigmoid(g) * sum_t w_t
+    |c_t|, the gated probability-weighted absolute latent."""
+    codes, exps = quantize_query_rows(q_nope, q_rope)
+    qd = dequantize_query_rows(codes, exps)
+    res = attend_rows(qd[:, :dc], qd[:, dc:], slab8, page_table, seq_lens, n_q, num_heads, scale,
+                      num_pages=num_pages, page_stride=page_stride, page_tokens=page_tokens,
+                      dc=dc, dr=dr, rows=rows, threads=threads, kv_format="e4m3",
+                      kv_scale=kv_scale, with_abs=with_abs)
+    g = _bf16_to_f64(gate).reshape(-1, dc)
+    if rows is not None:
+        g = g[np.asarray(rows, dtype=np.int64)]
+    out = gate_sigmoid(res[0], g)
+    if with_abs:
+        return out, res[1], gate_sigmoid(res[2], g)
+    return out, res[1]
+
+
+def kv_append_e4m3(slab8, page_table, seq_lens, latent_new, rope_new, n_new, kv_scale, *,
+                   page_tokens=PAGE_TOKENS, page_stride=None, dc=DC, dr=DR):
+    """kv_append into E4M3 pages: each new bf16 value x is stored as the E4M3
+    code of x / kv_scale, the quotient taken in float32 (x and kv_scale as
+    float32, one correctly rounded division).  Positions, pages and errors as in
+    kv_append."""
+    sl = _u8(slab8).copy()
+    shape = sl.shape
+    flat = sl.reshape(-1)
+    pt, lens = _i32(page_table), _i32(seq_lens)
+    R = lens.shape[0]
+    if pt.ndim == 1:
+        pt = pt.reshape(R, -1)
+    row_elems = dc + dr
+    if page_stride is None:
+        page_stride = page_tokens * row_elems
+    num_pages = flat.size // page_stride
+    s32 = np.float32(kv_scale)
+    lat = (_bf16_to_f64(latent_new).astype(np.float32) / s32).reshape(R * n_new, dc)
+    rope = (_bf16_to_f64(rope_new).astype(np.float32) / s32).reshape(R * n_new, dr)
+    lat_c, rope_c = e4m3_encode(lat), e4m3_encode(rope)
+    for r in range(R):
+        for j in range(n_new):
+            p = int(lens[r]) - n_new + j
+            if p < 0:
+                raise IndexError("new token before the start of the history")
+            page = int(pt[r, p // page_tokens])
+            if page < 0 or page >= num_pages:
+                raise IndexError("page table entry outside the pool")
+            base = page * page_stride + (p % page_tokens) * row_elems
+            flat[base:base + dc] = lat_c[r * n_new + j]
+            flat[base + dc:base + row_elems] = rope_c[r * n_new + j]
     return flat.reshape(shape)

@@ -37,6 +37,14 @@
  * The sigmoid output gate is applied by the Python side of the oracle.
  *
  * All arithmetic is in double; bf16 inputs are widened exactly.
+ *
+ * FP8 pages: the deployment keeps its MLA cache in FP8 (TokenSpeed AgentX post,
+ * memory-budget paragraph: "FP8 target/drafter KV cache").  With kv_fp8 set,
+ * every slab element is one OCP E4M3 byte (1 sign bit, 4 exponent bits with
+ * bias 7, 3 mantissa bits; exponent 0 is subnormal, S.1111.111 is NaN, there is
+ * no infinity) and the stored value is kv_scale times the decoded number.
+ * The query is passed in double, so the caller decides what it is (for the FP8
+ * decode: the dequantised FP8 query).
  */
 #include <math.h>
 #include <stdint.h>
@@ -51,18 +59,47 @@ static double bf16_to_double(uint16_t bits)
     return (double)f;
 }
 
+/* OCP E4M3: value = (-1)^s * 2^(e-7) * (1 + m/8) for e >= 1, (-1)^s * 2^-6 * m/8
+ * for e = 0; e = 15 with m = 7 is NaN. */
+static double e4m3_to_double(uint8_t b)
+{
+    int sign = b >> 7, e = (b >> 3) & 0xF, m = b & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -v : v;
+}
+
+/* Element `idx` of the slab as a double: a bf16 value, or kv_scale times an
+ * E4M3 value. */
+static double kv_elem(const void *slab, int64_t idx, int kv_fp8, double kv_scale)
+{
+    if (kv_fp8)
+        return kv_scale * e4m3_to_double(((const uint8_t *)slab)[idx]);
+    return bf16_to_double(((const uint16_t *)slab)[idx]);
+}
+
 /* Attention for one output row.  Returns 0 on success, -1 if a page index read
- * from the page table lies outside [0, num_pages). */
-static int attend_one_row(const uint16_t *qn, const uint16_t *qr, const uint16_t *slab,
-                          int64_t num_pages, int64_t page_stride, int64_t page_tokens,
-                          int64_t row_elems, const int32_t *table_row, int64_t L_eff,
-                          int64_t t_lo, int64_t t_hi, int64_t dc, int64_t dr, double scale,
-                          double *o_out, double *lse_out, double *scores)
+ * from the page table lies outside [0, num_pages).  o_abs (may be NULL)
+ * receives sum_t w_t |c_t[d]|, the probability-weighted absolute latent. */
+static int attend_one_row(const double *qn, const double *qr, const void *slab, int kv_fp8,
+                          double kv_scale, int64_t num_pages, int64_t page_stride,
+                          int64_t page_tokens, int64_t row_elems, const int32_t *table_row,
+                          int64_t L_eff, int64_t t_lo, int64_t t_hi, int64_t dc, int64_t dr,
+                          double scale, double *o_out, double *o_abs, double *lse_out,
+                          double *scores)
 {
     int64_t lo = t_lo < 0 ? 0 : t_lo;
     int64_t hi = t_hi < L_eff ? t_hi : L_eff;
-    for (int64_t d = 0; d < dc; ++d)
+    for (int64_t d = 0; d < dc; ++d) {
         o_out[d] = 0.0;
+        if (o_abs)
+            o_abs[d] = 0.0;
+    }
     if (hi <= lo) {
         *lse_out = -INFINITY;
         return 0;
@@ -73,12 +110,12 @@ static int attend_one_row(const uint16_t *qn, const uint16_t *qr, const uint16_t
         int64_t page = table_row[t / page_tokens];
         if (page < 0 || page >= num_pages)
             return -1;
-        const uint16_t *x = slab + page * page_stride + (t % page_tokens) * row_elems;
+        int64_t x = page * page_stride + (t % page_tokens) * row_elems;
         double dot = 0.0;
         for (int64_t d = 0; d < dc; ++d)
-            dot += bf16_to_double(qn[d]) * bf16_to_double(x[d]);
+            dot += qn[d] * kv_elem(slab, x + d, kv_fp8, kv_scale);
         for (int64_t d = 0; d < dr; ++d)
-            dot += bf16_to_double(qr[d]) * bf16_to_double(x[dc + d]);
+            dot += qr[d] * kv_elem(slab, x + dc + d, kv_fp8, kv_scale);
         double s = scale * dot;
         scores[t - lo] = s;
         if (s > m)
@@ -90,10 +127,14 @@ static int attend_one_row(const uint16_t *qn, const uint16_t *qr, const uint16_t
         Z += exp(scores[t - lo] - m);
     for (int64_t t = lo; t < hi; ++t) {
         int64_t page = table_row[t / page_tokens];
-        const uint16_t *x = slab + page * page_stride + (t % page_tokens) * row_elems;
+        int64_t x = page * page_stride + (t % page_tokens) * row_elems;
         double p = exp(scores[t - lo] - m) / Z;
-        for (int64_t d = 0; d < dc; ++d)
-            o_out[d] += p * bf16_to_double(x[d]);
+        for (int64_t d = 0; d < dc; ++d) {
+            double c = kv_elem(slab, x + d, kv_fp8, kv_scale);
+            o_out[d] += p * c;
+            if (o_abs)
+                o_abs[d] += p * fabs(c);
+        }
     }
     *lse_out = m + log(Z);
     return 0;
@@ -103,24 +144,27 @@ static int attend_one_row(const uint16_t *qn, const uint16_t *qr, const uint16_t
  * oracle_attend_rows -- ungated attention output and log-sum-exp for a list of
  * output rows.
  *
- * q_nope   [R*n_q, H, dc] bf16 (absorbed query, latent part)
- * q_rope   [R*n_q, H, dr] bf16
+ * q_nope   [R*n_q, H, dc] double (absorbed query, latent part)
+ * q_rope   [R*n_q, H, dr] double
  * slab     num_pages pages, page p at element offset p*page_stride; token i of a
- *          page at i*row_elems; row = dc latent values then dr rope values
+ *          page at i*row_elems; row = dc latent values then dr rope values;
+ *          bf16 elements, or E4M3 bytes times kv_scale when kv_fp8 != 0
  * page_table [R, table_ld] int32 global page IDs
  * seq_lens [R] int32 (includes the n_q draft tokens)
  * rows     [n_rows] flat row ids ((r*n_q + j)*H + h); NULL means all rows
  * t_lo, t_hi  token window applied to every row (partial-state evaluation)
- * o        [n_rows, dc] double, lse [n_rows] double (outputs)
+ * o        [n_rows, dc] double, lse [n_rows] double (outputs); o_abs [n_rows, dc]
+ *          (NULL allowed) the probability-weighted absolute latent
  *
  * Returns 0, or -1 if a page ID is out of range, or -2 on allocation failure.
  */
-int oracle_attend_rows(const uint16_t *q_nope, const uint16_t *q_rope, const uint16_t *slab,
-                       int64_t num_pages, int64_t page_stride, int64_t page_tokens,
-                       int64_t row_elems, const int32_t *page_table, int64_t table_ld,
-                       const int32_t *seq_lens, int64_t R, int64_t n_q, int64_t H, int64_t dc,
-                       int64_t dr, double scale, const int64_t *rows, int64_t n_rows,
-                       int64_t t_lo, int64_t t_hi, double *o, double *lse, int num_threads)
+int oracle_attend_rows(const double *q_nope, const double *q_rope, const void *slab, int kv_fp8,
+                       double kv_scale, int64_t num_pages, int64_t page_stride,
+                       int64_t page_tokens, int64_t row_elems, const int32_t *page_table,
+                       int64_t table_ld, const int32_t *seq_lens, int64_t R, int64_t n_q,
+                       int64_t H, int64_t dc, int64_t dr, double scale, const int64_t *rows,
+                       int64_t n_rows, int64_t t_lo, int64_t t_hi, double *o, double *o_abs,
+                       double *lse, int num_threads)
 {
     int64_t total_rows = R * n_q * H;
     if (rows == NULL)
@@ -141,15 +185,14 @@ int oracle_attend_rows(const uint16_t *q_nope, const uint16_t *q_rope, const uin
                 continue;
             }
             int64_t row = rows ? rows[i] : i;
-            int64_t h = row % H;
             int64_t tok = row / H; /* r*n_q + j */
             int64_t r = tok / n_q;
             int64_t j = tok % n_q;
             int64_t L_eff = (int64_t)seq_lens[r] - (n_q - 1 - j);
-            int rc = attend_one_row(q_nope + row * dc, q_rope + row * dr, slab, num_pages,
-                                    page_stride, page_tokens, row_elems,
+            int rc = attend_one_row(q_nope + row * dc, q_rope + row * dr, slab, kv_fp8, kv_scale,
+                                    num_pages, page_stride, page_tokens, row_elems,
                                     page_table + r * table_ld, L_eff, t_lo, t_hi, dc, dr, scale,
-                                    o + i * dc, lse + i, scores);
+                                    o + i * dc, o_abs ? o_abs + i * dc : NULL, lse + i, scores);
             if (rc != 0) {
 #pragma omp atomic write
                 status = rc;
