@@ -36,7 +36,9 @@ UNIT = "GB/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
-KERNELS_PER_STEP = 3          # plan, split decode, combine+gate
+KERNELS_PER_STEP = 3          # plan (and, for FP8 pages, the query quantiser), split decode,
+                              # combine+gate
+KV_SCALE_FP8 = 6.0 / 448.0    # the synthetic FP8 cache's scale
 DECODE_SOURCES = ["plmla_decode_tc.cu", "plmla_internal.cuh"]
 
 
@@ -51,6 +53,9 @@ def parse_args(argv=None):
                          "writing a block of new rows per request into the same pool")
     ap.add_argument("--append-tokens", type=int, default=4096,
                     help="new tokens per request for --op append")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="cache format: bf16 pages (the default workload) or E4M3 pages "
+                         "(the deployment's FP8 cache, 576 bytes per token row)")
     ap.add_argument("--workload", default="steady",
                     choices=["tiny", "steady", "agentic", "spec", "long"])
     ap.add_argument("--no-e2e", action="store_true")
@@ -206,10 +211,11 @@ def decode_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload, kv_bytes):
+def profiled_traffic(workload, kv_bytes, fp8=False):
     """DRAM bytes per decode launch from the committed ncu summary, if it was
     taken on the current decode kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.json")
+    name = f"decode_{workload}_fp8_traffic.json" if fp8 else f"decode_{workload}_traffic.json"
+    path = os.path.join(ROOT, "profiles", name)
     try:
         with open(path) as f:
             rec = json.load(f)
@@ -244,29 +250,38 @@ def oracle_sample(w, qn, qr, gate, slab_dev, req_ids):
             len(phys))
 
 
-def run_oracle(w, sample):
+def run_oracle(w, sample, kv_scale=None):
     import oracle
     qn, qr, gate, slab, table, lens, npages = sample
     t = time.perf_counter()
-    oracle.mla_decode_reference(qn, qr, gate, slab, table, lens, w.n_q, w.num_heads,
-                                1.0 / math.sqrt(192.0), num_pages=npages,
-                                page_stride=w.page_stride)
+    if kv_scale is None:
+        oracle.mla_decode_reference(qn, qr, gate, slab, table, lens, w.n_q, w.num_heads,
+                                    1.0 / math.sqrt(192.0), num_pages=npages,
+                                    page_stride=w.page_stride)
+    else:
+        oracle.mla_decode_e4m3_reference(qn, qr, gate, slab, kv_scale, table, lens, w.n_q,
+                                         w.num_heads, 1.0 / math.sqrt(192.0), num_pages=npages,
+                                         page_stride=w.page_stride)
     return time.perf_counter() - t
 
 
-def cpu_baseline(w, qn, qr, gate, slab_dev, target_s):
+def kv_row_bytes(w, fp8):
+    return (w.dc + w.dr) * (1 if fp8 else 2)
+
+
+def cpu_baseline(w, qn, qr, gate, slab_dev, target_s, kv_scale=None):
     import oracle
     cores = oracle.oracle.default_threads()
     order = list(range(w.num_reqs))
     one = oracle_sample(w, qn, qr, gate, slab_dev, order[:1])
-    t1 = run_oracle(w, one)
+    t1 = run_oracle(w, one, kv_scale)
     n = max(1, min(w.num_reqs, int(target_s / max(t1, 1e-3))))
     sample = oracle_sample(w, qn, qr, gate, slab_dev, order[:n])
     elapsed, reps = 0.0, 0
     while elapsed < 0.5 * target_s or reps == 0:
-        elapsed += run_oracle(w, sample)
+        elapsed += run_oracle(w, sample, kv_scale)
         reps += 1
-    kv = int(sum(int(w.seq_lens[r]) for r in order[:n])) * (w.dc + w.dr) * 2
+    kv = int(sum(int(w.seq_lens[r]) for r in order[:n])) * kv_row_bytes(w, kv_scale is not None)
     gbs = kv * reps / elapsed / 1e9
     return {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} of {w.num_reqs} requests x all {w.num_heads} heads, {reps} pass(es), "
@@ -278,10 +293,11 @@ def cpu_baseline(w, qn, qr, gate, slab_dev, target_s):
 # GPU arm
 # --------------------------------------------------------------------------
 
-def workload_description(w):
+def workload_description(w, fp8=False):
     lens = w.seq_lens
+    fmt = (f"E4M3 (FP8 cache, kv_scale {KV_SCALE_FP8:.6g})" if fp8 else "bf16")
     return (f"{w.name} decode: {w.num_reqs} requests x {w.n_q} query token(s), {w.num_heads} "
-            f"heads, 512 latent + 64 rope bf16, histories {int(lens.min())}..{int(lens.max())} "
+            f"heads, 512 latent + 64 rope {fmt}, histories {int(lens.min())}..{int(lens.max())} "
             f"tokens (sum {int(lens.sum())}), {w.num_pages} pages of 1536 tokens, "
             f"{w.num_slabs} slab(s), seed {w.seed}")
 
@@ -297,17 +313,24 @@ def run_gpu(args):
     dist = dist_init(world, "nccl")
 
     w = inputs.make_workload(args.workload)
+    fp8 = args.kv == "fp8"
     layers = w.num_slabs
     qs = [inputs.make_queries(w, device, layer=l) for l in range(layers)]
-    slabs = [inputs.make_slab(w, device, layer=l) for l in range(layers)]
+    if fp8:
+        slabs = [inputs.make_slab_e4m3(w, device, layer=l, kv_scale=KV_SCALE_FP8)
+                 for l in range(layers)]
+    else:
+        slabs = [inputs.make_slab(w, device, layer=l) for l in range(layers)]
     table = torch.as_tensor(w.page_table, device=device)
     lens = torch.as_tensor(w.seq_lens, device=device)
-    ws = plmla.allocate_workspace(w.num_reqs, w.n_q, w.num_heads, 0, w.min_splits, device)
+    ws = plmla.allocate_workspace(w.num_reqs, w.n_q, w.num_heads, 0, w.min_splits, device,
+                                  fp8=fp8)
     outs = [torch.empty_like(q[0]) for q in qs]
     lses = [torch.empty(w.num_tokens, w.num_heads, dtype=torch.float32, device=device)
             for _ in qs]
-    kv_bytes_layer = w.kv_bytes_per_layer
+    kv_bytes_layer = w.kv_tokens * kv_row_bytes(w, fp8)
     kv_bytes_step = kv_bytes_layer * layers
+    decode = decoder(plmla, fp8)
 
     K, W = args.steps, args.warmup
     n_ev = K * layers
@@ -320,9 +343,9 @@ def run_gpu(args):
     def step(ev_base=None):
         for l in range(layers):
             qn, qr, gate = qs[l]
-            plmla.mla_decode(qn, qr, gate, slabs[l], table, lens, n_q=w.n_q, out=outs[l],
-                             lse=lses[l], workspace=ws, min_splits=w.min_splits,
-                             events=None if ev_base is None else evs[ev_base + l])
+            decode(qn, qr, gate, slabs[l], table, lens, n_q=w.n_q, out=outs[l],
+                   lse=lses[l], workspace=ws, min_splits=w.min_splits,
+                   events=None if ev_base is None else evs[ev_base + l])
 
     for _ in range(W):
         step()
@@ -365,7 +388,7 @@ def run_gpu(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, qs, slabs, table, lens, ws, device, dist)
+        e2e = run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode, kv_bytes_layer)
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(host_t0, host_t1)
@@ -377,10 +400,13 @@ def run_gpu(args):
     peak, peak_src = hbm_peak()
     dec_avg = statistics.mean(decode_ms)
     achieved = kv_bytes_layer / (dec_avg / 1e3) / 1e9
-    traffic = profiled_traffic(args.workload, kv_bytes_layer)
+    traffic = profiled_traffic(args.workload, kv_bytes_layer, fp8)
     # Which roofline bounds the decode: 2 * (576 + 512) flop per (query row, KV
     # token) against 1,152 bytes per KV token, compared with the measured ridge.
     tpeak, tpeak_src = tensor_peak()
+    if fp8:
+        # E4M3 MMAs run at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s dense)
+        tpeak, tpeak_src = 2.0 * tpeak, tpeak_src + " x 2 (nominal E4M3 / bf16 ratio)"
     flops_layer = 2.0 * (w.dc + w.dr + w.dc) * w.n_q * w.num_heads * w.kv_tokens
     intensity = flops_layer / kv_bytes_layer
     ridge = tpeak * 1e12 / (peak * 1e9)
@@ -401,8 +427,9 @@ def run_gpu(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_description(w), "requests": w.num_reqs,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if fp8 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload_description(w, fp8), "requests": w.num_reqs,
                    "n_q": w.n_q, "heads": w.num_heads, "layers": layers,
                    "kv_tokens": w.kv_tokens, "kv_bytes_per_step": kv_bytes_step,
                    "l2": "inputs larger than L2 (KV per step >> 129 MB L2), no flush",
@@ -424,15 +451,24 @@ def run_gpu(args):
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, qs[0][0], qs[0][1], qs[0][2], slabs[0],
-                                            args.cpu_seconds)
+                                            args.cpu_seconds, KV_SCALE_FP8 if fp8 else None)
     return line
 
 
-def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist):
+def decoder(plmla, fp8):
+    """The public decode call for the cache format."""
+    if not fp8:
+        return plmla.mla_decode
+
+    def decode_fp8(*a, **k):
+        return plmla.mla_decode_fp8(*a, kv_scale=KV_SCALE_FP8, **k)
+    return decode_fp8
+
+
+def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode, kv_bytes_layer):
     """Same metric through the public call with pinned host buffers: each step
     copies its inputs host->device, decodes, and reads the result back."""
     import torch
-    import paged_latent_attention_gb300 as plmla
     layers = w.num_slabs
     host_q = [[t.cpu().pin_memory() for t in q] for q in qs]
     host_table = table.cpu().pin_memory()
@@ -456,9 +492,9 @@ def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist):
         for l in range(layers):
             for d, h in zip(dev_q[l], host_q[l]):
                 d.copy_(h, non_blocking=True)
-            plmla.mla_decode(dev_q[l][0], dev_q[l][1], dev_q[l][2], slabs[l], dev_table,
-                             dev_lens, n_q=w.n_q, out=dev_out[l], lse=dev_lse[l], workspace=ws,
-                             min_splits=w.min_splits)
+            decode(dev_q[l][0], dev_q[l][1], dev_q[l][2], slabs[l], dev_table, dev_lens,
+                   n_q=w.n_q, out=dev_out[l], lse=dev_lse[l], workspace=ws,
+                   min_splits=w.min_splits)
             host_out[l].copy_(dev_out[l], non_blocking=True)
             host_lse[l].copy_(dev_lse[l], non_blocking=True)
 
@@ -473,7 +509,7 @@ def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist):
     end.record(stream)
     torch.cuda.synchronize(device)
     ms = start.elapsed_time(end)
-    max_ms, units = aggregate(dist, ms, w.kv_bytes_per_layer * layers * args.steps, device)
+    max_ms, units = aggregate(dist, ms, kv_bytes_layer * layers * args.steps, device)
     return {"value": units / (max_ms / 1e3) / 1e9, "unit": UNIT,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": max_ms / args.steps,
@@ -689,25 +725,30 @@ def run_reference(args):
     import oracle
     from paged_latent_attention_gb300 import inputs
     w = inputs.make_workload(args.workload)
+    fp8 = args.kv == "fp8"
+    kv_scale = KV_SCALE_FP8 if fp8 else None
     qn, qr, gate = inputs.make_queries(w, "cpu")
     # the pool rows the sampled requests read, generated on the host
-    slab = inputs.make_slab(w, "cpu", pages_per_chunk=16) if w.num_pages <= 4096 else None
+    slab = None
+    if w.num_pages <= 4096:
+        slab = (inputs.make_slab_e4m3(w, "cpu", kv_scale=KV_SCALE_FP8, pages_per_chunk=16)
+                if fp8 else inputs.make_slab(w, "cpu", pages_per_chunk=16))
     if slab is None:
         return {"impl": "reference", "unavailable": "pool too large for a host copy"}
     cores = oracle.oracle.default_threads()
     total = args.steps + args.warmup
     budget_s = 150.0
     one = oracle_sample(w, qn, qr, gate, slab, [0])
-    t1 = run_oracle(w, one)
+    t1 = run_oracle(w, one, kv_scale)
     per_step = max(1, min(w.num_reqs, int(budget_s / total / max(t1, 1e-3))))
     times, kv = [], []
     for s in range(total):
         ids = [(s * per_step + i) % w.num_reqs for i in range(per_step)]
         sample = oracle_sample(w, qn, qr, gate, slab, ids)
-        dt = run_oracle(w, sample)
+        dt = run_oracle(w, sample, kv_scale)
         if s >= args.warmup:
             times.append(dt)
-            kv.append(sum(int(w.seq_lens[r]) for r in ids) * (w.dc + w.dr) * 2)
+            kv.append(sum(int(w.seq_lens[r]) for r in ids) * kv_row_bytes(w, fp8))
     elapsed = sum(times)
     value = sum(kv) / elapsed / 1e9
     desc = (f"{per_step} of {w.num_reqs} requests x all {w.num_heads} heads per step "
@@ -716,7 +757,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": workload_description(w)},
+        "data": "synthetic", "config": {"workload": workload_description(w, fp8)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -234,6 +234,75 @@ plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q_rope, cons
                            const plmla_stage_events *events);
 
 /*
+ * mla_workspace_size_fp8 -- workspace bytes of mla_decode_fp8 for a shape: that
+ * of mla_decode plus the quantised queries (num_reqs*n_q*num_heads rows of 576
+ * bytes and one int32 exponent each).  0 for an unsupported shape.
+ */
+size_t mla_workspace_size_fp8(int32_t num_reqs, int32_t n_q, int32_t num_heads,
+                              int32_t cta_budget, int32_t min_splits_per_req);
+
+/*
+ * mla_decode_fp8 -- mla_decode over FP8 pages, the deployment's cache format
+ * ("FP8 target/drafter KV cache": TokenSpeed AgentX post, memory-budget
+ * paragraph; float8_e4m3fn, as named in the AMD notes of the AgentX -
+ * InferenceXv3 report).
+ *
+ * Every slab element is one OCP E4M3 byte (bias 7, 3 mantissa bits, no
+ * infinity, S.1111.111 = NaN) and stands for kv_scale * its value; a token row
+ * is 576 bytes (512 latent, then 64 rope).  The queries stay bf16 at the
+ * boundary; the call quantises each query row q = [q_nope | q_rope] (576
+ * values) to E4M3 codes of q * 2^-e, with e the smallest integer >= -126 for
+ * which max|q| * 2^-e <= 448 (0 for an all-zero row), because the FP8
+ * tensor-core MMA multiplies E4M3 by E4M3.  Then, with q' = 2^e * code:
+ *
+ *   s_t = scale * kv_scale * (q'[0:512] . x_t[0:512] + q'[512:576] . x_t[512:576])
+ *   o   = kv_scale * sum_{t < L'} softmax(s)_t * x_t[0:512]
+ *   lse = ln sum_{t < L'} exp(s_t);   out = bf16_rn(sigmoid(gate) * o)
+ *
+ * computed with fp32 accumulation; the probabilities enter the value MMA as
+ * E4M3 (relative rounding <= 2^-4 per weight), their sum for the normaliser
+ * and lse stays fp32.
+ *
+ * Arguments as mla_decode, except:
+ * slab_base          E4M3 bytes, 16-byte aligned
+ * page_stride_elems  bytes from one page to the next, >= 1536*576, multiple of 16
+ * kv_scale           finite, > 0
+ * workspace_bytes    >= mla_workspace_size_fp8(...)
+ * Enqueues: plan kernel (its grid also quantises the queries) -> split-decode
+ * kernel -> combine/gate kernel.  Returns PLMLA_INVALID_ARGUMENT also for a
+ * non-finite or non-positive kv_scale.
+ */
+plmla_status mla_decode_fp8(const void *q_nope_absorbed, const void *q_rope, const void *gate,
+                            const void *slab_base, int64_t num_pages, int64_t page_stride_elems,
+                            float kv_scale, const int32_t *page_table, int64_t page_table_ld,
+                            const int32_t *seq_lens, int32_t num_reqs, int32_t n_q_per_req,
+                            int32_t num_heads, float scale, void *out, float *lse,
+                            void *workspace, size_t workspace_bytes, int32_t cta_budget,
+                            int32_t min_splits_per_req, void *stream);
+
+/*
+ * mla_quantize_queries_fp8 -- the query step of mla_decode_fp8 on its own: rows
+ * of [q_nope | q_rope] (512 + 64 bf16 values, row i at q_nope + 512 i and
+ * q_rope + 64 i) become q8[576 i .. 576 i + 575] = E4M3 codes of q * 2^-e
+ * (round to nearest even) and qexp[i] = e, the smallest integer >= -126 with
+ * max|q| * 2^-e <= 448 (0 for an all-zero row).  q_nope, q_rope and q8 16-byte
+ * aligned; rows 0 .. 2^31-1.  Asynchronous on `stream`.
+ */
+plmla_status mla_quantize_queries_fp8(const void *q_nope_absorbed, const void *q_rope,
+                                      int64_t rows, void *q8, int32_t *qexp, void *stream);
+
+/* mla_decode_fp8 with optional stage events (as mla_decode_ex). */
+plmla_status mla_decode_fp8_ex(const void *q_nope_absorbed, const void *q_rope, const void *gate,
+                               const void *slab_base, int64_t num_pages,
+                               int64_t page_stride_elems, float kv_scale,
+                               const int32_t *page_table, int64_t page_table_ld,
+                               const int32_t *seq_lens, int32_t num_reqs, int32_t n_q_per_req,
+                               int32_t num_heads, float scale, void *out, float *lse,
+                               void *workspace, size_t workspace_bytes, int32_t cta_budget,
+                               int32_t min_splits_per_req, void *stream,
+                               const plmla_stage_events *events);
+
+/*
  * mla_split_combine -- merge the partial softmax states of each request's KV
  * chunks and apply the sigmoid output gate [K3, Gated MLA decode paragraph;
  * AX, gating bullet].  Split order is fixed, so results are deterministic.
@@ -287,6 +356,20 @@ plmla_status mla_kv_append(const void *latent_new, const void *rope_new, void *s
                            int64_t num_pages, int64_t page_stride_elems, const int32_t *page_table,
                            int64_t page_table_ld, const int32_t *seq_lens, int32_t num_reqs,
                            int32_t n_new, int32_t *status, void *stream);
+
+/*
+ * mla_kv_append_fp8 -- mla_kv_append into E4M3 pages (see mla_decode_fp8): each
+ * new bf16 value x is stored as the E4M3 code of x / kv_scale (one correctly
+ * rounded fp32 division, then round to nearest even, saturating at +-448; NaN
+ * stays NaN).  Positions, pages, the status word and errors as mla_kv_append;
+ * page_stride_elems counts bytes (>= 1536*576, multiple of 16) and kv_scale
+ * must be finite and > 0.
+ */
+plmla_status mla_kv_append_fp8(const void *latent_new, const void *rope_new, void *slab_base,
+                               int64_t num_pages, int64_t page_stride_elems, float kv_scale,
+                               const int32_t *page_table, int64_t page_table_ld,
+                               const int32_t *seq_lens, int32_t num_reqs, int32_t n_new,
+                               int32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

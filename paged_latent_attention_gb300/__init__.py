@@ -8,9 +8,13 @@ from .api import (  # noqa: F401
     allocate_workspace,
     device_status,
     mla_decode,
+    mla_decode_fp8,
     mla_kv_append,
+    mla_kv_append_fp8,
     mla_plan_splits,
+    mla_quantize_queries_fp8,
     mla_split_budget,
     mla_split_combine,
     mla_workspace_size,
+    mla_workspace_size_fp8,
 )

@@ -31,6 +31,14 @@ SIGNATURES = {
     "mla_decode_static_scratch": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _p, _i64, _p, _i32,
                                                  _i32, _i32, _f, _p, _p, _i32, _i32, _p]),
     "mla_kv_append": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _p, _i64, _p, _i32, _i32, _p, _p]),
+    "mla_workspace_size_fp8": (_sz, [_i32, _i32, _i32, _i32, _i32]),
+    "mla_decode_fp8": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _f, _p, _i64, _p, _i32, _i32,
+                                      _i32, _f, _p, _p, _p, _sz, _i32, _i32, _p]),
+    "mla_decode_fp8_ex": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _f, _p, _i64, _p, _i32,
+                                         _i32, _i32, _f, _p, _p, _p, _sz, _i32, _i32, _p, _p]),
+    "mla_kv_append_fp8": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _f, _p, _i64, _p, _i32, _i32,
+                                         _p, _p]),
+    "mla_quantize_queries_fp8": (ctypes.c_int, [_p, _p, _i64, _p, _p, _p]),
 }
 
 _lib = None

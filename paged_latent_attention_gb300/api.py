@@ -58,10 +58,29 @@ def mla_workspace_size(num_reqs, n_q, num_heads, cta_budget=0, min_splits=1) -> 
     return int(n)
 
 
-def allocate_workspace(num_reqs, n_q, num_heads, cta_budget=0, min_splits=1, device=None):
-    """A caller-owned workspace tensor (uint8) of the size mla_decode needs."""
-    n = mla_workspace_size(num_reqs, n_q, num_heads, cta_budget, min_splits)
+def mla_workspace_size_fp8(num_reqs, n_q, num_heads, cta_budget=0, min_splits=1) -> int:
+    n = _native.lib().mla_workspace_size_fp8(num_reqs, n_q, num_heads, cta_budget, min_splits)
+    if n == 0:
+        raise ValueError("invalid shape for mla_workspace_size_fp8")
+    return int(n)
+
+
+def allocate_workspace(num_reqs, n_q, num_heads, cta_budget=0, min_splits=1, device=None,
+                       fp8=False):
+    """A caller-owned workspace tensor (uint8) of the size mla_decode (or, with
+    ``fp8``, mla_decode_fp8) needs."""
+    size = mla_workspace_size_fp8 if fp8 else mla_workspace_size
+    n = size(num_reqs, n_q, num_heads, cta_budget, min_splits)
     return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _byte_view(slab):
+    """An E4M3 slab as uint8 (float8_e4m3fn tensors are viewed, not copied)."""
+    if slab.dtype == torch.uint8:
+        return slab
+    _require(slab.dtype == getattr(torch, "float8_e4m3fn", None),
+             "an FP8 slab must be uint8 or float8_e4m3fn")
+    return slab.view(torch.uint8)
 
 
 def mla_decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *, n_q=1,
@@ -79,6 +98,27 @@ def mla_decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *, n_q
     page at r*576).  page_table: [R, ld] int32 with unit column stride (its row
     stride is passed through, so a strided view works).  seq_lens: [R] int32.
     """
+    return _decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, None, n_q, scale,
+                   out, lse, workspace, cta_budget, min_splits, stream, with_lse, events)
+
+
+def mla_decode_fp8(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *, kv_scale,
+                   n_q=1, scale=DEFAULT_SCALE, out=None, lse=None, workspace=None, cta_budget=0,
+                   min_splits=1, stream=None, with_lse=True, events=None):
+    """mla_decode over E4M3 pages: slab is [num_pages, page_stride] uint8 (or
+    float8_e4m3fn) holding E4M3 codes of value / kv_scale, 576 bytes per token
+    row (page_stride >= 1536*576, a multiple of 16).  The queries stay bf16;
+    the library quantises each query row to E4M3 with a power-of-two scale.
+    The workspace must come from allocate_workspace(..., fp8=True)."""
+    _require(math.isfinite(kv_scale) and kv_scale > 0, "kv_scale must be finite and > 0")
+    return _decode(q_nope_absorbed, q_rope, gate, _byte_view(slab), page_table, seq_lens,
+                   float(kv_scale), n_q, scale, out, lse, workspace, cta_budget, min_splits,
+                   stream, with_lse, events)
+
+
+def _decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, kv_scale, n_q, scale,
+            out, lse, workspace, cta_budget, min_splits, stream, with_lse, events):
+    fp8 = kv_scale is not None
     _require(q_nope_absorbed.dim() == 3, "q_nope_absorbed must be [R*n_q, H, 512]")
     T, H, _ = q_nope_absorbed.shape
     _require(T % n_q == 0, "first dimension must be num_reqs * n_q")
@@ -87,8 +127,9 @@ def mla_decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *, n_q
     _check_bf16(q_nope_absorbed, "q_nope_absorbed", (T, H, LATENT))
     _check_bf16(q_rope, "q_rope", (T, H, ROPE))
     _check_bf16(gate, "gate", (T, H, LATENT))
-    _require(slab.is_cuda and slab.dtype == torch.bfloat16 and slab.dim() == 2,
-             "slab must be a 2-D CUDA bf16 tensor [num_pages, page_stride]")
+    want = torch.uint8 if fp8 else torch.bfloat16
+    _require(slab.is_cuda and slab.dtype == want and slab.dim() == 2,
+             f"slab must be a 2-D CUDA {want} tensor [num_pages, page_stride]")
     _require(slab.stride(1) == 1, "slab pages must be contiguous")
     num_pages, page_stride = slab.shape[0], slab.stride(0)
     _require(slab.shape[1] >= PAGE_TOKENS * ROW, "slab page too small")
@@ -107,7 +148,7 @@ def mla_decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *, n_q
         _require(lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()
                  and tuple(lse.shape) == (T, H), "lse must be a contiguous CUDA fp32 [T, H]")
     if workspace is None:
-        workspace = allocate_workspace(R, n_q, H, cta_budget, min_splits, device)
+        workspace = allocate_workspace(R, n_q, H, cta_budget, min_splits, device, fp8=fp8)
     _require(workspace.is_cuda and workspace.is_contiguous(), "workspace must be CUDA memory")
     nbytes = workspace.numel() * workspace.element_size()
     ev = None
@@ -118,15 +159,37 @@ def mla_decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *, n_q
             _require(h != 0, "stage events must have been recorded once before use")
             handles.append(h)
         ev = _native.StageEvents(*handles)
-    status = _native.lib().mla_decode_ex(
-        q_nope_absorbed.data_ptr(), q_rope.data_ptr(), gate.data_ptr(), slab.data_ptr(),
-        num_pages, page_stride, page_table.data_ptr(), page_table.stride(0),
-        seq_lens.data_ptr(), R, n_q, H, float(scale), out.data_ptr(),
-        lse.data_ptr() if lse is not None else None, workspace.data_ptr(), nbytes,
-        int(cta_budget), int(min_splits), _stream_ptr(stream, device),
-        ctypes.byref(ev) if ev is not None else None)
-    _native.check(status, "mla_decode")
+    lib = _native.lib()
+    head = (q_nope_absorbed.data_ptr(), q_rope.data_ptr(), gate.data_ptr(), slab.data_ptr(),
+            num_pages, page_stride)
+    tail = (page_table.data_ptr(), page_table.stride(0), seq_lens.data_ptr(), R, n_q, H,
+            float(scale), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            workspace.data_ptr(), nbytes, int(cta_budget), int(min_splits),
+            _stream_ptr(stream, device), ctypes.byref(ev) if ev is not None else None)
+    if fp8:
+        status = lib.mla_decode_fp8_ex(*head, kv_scale, *tail)
+    else:
+        status = lib.mla_decode_ex(*head, *tail)
+    _native.check(status, "mla_decode_fp8" if fp8 else "mla_decode")
     return out, lse
+
+
+def mla_quantize_queries_fp8(q_nope_absorbed, q_rope, stream=None):
+    """The FP8 decode's query step: (codes [rows, 576] uint8, exps [rows] int32)
+    for the rows of [q_nope | q_rope] (any leading shape, flattened)."""
+    _require(q_nope_absorbed.is_cuda and q_nope_absorbed.dtype == torch.bfloat16
+             and q_nope_absorbed.is_contiguous() and q_nope_absorbed.shape[-1] == LATENT,
+             "q_nope_absorbed must be contiguous CUDA bf16 [..., 512]")
+    rows = q_nope_absorbed.numel() // LATENT
+    _require(q_rope.is_cuda and q_rope.dtype == torch.bfloat16 and q_rope.is_contiguous()
+             and q_rope.numel() == rows * ROPE, "q_rope must be contiguous CUDA bf16 [..., 64]")
+    codes = torch.empty(rows, ROW, dtype=torch.uint8, device=q_nope_absorbed.device)
+    exps = torch.empty(rows, dtype=torch.int32, device=q_nope_absorbed.device)
+    status = _native.lib().mla_quantize_queries_fp8(
+        q_nope_absorbed.data_ptr(), q_rope.data_ptr(), rows, codes.data_ptr(), exps.data_ptr(),
+        _stream_ptr(stream, q_nope_absorbed.device))
+    _native.check(status, "mla_quantize_queries_fp8")
+    return codes, exps
 
 
 def device_status(workspace) -> int:
@@ -176,6 +239,14 @@ def mla_split_combine(o_part, lse_part, split_indptr, gate, *, n_q=1, out=None, 
     return out, lse
 
 
+def mla_kv_append_fp8(latent_new, rope_new, slab, page_table, seq_lens, n_new, *, kv_scale,
+                      status=None, stream=None):
+    """mla_kv_append into E4M3 pages (slab uint8 or float8_e4m3fn [num_pages,
+    page_stride]): each value is stored as the E4M3 code of value / kv_scale."""
+    return _append(latent_new, rope_new, _byte_view(slab), page_table, seq_lens, n_new, status,
+                   stream, float(kv_scale))
+
+
 def mla_kv_append(latent_new, rope_new, slab, page_table, seq_lens, n_new, *, status=None,
                   stream=None):
     """Write each request's n_new new latent / rope rows into the page pool.
@@ -187,13 +258,20 @@ def mla_kv_append(latent_new, rope_new, slab, page_table, seq_lens, n_new, *, st
     element that the kernel sets to 32 (a history shorter than n_new) or 33 (a
     page ID outside the pool); such rows are skipped.  Asynchronous.
     """
+    return _append(latent_new, rope_new, slab, page_table, seq_lens, n_new, status, stream,
+                   None)
+
+
+def _append(latent_new, rope_new, slab, page_table, seq_lens, n_new, status, stream, kv_scale):
+    fp8 = kv_scale is not None
     R = int(seq_lens.shape[0]) if hasattr(seq_lens, "shape") else 0
     _require(seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
              and seq_lens.dim() == 1, "seq_lens must be a contiguous CUDA int32 vector")
     _check_bf16(latent_new, "latent_new", (R * n_new, 512))
     _check_bf16(rope_new, "rope_new", (R * n_new, 64))
-    _require(slab.is_cuda and slab.dtype == torch.bfloat16 and slab.dim() == 2
-             and slab.stride(1) == 1, "slab must be a CUDA bf16 [num_pages, page_stride] view")
+    want = torch.uint8 if fp8 else torch.bfloat16
+    _require(slab.is_cuda and slab.dtype == want and slab.dim() == 2 and slab.stride(1) == 1,
+             f"slab must be a CUDA {want} [num_pages, page_stride] view")
     _require(slab.shape[1] >= PAGE_TOKENS * ROW, "slab page too small")
     _require(page_table.is_cuda and page_table.dtype == torch.int32 and page_table.dim() == 2
              and page_table.shape[0] == R and page_table.stride(1) == 1,
@@ -201,9 +279,13 @@ def mla_kv_append(latent_new, rope_new, slab, page_table, seq_lens, n_new, *, st
     if status is not None:
         _require(status.is_cuda and status.dtype == torch.int32 and status.numel() >= 1,
                  "status must be a CUDA int32 tensor")
-    rc = _native.lib().mla_kv_append(
-        latent_new.data_ptr(), rope_new.data_ptr(), slab.data_ptr(), slab.shape[0],
-        slab.stride(0), page_table.data_ptr(), page_table.stride(0), seq_lens.data_ptr(), R,
-        int(n_new), None if status is None else status.data_ptr(),
-        _stream_ptr(stream, slab.device))
-    _native.check(rc, "mla_kv_append")
+    lib = _native.lib()
+    head = (latent_new.data_ptr(), rope_new.data_ptr(), slab.data_ptr(), slab.shape[0],
+            slab.stride(0))
+    tail = (page_table.data_ptr(), page_table.stride(0), seq_lens.data_ptr(), R, int(n_new),
+            None if status is None else status.data_ptr(), _stream_ptr(stream, slab.device))
+    if fp8:
+        rc = lib.mla_kv_append_fp8(*head, kv_scale, *tail)
+    else:
+        rc = lib.mla_kv_append(*head, *tail)
+    _native.check(rc, "mla_kv_append_fp8" if fp8 else "mla_kv_append")

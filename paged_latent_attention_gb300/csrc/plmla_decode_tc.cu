@@ -69,42 +69,65 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;                // warps 2..9: two per TMEM lane quadrant
 constexpr int kSoftmaxThreads = 32 * kSoftmaxWarps;
 constexpr int kWarpVProducer = 10, kWarpPvIssuer = 11;
-constexpr int kSub = 9;                         // 8 latent column blocks + 1 rope block
-constexpr int kVItems = 8;                      // V items per tile (4 O^T blocks x 2 token halves)
 constexpr int kSubBytes = kTile * 64 * 2;       // one ring slot: 16 KB
-constexpr int kVHalf = 64 * 64 * 2;             // one 64 x 64 half of a V item
+constexpr int kVHalf = 64 * 64 * 2;             // one 64 x 64 half of a bf16 V item
 constexpr int kTmemCols = 512;
 constexpr int kTmemS = 256;                     // S^T buffers at columns 256 and 320
-constexpr float kTau = 8.0f;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
 constexpr int kMaxDynSmem = 232448;
 constexpr int kMaxK = 8, kMaxV = 8;             // ring slots (K, V) at most
 
-template <int NG>
+// How a 128-token tile moves through the rings, per cache format.
+//   bf16 pages: nine K items of 64 columns (8 latent blocks + the rope block),
+//     4 MMAs of K = 16 each; eight V items of 64 tokens x 128 latent rows, each
+//     two 64-column TMA boxes; P^T in bf16 (tcgen05 kind::f16).
+//   E4M3 pages (FP8 cache): five K items of 128 byte-columns (4 latent blocks +
+//     the rope block, whose upper 64 columns the TMA unit fills with zeros and no
+//     MMA reads), 4 MMAs of K = 32 each (2 on the rope); four V items of 128
+//     tokens x 128 latent rows; P^T in E4M3 (kind::f8f6f4, E4M3 x E4M3).
+// P = 2^(x - m + p_off) with x - m <= tau keeps P finite in its format; the
+// E4M3 offset moves the bulk of a diffuse softmax above E4M3's subnormals.
+template <bool F8>
+struct Fmt {
+    static constexpr int sub = F8 ? 5 : 9;              // K items per tile
+    static constexpr int col_step = F8 ? 128 : 64;      // K item width (elements)
+    static constexpr int rope_mmas = F8 ? 2 : 4;        // MMAs on the rope item
+    static constexpr int v_items = F8 ? 4 : 8;          // V items per tile
+    static constexpr int v_tokens = F8 ? 128 : 64;      // tokens per V item
+    static constexpr float tau = F8 ? 4.f : 8.f;        // lagged-maximum threshold (log2)
+    static constexpr float p_off = F8 ? 4.f : 0.f;
+};
+
+template <int NG, bool F8>
 struct Smem {
-    static constexpr int q_chunk = NG * 128;                // one 64-column chunk of Q^T
-    static constexpr int p_bytes = kTile * 2 * NG;          // P^T, bf16
+    using F = Fmt<F8>;
+    static constexpr int pn = F8 && NG < 32 ? 32 : NG;      // P^T columns (MMA N of P^T V)
+    static constexpr int p_row = F8 ? pn : 2 * NG;          // bytes per token row of P^T
+    static constexpr int q_chunk = NG * 128;                // one 128-byte column block of Q^T
+    static constexpr int p_bytes = kTile * p_row;           // P^T
     static constexpr int bar_bytes = 512;
-    static constexpr int misc_bytes = bar_bytes + 4 * 64 * 4 + 3 * 64 * 4 + 32;
-    static constexpr int fixed = p_bytes + kSub * q_chunk + misc_bytes + 1024;
+    static constexpr int misc_bytes = bar_bytes + 4 * 64 * 4 + 4 * 64 * 4 + 32;
+    static constexpr int fixed = p_bytes + F::sub * q_chunk + misc_bytes + 1024;
     static constexpr int slots_fit = (kMaxDynSmem - fixed) / kSubBytes;
-    // half of the slots for each ring
-    static constexpr int v_slots = slots_fit / 2 < kMaxV ? slots_fit / 2 : kMaxV;
+    // bf16: half of the slots for each ring; E4M3: one tile of V items, the rest K
+    static constexpr int v_slots = F8 ? 4 : (slots_fit / 2 < kMaxV ? slots_fit / 2 : kMaxV);
     static constexpr int k_slots = slots_fit - v_slots < kMaxK ? slots_fit - v_slots : kMaxK;
     static constexpr int v_off = k_slots * kSubBytes;
     static constexpr int p_off = v_off + v_slots * kSubBytes;
     static constexpr int q_off = p_off + p_bytes;            // 1024-aligned
-    static constexpr int bar_off = q_off + kSub * q_chunk;   // 1024-aligned
+    static constexpr int bar_off = q_off + F::sub * q_chunk; // 1024-aligned
     static constexpr int red_off = bar_off + bar_bytes;      // float red[4][64]
     static constexpr int fin_off = red_off + 4 * 64 * 4;     // float fin[64]
     static constexpr int m_off = fin_off + 64 * 4;           // float m[64]   (log2 units)
     static constexpr int al_off = m_off + 64 * 4;            // float alpha[64]
-    static constexpr int misc_off = al_off + 64 * 4;         // tmem addr, abort, need[2], cta
+    static constexpr int cf_off = al_off + 64 * 4;           // float cf[64]  (E4M3 score factors)
+    static constexpr int misc_off = cf_off + 64 * 4;         // tmem addr, abort, need[2], cta
     static constexpr int bytes = misc_off + 32;
     static constexpr int alloc = bytes + 1024;               // slack for 1024-B alignment
     static_assert(k_slots >= 2 && v_slots >= 2, "ring depth");
+    static_assert(p_bytes % 1024 == 0 && q_chunk % 1024 == 0, "swizzle atom alignment");
     static_assert(alloc <= kMaxDynSmem, "shared memory budget");
 };
 
@@ -277,6 +300,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
            ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4: fp32 accumulate, E4M3 A and B.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return (1u << 4) | (0u << 7) | (0u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
+           ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate)
 {
@@ -285,6 +316,39 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+
+template <bool F8>
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                    uint32_t accumulate)
+{
+    if constexpr (F8)
+        mma_e4m3(d_tmem, a, b, idesc, accumulate);
+    else
+        mma_bf16(d_tmem, a, b, idesc, accumulate);
+}
+
+template <bool F8>
+__host__ __device__ constexpr uint32_t idesc_for(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return F8 ? idesc_e4m3(M, N, a_mn_major, b_mn_major)
+              : idesc_bf16(M, N, a_mn_major, b_mn_major);
+}
+
+// Swizzle mode of a K- or MN-major operand whose rows are `row_bytes` wide.
+__host__ __device__ constexpr uint32_t layout_for_row(int row_bytes)
+{
+    return row_bytes == 128 ? kSw128 : (row_bytes == 64 ? kSw64 : kSw32);
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar)
@@ -468,16 +532,31 @@ __device__ __forceinline__ void scatter_to_red(const float (&v)[NG], float *red_
 // This thread's row of S^T (one token, NG query rows) in log2 units, with the
 // tokens a row may not see set to -inf: past the chunk end, or past the row's
 // causal limit L - (n_q - 1 - j) among the draft tokens.  The mask runs behind
-// one branch that is taken only on a request's last tiles.
-template <int NG>
-__device__ __forceinline__ void load_scores(uint32_t taddr, float scale_log2, bool tile_visible,
-                                            int t, int t_end, int vis_all, int row0, int heads,
-                                            float (&x)[NG])
+// one branch that is taken only on a request's last tiles.  bf16 scores take the
+// one factor scale * log2 e; E4M3 scores the per-row factor at cf_addr
+// (scale * log2 e * kv_scale * 2^e_row, the query row's power-of-two scale).
+template <int NG, bool F8>
+__device__ __forceinline__ void load_scores(uint32_t taddr, float scale_log2, uint32_t cf_addr,
+                                            bool tile_visible, int t, int t_end, int vis_all,
+                                            int row0, int heads, float (&x)[NG])
 {
     tmem_load_cols<NG>(taddr, x);
+    if constexpr (F8) {
 #pragma unroll
-    for (int c = 0; c < NG; ++c)
-        x[c] *= scale_log2;
+        for (int c4 = 0; c4 < NG; c4 += 4) {
+            float f[4];
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3])
+                         : "r"(cf_addr + 4 * c4));
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                x[c4 + e] *= f[e];
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < NG; ++c)
+            x[c] *= scale_log2;
+    }
     if (!tile_visible) {
 #pragma unroll
         for (int c = 0; c < NG; ++c) {
@@ -488,13 +567,14 @@ __device__ __forceinline__ void load_scores(uint32_t taddr, float scale_log2, bo
     }
 }
 
-// Shift this thread's scores to x - m (m = the row's reference maximum, 0
-// while still -inf) and report whether any score lies more than kTau above m.
-// A row whose m is -inf yields +inf for a visible score (flagged) and NaN for
-// a masked one (ignored by fmaxf).
-template <int NG>
+// Shift this thread's scores to x - m + p_off (m = the row's reference
+// maximum; no shift while it is still -inf) and report whether any score lies
+// more than tau above m.  A row whose m is -inf yields +inf for a visible score
+// (flagged) and NaN for a masked one (ignored by fmaxf).
+template <int NG, bool F8>
 __device__ __forceinline__ bool shift_and_test(float (&x)[NG], uint32_t m_addr)
 {
+    using F = Fmt<F8>;
     float vmax = -INFINITY;
 #pragma unroll
     for (int c4 = 0; c4 < NG; c4 += 4) {
@@ -505,10 +585,10 @@ __device__ __forceinline__ bool shift_and_test(float (&x)[NG], uint32_t m_addr)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             vmax = fmaxf(vmax, x[c4 + e] - m[e]);
-            x[c4 + e] -= m[e] == -INFINITY ? 0.f : m[e];
+            x[c4 + e] -= m[e] == -INFINITY ? 0.f : m[e] - F::p_off;
         }
     }
-    return vmax > kTau;
+    return vmax > F::tau;
 }
 
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
@@ -522,13 +602,14 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
 // the kernel
 // ---------------------------------------------------------------------------
 
-template <int NG>
+template <int NG, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
                  const DecodeArgs a)
 {
-    using L = Smem<NG>;
+    using L = Smem<NG, F8>;
+    using F = Fmt<F8>;
     constexpr int NK = L::k_slots, NV = L::v_slots;
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem = reinterpret_cast<unsigned char *>(
@@ -554,6 +635,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     float *fin = reinterpret_cast<float *>(smem + L::fin_off);
     float *m_sm = reinterpret_cast<float *>(smem + L::m_off);
     float *al_sm = reinterpret_cast<float *>(smem + L::al_off);
+    float *cf_sm = reinterpret_cast<float *>(smem + L::cf_off);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
     volatile int *need_sm = reinterpret_cast<volatile int *>(smem + L::misc_off + 16);   // [2]
@@ -660,10 +742,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     break;
                 }
                 const int qrow = seg.x * a.rows_per_req + row0;
-                mbar_arrive_expect_tx(bar_q, kSub * L::q_chunk);
-                for (int k = 0; k < kSub - 1; ++k)
-                    tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 64 * k, qrow, bar_q);
-                tma_load_2d(s_q + (kSub - 1) * L::q_chunk, &tm_qr, 0, qrow, bar_q);
+                mbar_arrive_expect_tx(bar_q, F::sub * L::q_chunk);
+                if constexpr (F8) {
+                    // E4M3 rows of 576 bytes: four latent blocks and the rope block
+                    // (its columns past 576 are zero-filled)
+                    for (int k = 0; k < F::sub; ++k)
+                        tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 128 * k, qrow, bar_q);
+                } else {
+                    for (int k = 0; k < F::sub - 1; ++k)
+                        tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 64 * k, qrow, bar_q);
+                    tma_load_2d(s_q + (F::sub - 1) * L::q_chunk, &tm_qr, 0, qrow, bar_q);
+                }
                 ++q_loads;
                 const int32_t *trow = a.page_table + (int64_t)seg.x * a.table_ld;
                 const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
@@ -671,15 +760,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     const int t = seg.y + i * kTile;
                     const int page = trow[t / kPageTokens];
                     const int tok = t % kPageTokens;
-                    for (int k = 0; k < kSub; ++k) {
+                    for (int k = 0; k < F::sub; ++k) {
                         if (!wait_bounded(bar_empty_k + 8 * slot, phase ^ 1, abort_flag, a.status,
                                           2)) {
                             ok = false;
                             break;
                         }
                         mbar_arrive_expect_tx(bar_full_k + 8 * slot, kSubBytes);
-                        tma_load_3d_hint(s_k + slot * kSubBytes, &tm_kv, 64 * k, tok, page,
-                                         bar_full_k + 8 * slot, k < kSub - 1 ? pol_keep : pol_once);
+                        tma_load_3d_hint(s_k + slot * kSubBytes, &tm_kv, F::col_step * k, tok,
+                                         page, bar_full_k + 8 * slot,
+                                         k < F::sub - 1 ? pol_keep : pol_once);
                         ++issued;
                         if (++slot == NK) {
                             slot = 0;
@@ -697,7 +787,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         }
     } else if (warp == kWarpVProducer) {
         // ---------------------------------------------------------- V producer
-        // V item v of a tile = latent block v / 2 (128 columns), token half v % 2.
+        // bf16: V item v of a tile = latent block v / 2 (128 columns), token half
+        // v % 2.  E4M3: item v = latent block v, all 128 tokens of the tile.
         // Items of a request's last tile that reach past the history land on
         // bar_vtmp first; the warp zeroes the rows past the history and then
         // releases the item to the issuer.  An item entirely past the history is
@@ -717,9 +808,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 const int t = seg.y + i * kTile;
                 const int page = trow[t / kPageTokens];
                 const int tok = t % kPageTokens;
-                for (int v = 0; v < kVItems; ++v) {
-                    // this item's 64 tokens reach past the history: mask it
-                    const bool partial = t + 64 * (v & 1) + 64 > seg.z;
+                for (int v = 0; v < F::v_items; ++v) {
+                    // first token of the item within the tile
+                    const int toff = F8 ? 0 : 64 * (v & 1);
+                    // this item's tokens reach past the history: mask it
+                    const bool partial = t + toff + F::v_tokens > seg.z;
                     bool got = true;
                     if (lane == 0)
                         got = wait_bounded(bar_empty_v + 8 * slot, phase ^ 1, abort_flag, a.status,
@@ -729,20 +822,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                         break;
                     }
                     const uint32_t dst = s_v + slot * kSubBytes;
-                    const int col = 128 * (v >> 1), tk = tok + 64 * (v & 1);
-                    // all 64 tokens of the item past the history: nothing to load
-                    const bool dead = t + 64 * (v & 1) >= seg.z;
+                    const int col = F8 ? 128 * v : 128 * (v >> 1), tk = tok + toff;
+                    // all tokens of the item past the history: nothing to load
+                    const bool dead = t + toff >= seg.z;
                     const uint32_t done_bar = partial ? bar_vtmp : bar_full_v + 8 * slot;
                     if (lane == 0 && !dead) {
                         mbar_arrive_expect_tx(done_bar, kSubBytes);
                         tma_load_3d_hint(dst, &tm_v, col, tk, page, done_bar, pol_once);
-                        tma_load_3d_hint(dst + kVHalf, &tm_v, col + 64, tk, page, done_bar,
-                                         pol_once);
+                        if constexpr (!F8)
+                            tma_load_3d_hint(dst + kVHalf, &tm_v, col + 64, tk, page, done_bar,
+                                             pol_once);
                     }
                     ++issued;
                     partial_bits = (partial_bits << 1) | (partial ? 1u : 0u);
                     if (partial) {
-                        // rows r of this item hold token t + 64 * (v % 2) + r
+                        // rows r of this item hold token t + toff + r
                         const bool landed =
                             dead || wait_bounded(bar_vtmp, vtmp_phase, abort_flag, a.status, 12);
                         if (!__all_sync(0xffffffffu, landed)) {
@@ -752,11 +846,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                         }
                         if (!dead)
                             vtmp_phase ^= 1;
-                        const int first_dead = seg.z - (t + 64 * (v & 1));   // may be <= 0
-                        for (int r = lane; r < 64; r += 32) {
+                        const int first_dead = seg.z - (t + toff);   // may be <= 0
+                        for (int r = lane; r < F::v_tokens; r += 32) {
                             if (r >= first_dead) {
 #pragma unroll
-                                for (int half = 0; half < 2; ++half)
+                                for (int half = 0; half < (F8 ? 1 : 2); ++half)
 #pragma unroll
                                     for (int ch = 0; ch < 8; ++ch)
                                         st_shared_v4(dst + half * kVHalf + r * 128 + 16 * ch, 0u,
@@ -790,7 +884,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         // -------------------------------------------------------- S^T issuer
         if (lane == 0) {
             bool issued = false, ok = true;
-            constexpr uint32_t idesc_s = idesc_bf16(128, NG, false, false);
+            constexpr uint32_t idesc_s = idesc_for<F8>(128, NG, false, false);
             const uint64_t dk0 = sdesc(s_k, 16, 1024, kSw128);
             const uint64_t dq0 = sdesc(s_q, 16, 1024, kSw128);
             int slot = 0;
@@ -823,18 +917,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     tc_fence_after();
                     const uint32_t d_s = tmem + kTmemS + 64 * b;
 #pragma unroll
-                    for (int k = 0; k < kSub; ++k) {
+                    for (int k = 0; k < F::sub; ++k) {
                         if (!wait_bounded(bar_full_k + 8 * slot, phase, abort_flag, a.status, 4)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint64_t da = dk0 + (uint64_t)(slot * (kSubBytes >> 4));
+                        // 32-byte K steps inside the 128-byte swizzled rows
+                        constexpr int last_mmas = F::rope_mmas;
+                        const int n_mma = k == F::sub - 1 ? last_mmas : 4;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16(d_s, da + 2 * kk,
-                                     dq0 + (uint64_t)(k * (L::q_chunk >> 4) + 2 * kk), idesc_s,
-                                     (k | kk) != 0);
+                            if (kk < n_mma)
+                                mma<F8>(d_s, da + 2 * kk,
+                                        dq0 + (uint64_t)(k * (L::q_chunk >> 4) + 2 * kk), idesc_s,
+                                        (k | kk) != 0);
                         mma_commit(bar_empty_k + 8 * slot);
                         issued = true;
                         if (++slot == NK) {
@@ -858,10 +956,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         // ----------------------------------------------------- P^T V issuer
         if (lane == 0) {
             bool issued = false, ok = true;
-            constexpr uint32_t idesc_pv = idesc_bf16(128, NG, true, true);
-            constexpr uint32_t p_layout = NG == 64 ? kSw128 : (NG == 32 ? kSw64 : kSw32);
+            constexpr uint32_t idesc_pv = idesc_for<F8>(128, L::pn, true, true);
+            constexpr uint32_t p_layout = layout_for_row(L::p_row);
+            // MN-major operands: 8-token row groups 1024 bytes (V) and 8 P^T rows apart
             const uint64_t dv0 = sdesc(s_v, kVHalf, 1024, kSw128);
-            const uint64_t dp0 = sdesc(s_p, 8192, 16 * NG, p_layout);
+            const uint64_t dp0 = sdesc(s_p, 8192, 8 * L::p_row, p_layout);
             int slot = 0;
             uint32_t phase = 0;
             int g = 0;
@@ -882,19 +981,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     }
                     tc_fence_after();
 #pragma unroll
-                    for (int v = 0; v < kVItems; ++v) {
+                    for (int v = 0; v < F::v_items; ++v) {
                         if (!wait_bounded(bar_full_v + 8 * slot, phase, abort_flag, a.status, 14)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint64_t da = dv0 + (uint64_t)(slot * (kSubBytes >> 4));
-                        const int j = v >> 1, h = v & 1;
+                        // O^T block j; the item's token half h (bf16 items are 64 tokens)
+                        const int j = F8 ? v : v >> 1, h = F8 ? 0 : v & 1;
+                        // each MMA takes 16 (bf16) or 32 (E4M3) tokens: 2 or 4 row groups
+                        constexpr int k_tok = F8 ? 32 : 16;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16(tmem + 64 * j, da + (uint64_t)(128 * kk),
-                                     dp0 + (uint64_t)((4 * h + kk) * 2 * NG), idesc_pv,
-                                     (i | h | kk) != 0);
+                            mma<F8>(tmem + 64 * j, da + (uint64_t)((k_tok * 128 >> 4) * kk),
+                                    dp0 + (uint64_t)(((64 * h + k_tok * kk) * L::p_row) >> 4),
+                                    idesc_pv, (i | h | kk) != 0);
                         mma_commit(bar_empty_v + 8 * slot);
                         issued = true;
                         if (++slot == NV) {
@@ -926,6 +1028,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         const uint32_t t_lane = (uint32_t)(32 * q) << 16;
         const uint32_t m_addr = smem_u32(m_sm) + 4 * col0;
         const uint32_t al_addr = smem_u32(al_sm) + 4 * col0;
+        const uint32_t cf_addr = smem_u32(cf_sm) + 4 * col0;
+        // E4M3 with fewer than 32 query rows: the P^T rows are padded to 32 bytes
+        // and the padding stays zero (the P^T V MMA multiplies it into unused columns)
+        if constexpr (L::pn > NG) {
+            for (int r = st; r < kTile; r += kSoftmaxThreads) {
+                const uint32_t off = (uint32_t)(r * L::p_row + 16);
+                st_shared_v4(s_p + (off ^ (((off >> 7) & 1u) << 4)), 0u, 0u, 0u, 0u);
+            }
+        }
         bool ok = true;
         int gt = 0;
         for (int s = seg_begin; s < seg_end && ok; ++s) {
@@ -936,8 +1047,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             const int vis_all = Lr - (a.n_q - 1);   // tokens below this are visible to every row
             if (local > 0)
                 softmax_bar();                       // previous epilogue is done with m_sm
-            for (int c = st; c < NG; c += kSoftmaxThreads)
+            for (int c = st; c < NG; c += kSoftmaxThreads) {
                 m_sm[c] = -INFINITY;
+                if constexpr (F8) {
+                    // score factor of query row c: scale * log2 e * kv_scale * 2^e
+                    const int e = a.qexp[(int64_t)seg.x * a.rows_per_req + row0 + c];
+                    cf_sm[c] = a.scale_log2 * a.kv_scale * __uint_as_float((uint32_t)(e + 127) << 23);
+                }
+            }
             softmax_bar();
             float lsum[CH];
 #pragma unroll
@@ -957,9 +1074,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 bool exceed = false;
                 if (got) {
                     tc_fence_after();
-                    load_scores<CH>(tmem + t_lane + s_col, a.scale_log2, tile_visible, t, seg.z,
-                                    vis_all, row0 + col0, a.num_heads, x);
-                    exceed = shift_and_test<CH>(x, m_addr);
+                    load_scores<CH, F8>(tmem + t_lane + s_col, a.scale_log2, cf_addr, tile_visible,
+                                        t, seg.z, vis_all, row0 + col0, a.num_heads, x);
+                    exceed = shift_and_test<CH, F8>(x, m_addr);
                 }
                 if (softmax_bar_or(exceed || !got || *abort_flag)) {
                     // rare: a score exceeds its reference maximum (always on a segment's
@@ -986,7 +1103,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                                 if (mu == -INFINITY) {
                                     m_sm[c] = mx;       // first visible token of this row
                                     alpha = 0.f;
-                                } else if (mx - mu > kTau) {
+                                } else if (mx - mu > F::tau) {
                                     m_sm[c] = mx;
                                     alpha = fast_exp2(mu - mx);
                                 }
@@ -1020,24 +1137,39 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                             tmem_wait_st();
                         }
                     }
-                    load_scores<CH>(tmem + t_lane + s_col, a.scale_log2, tile_visible, t, seg.z,
-                                    vis_all, row0 + col0, a.num_heads, x);
-                    shift_and_test<CH>(x, m_addr);
+                    load_scores<CH, F8>(tmem + t_lane + s_col, a.scale_log2, cf_addr, tile_visible,
+                                        t, seg.z, vis_all, row0 + col0, a.num_heads, x);
+                    shift_and_test<CH, F8>(x, m_addr);
                 }
                 // this S^T buffer may now be overwritten by the tile after next
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     mbar_arrive(bar_sfree + 8 * b);
-                // probabilities 2^(x - m) (x is already shifted) and running sums
-                uint32_t pk[CH / 2];
+                // probabilities 2^(x - m + p_off) (x is already shifted) and running
+                // sums (of the fp32 values; only the MMA operand is rounded)
+                constexpr int kWords = F8 ? CH / 4 : CH / 2;
+                uint32_t pk[kWords];
+                if constexpr (F8) {
 #pragma unroll
-                for (int c = 0; c < CH; c += 2) {
-                    const float p0 = fast_exp2(x[c]);        // 2^-inf = 0
-                    const float p1 = fast_exp2(x[c + 1]);
-                    lsum[c] += p0;
-                    lsum[c + 1] += p1;
-                    pk[c / 2] = pack_bf16x2(p0, p1);
+                    for (int c = 0; c < CH; c += 4) {
+                        float p[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            p[e] = fast_exp2(x[c + e]);       // 2^-inf = 0
+                            lsum[c + e] += p[e];
+                        }
+                        pk[c / 4] = (uint32_t)e4m3x2(p[0], p[1]) | ((uint32_t)e4m3x2(p[2], p[3]) << 16);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < CH; c += 2) {
+                        const float p0 = fast_exp2(x[c]);    // 2^-inf = 0
+                        const float p1 = fast_exp2(x[c + 1]);
+                        lsum[c] += p0;
+                        lsum[c + 1] += p1;
+                        pk[c / 2] = pack_bf16x2(p0, p1);
+                    }
                 }
                 // P^T is free once the previous tile's P^T V has completed
                 if (gt > 0) {
@@ -1049,17 +1181,27 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     }
                 }
                 {
-                    // this token's row of P^T (2*NG bytes, 16-byte chunks swizzled
+                    // this token's row of P^T (p_row bytes, 16-byte chunks swizzled
                     // like the MMA operand); this thread writes its column half
-                    constexpr int row_bytes = 2 * NG;
-                    constexpr int swz_bits = NG == 64 ? 3 : (NG == 32 ? 2 : 1);
-                    constexpr int chunks = CH * 2 / 16;
+                    constexpr int row_bytes = L::p_row;
+                    constexpr int swz_bits = row_bytes == 128 ? 3 : (row_bytes == 64 ? 2 : 1);
+                    constexpr int my_bytes = kWords * 4;
+                    if constexpr (my_bytes >= 16) {
 #pragma unroll
-                    for (int ch = 0; ch < chunks; ++ch) {
-                        const uint32_t off = (uint32_t)(tok * row_bytes + h * CH * 2 + 16 * ch);
+                        for (int ch = 0; ch < my_bytes / 16; ++ch) {
+                            const uint32_t off =
+                                (uint32_t)(tok * row_bytes + h * my_bytes + 16 * ch);
+                            const uint32_t sw = off ^ (((off >> 7) & ((1u << swz_bits) - 1u)) << 4);
+                            st_shared_v4(s_p + sw, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
+                                         pk[4 * ch + 3]);
+                        }
+                    } else {
+                        // 8 bytes (E4M3, 16 query rows): half of a 16-byte chunk
+                        const uint32_t off = (uint32_t)(tok * row_bytes + h * my_bytes);
                         const uint32_t sw = off ^ (((off >> 7) & ((1u << swz_bits) - 1u)) << 4);
-                        st_shared_v4(s_p + sw, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2],
-                                     pk[4 * ch + 3]);
+                        asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(s_p + sw),
+                                     "r"(pk[0]), "r"(pk[1])
+                                     : "memory");
                     }
                 }
                 fence_proxy_async();
@@ -1084,9 +1226,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             if (q == 0 && lane < CH) {
                 const int c = col0 + lane;
                 const float l = red[c] + red[64 + c] + red[128 + c] + red[192 + c];
-                fin[c] = l > 0.f ? 1.f / l : 0.f;   // 1 / row sum (0 for an empty row)
+                // 1 / row sum (0 for an empty row); E4M3 values carry kv_scale
+                fin[c] = l > 0.f ? (F8 ? a.kv_scale : 1.f) / l : 0.f;
                 a.lse_part[(int64_t)(team * seg_total + s) * NG + c] =
-                    l > 0.f ? (m_sm[c] + log2f(l)) * kLn2 : -INFINITY;
+                    l > 0.f ? (m_sm[c] + log2f(l) - F::p_off) * kLn2 : -INFINITY;
             }
             softmax_bar();
             // normalised partial output: thread = latent row of each O^T block;
@@ -1165,22 +1308,23 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-bool make_map(CUtensorMap *map, const void *base, int rank, const cuuint64_t *dims,
-              const cuuint64_t *strides, const cuuint32_t *box)
+bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, int rank,
+              const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr)
         return false;
     const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), dims,
-              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    // out-of-range elements (the E4M3 rope block's columns past 576) read as zero
+    return fn(map, dtype, rank, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int NG>
-cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
+cudaError_t make_maps_bf16(const DecodeArgs &a, CUtensorMap *maps)
 {
-    CUtensorMap tm_kv, tm_v, tm_qn, tm_qr;
+    const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const cuuint64_t kv_dims[3] = {(cuuint64_t)kRow, (cuuint64_t)kPageTokens,
                                    (cuuint64_t)a.num_pages};
     const cuuint64_t kv_strides[2] = {(cuuint64_t)kRow * 2, (cuuint64_t)a.page_stride * 2};
@@ -1192,14 +1336,46 @@ cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
     const cuuint64_t qr_dims[2] = {(cuuint64_t)kRope, rows};
     const cuuint64_t qr_strides[1] = {(cuuint64_t)kRope * 2};
     const cuuint32_t q_box[2] = {64, (cuuint32_t)NG};
-    if (!make_map(&tm_kv, a.slab, 3, kv_dims, kv_strides, kv_box) ||
-        !make_map(&tm_v, a.slab, 3, kv_dims, kv_strides, v_box) ||
-        !make_map(&tm_qn, a.q_nope, 2, qn_dims, qn_strides, q_box) ||
-        !make_map(&tm_qr, a.q_rope, 2, qr_dims, qr_strides, q_box))
+    if (!make_map(&maps[0], bf16, a.slab, 3, kv_dims, kv_strides, kv_box) ||
+        !make_map(&maps[1], bf16, a.slab, 3, kv_dims, kv_strides, v_box) ||
+        !make_map(&maps[2], bf16, a.q_nope, 2, qn_dims, qn_strides, q_box) ||
+        !make_map(&maps[3], bf16, a.q_rope, 2, qr_dims, qr_strides, q_box))
         return cudaErrorInvalidValue;
-    constexpr int smem = Smem<NG>::alloc;
-    cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<NG>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return cudaSuccess;
+}
+
+// E4M3 pages: byte tensors; K and V items use the same 128 x 128 box, and the
+// queries are the quantised rows [R*n_q*H, 576] (the fourth map is unused).
+template <int NG>
+cudaError_t make_maps_e4m3(const DecodeArgs &a, CUtensorMap *maps)
+{
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const cuuint64_t kv_dims[3] = {(cuuint64_t)kRow, (cuuint64_t)kPageTokens,
+                                   (cuuint64_t)a.num_pages};
+    const cuuint64_t kv_strides[2] = {(cuuint64_t)kRow, (cuuint64_t)a.page_stride};
+    const cuuint32_t kv_box[3] = {128, (cuuint32_t)kTile, 1};
+    const cuuint64_t rows = (cuuint64_t)a.num_reqs * a.rows_per_req;
+    const cuuint64_t q_dims[2] = {(cuuint64_t)kRow, rows};
+    const cuuint64_t q_strides[1] = {(cuuint64_t)kRow};
+    const cuuint32_t q_box[2] = {128, (cuuint32_t)NG};
+    if (!make_map(&maps[0], u8, a.slab, 3, kv_dims, kv_strides, kv_box) ||
+        !make_map(&maps[2], u8, a.q8, 2, q_dims, q_strides, q_box))
+        return cudaErrorInvalidValue;
+    maps[1] = maps[0];
+    maps[3] = maps[2];
+    return cudaSuccess;
+}
+
+template <int NG, bool F8>
+cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
+{
+    CUtensorMap maps[4];
+    cudaError_t err = F8 ? make_maps_e4m3<NG>(a, maps) : make_maps_bf16<NG>(a, maps);
+    if (err != cudaSuccess)
+        return err;
+    constexpr int smem = Smem<NG, F8>::alloc;
+    err = cudaFuncSetAttribute(decode_tc_kernel<NG, F8>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess)
         return err;
     cudaLaunchConfig_t cfg = {};
@@ -1212,17 +1388,26 @@ cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NG>, tm_kv, tm_v, tm_qn, tm_qr, a);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NG, F8>, maps[0], maps[1], maps[2], maps[3],
+                              a);
 }
 
 }  // namespace
 
 cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream)
 {
+    if (args.fp8) {
+        switch (args.group_rows) {
+        case 64: return launch_ng<64, true>(args, stream);
+        case 32: return launch_ng<32, true>(args, stream);
+        case 16: return launch_ng<16, true>(args, stream);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (args.group_rows) {
-    case 64: return launch_ng<64>(args, stream);
-    case 32: return launch_ng<32>(args, stream);
-    case 16: return launch_ng<16>(args, stream);
+    case 64: return launch_ng<64, false>(args, stream);
+    case 32: return launch_ng<32, false>(args, stream);
+    case 16: return launch_ng<16, false>(args, stream);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -57,12 +57,18 @@ struct PlanBuffers {
     int32_t *claim;             // [n_claim] CTA-index claims of the decode grid, zeroed here
     int32_t n_claim;
     SmCalib *calib;             // per-device speed record (null: equal shares)
+    // FP8 decode: extra CTAs of the plan grid quantise the queries (null: none)
+    const __nv_bfloat16 *q_nope; // [q_rows, 512]
+    const __nv_bfloat16 *q_rope; // [q_rows, 64]
+    uint8_t *q8;                 // [q_rows, 576] E4M3 codes of q * 2^-e
+    int32_t *qexp;               // [q_rows] e
+    int32_t q_rows;
 };
 
 struct DecodeArgs {
     const __nv_bfloat16 *q_nope;   // [R*n_q, H, 512]
     const __nv_bfloat16 *q_rope;   // [R*n_q, H, 64]
-    const __nv_bfloat16 *slab;
+    const void *slab;              // bf16 elements, or E4M3 bytes when fp8
     int64_t page_stride;           // elements
     int64_t num_pages;
     const int32_t *page_table;
@@ -83,7 +89,17 @@ struct DecodeArgs {
     int32_t *done;                 // [groups * R] segments of (team, request) written
     int32_t *claim;                // [groups * members] CTA indices taken (zeroed by the plan)
     SmCalib *calib;                // per-device speed record, or null
+    // FP8 pages: slab holds E4M3 bytes (value = kv_scale * byte), the queries are
+    // read as E4M3 codes q8 with per-row exponents qexp (written by the plan grid)
+    int32_t fp8;
+    float kv_scale;
+    const uint8_t *q8;             // [R*n_q*H, 576]
+    const int32_t *qexp;           // [R*n_q*H]
 };
+
+// E4M3's largest finite value and the plan grid's query-quantising CTAs.
+constexpr float kE4m3Max = 448.f;
+constexpr int kQuantRowsPerCta = 64;
 
 // Largest of 64, 32, 16 that divides `rows`, or 0.
 inline int group_rows_for(int rows)
@@ -98,10 +114,9 @@ size_t plan_smem_bytes();
 cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int members,
                         PlanBuffers plan, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream);
-// Merge of chunk partials + sigmoid gate.  Row rw of request r (rw = j*H + h)
-// lives in group g = rw / group_rows at row rw % group_rows of the partials
-// of segments [g*stride + indptr[r], g*stride + indptr[r + 1]), where stride is
-// *seg_stride (or 0 when seg_stride is null).
+// The FP8 decode's query quantiser as a kernel of its own (rows of 576 values).
+cudaError_t launch_quantize(const __nv_bfloat16 *q_nope, const __nv_bfloat16 *q_rope, int rows,
+                            uint8_t *q8, int32_t *qexp, cudaStream_t stream);
 // KV append (plmla_append.cu): status codes it writes for a bad row.
 constexpr int32_t kStatusAppendPosition = 32;   // seq_lens[r] < n_new
 constexpr int32_t kStatusAppendPage = 33;       // page ID outside [0, num_pages)
@@ -109,7 +124,25 @@ cudaError_t launch_append(const void *latent, const void *rope, void *slab, int6
                           int64_t page_stride, const int32_t *table, int64_t table_ld,
                           const int32_t *seq_lens, int num_reqs, int n_new, int32_t *status,
                           cudaStream_t stream);
+// The same into E4M3 pages: each value stored as the E4M3 code of x / kv_scale.
+cudaError_t launch_append_fp8(const void *latent, const void *rope, void *slab,
+                              int64_t num_pages, int64_t page_stride, float kv_scale,
+                              const int32_t *table, int64_t table_ld, const int32_t *seq_lens,
+                              int num_reqs, int n_new, int32_t *status, cudaStream_t stream);
 
+// Shared by the query quantiser (plan grid) and the FP8 append: one E4M3 byte
+// pair from two floats, round to nearest even, saturating to +-448.
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Merge of chunk partials + sigmoid gate.  Row rw of request r (rw = j*H + h)
+// lives in group g = rw / group_rows at row rw % group_rows of the partials
+// of segments [g*stride + indptr[r], g*stride + indptr[r + 1]), where stride is
+// *seg_stride (or 0 when seg_stride is null).
 // With `done` (and `status`) set, the combine is launched while the decode is
 // still running and waits, per request, until done[team * R + r] counts all of
 // the request's segments; without it, it waits for the previous grid to finish.

@@ -163,6 +163,68 @@ __device__ __forceinline__ int chunk_mid2(int cost0, int tiles, int chunk_tiles,
                   : 2 * cost0 + 2 * kSegmentCostTiles + 2 * s * chunk_tiles + t;
 }
 
+// FP8 queries for the FP8 decode (its tensor-core kind multiplies E4M3 by E4M3):
+// row i of [q_nope | q_rope] (576 values) becomes the E4M3 codes of q * 2^-e,
+// with e the smallest exponent for which max |q| * 2^-e <= 448 (E4M3's largest
+// finite value), at least -126, and 0 for an all-zero row.  The scaling by a
+// power of two is exact; the conversion rounds to nearest even.  One warp per
+// row: lane l takes latent values [16 l, 16 l + 16) and, for l < 8, rope values
+// [8 l, 8 l + 8).
+__device__ void quantize_queries(const PlanBuffers &plan, int cta)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int row_end = min(plan.q_rows, (cta + 1) * kQuantRowsPerCta);
+    for (int row = cta * kQuantRowsPerCta + warp; row < row_end; row += kPlanWarps) {
+        const uint4 *qn = reinterpret_cast<const uint4 *>(plan.q_nope + (int64_t)row * kLatent);
+        const uint4 *qr = reinterpret_cast<const uint4 *>(plan.q_rope + (int64_t)row * kRope);
+        uint32_t w[12];
+        const uint4 a = qn[2 * lane], b = qn[2 * lane + 1];
+        const uint4 c = lane < 8 ? qr[lane] : make_uint4(0u, 0u, 0u, 0u);
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+        w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        w[8] = c.x; w[9] = c.y; w[10] = c.z; w[11] = c.w;
+        float v[24];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 12; ++i) {
+            v[2 * i] = __uint_as_float(w[i] << 16);
+            v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            amax = fmaxf(amax, fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1])));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const uint32_t bits = __float_as_uint(amax);
+        const int biased = (int)((bits >> 23) & 0xFFu);
+        int e = 0;
+        if (amax > 0.f) {
+            if (biased == 0) {
+                e = -126;                               // subnormal maximum
+            } else {
+                // amax = (1 + f) 2^k: 2^(k-8) keeps it <= 448 = 1.75 * 2^8 iff f <= 0.75
+                const int k = biased - 127;
+                e = max((bits & 0x7FFFFFu) <= 0x600000u ? k - 8 : k - 7, -126);
+            }
+        }
+        const float p2 = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, exact
+        uint32_t out[4], rope_out[2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            out[i] = (uint32_t)e4m3x2(v[4 * i] * p2, v[4 * i + 1] * p2) |
+                     ((uint32_t)e4m3x2(v[4 * i + 2] * p2, v[4 * i + 3] * p2) << 16);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            rope_out[i] = (uint32_t)e4m3x2(v[16 + 4 * i] * p2, v[16 + 4 * i + 1] * p2) |
+                          ((uint32_t)e4m3x2(v[16 + 4 * i + 2] * p2, v[16 + 4 * i + 3] * p2) << 16);
+        uint8_t *dst = plan.q8 + (int64_t)row * kRow;
+        *reinterpret_cast<uint4 *>(dst + 16 * lane) = make_uint4(out[0], out[1], out[2], out[3]);
+        if (lane < 8)
+            *reinterpret_cast<uint2 *>(dst + kLatent + 8 * lane) = make_uint2(rope_out[0], rope_out[1]);
+        if (lane == 0)
+            plan.qexp[row] = e;
+    }
+}
+
 __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int members,
             PlanBuffers plan)
@@ -171,8 +233,12 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     PlanSmem &sm = *reinterpret_cast<PlanSmem *>(plan_smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // the decode kernel may start its prologue now; it waits for this grid's
-    // completion before reading the plan
+    // completion before reading the plan (and the FP8 queries)
     asm volatile("griddepcontrol.launch_dependents;");
+    if (blockIdx.x > 0) {
+        quantize_queries(plan, blockIdx.x - 1);
+        return;
+    }
 
     // ---- histories
     const int r0 = tid * kReqPerThread;
@@ -526,7 +592,30 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     }
 }
 
+// The query quantiser on its own (the FP8 decode runs it inside the plan grid).
+__global__ void __launch_bounds__(kPlanThreads)
+quantize_kernel(PlanBuffers plan)
+{
+    quantize_queries(plan, blockIdx.x);
+}
+
 }  // namespace
+
+cudaError_t launch_quantize(const __nv_bfloat16 *q_nope, const __nv_bfloat16 *q_rope, int rows,
+                            uint8_t *q8, int32_t *qexp, cudaStream_t stream)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    PlanBuffers plan = {};
+    plan.q_nope = q_nope;
+    plan.q_rope = q_rope;
+    plan.q8 = q8;
+    plan.qexp = qexp;
+    plan.q_rows = rows;
+    quantize_kernel<<<(rows + kQuantRowsPerCta - 1) / kQuantRowsPerCta, kPlanThreads, 0, stream>>>(
+        plan);
+    return cudaGetLastError();
+}
 
 size_t plan_smem_bytes() { return sizeof(PlanSmem); }
 
@@ -538,7 +627,10 @@ cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int m
         cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess)
         return err;
-    plan_kernel<<<1, kPlanThreads, smem, stream>>>(seq_lens, num_reqs, budget, members, plan);
+    const int qctas =
+        plan.q8 != nullptr ? (plan.q_rows + kQuantRowsPerCta - 1) / kQuantRowsPerCta : 0;
+    plan_kernel<<<1 + qctas, kPlanThreads, smem, stream>>>(seq_lens, num_reqs, budget, members,
+                                                            plan);
     return cudaGetLastError();
 }
 

@@ -192,10 +192,38 @@ def make_slab(w: Workload, device="cpu", layer: int = 0, poison_nan: bool = Fals
     return slab
 
 
-def poison_slab(w: Workload, slab):
-    """Write NaN into every slab element a decode must not read."""
+# Scale of the synthetic FP8 cache: N(0, 1) values reach E4M3's largest finite
+# value (448) at 6 standard deviations.
+KV_SCALE_E4M3 = 6.0 / 448.0
+E4M3_NAN = 0x7F
+
+
+def make_slab_e4m3(w: Workload, device="cpu", layer: int = 0, poison_nan: bool = False,
+                   kv_scale: float = KV_SCALE_E4M3, pages_per_chunk: int = 64):
+    """One layer's FP8 slab: [num_pages, page_stride] uint8 holding E4M3 bytes of
+    N(0, 1) / kv_scale (clamped to +-448), made with torch's float8_e4m3fn cast
+    from the same seeded stream as make_slab.  page_stride counts bytes here.
+    With ``poison_nan`` the bytes a decode must not read hold the E4M3 NaN."""
     import torch
-    nan = float("nan")
+    g = _gen(device, w.seed * 1_000_003 + layer * 101 + 3)
+    slab = torch.empty(w.num_pages, w.page_stride, dtype=torch.uint8, device=device)
+    for p0 in range(0, w.num_pages, pages_per_chunk):
+        p1 = min(w.num_pages, p0 + pages_per_chunk)
+        vals = torch.empty(p1 - p0, w.page_stride, dtype=torch.float32, device=device)
+        vals.normal_(generator=g)
+        vals.div_(kv_scale).clamp_(-448.0, 448.0)
+        slab[p0:p1] = vals.to(torch.float8_e4m3fn).view(torch.uint8)
+        del vals
+    if poison_nan:
+        poison_slab(w, slab, value=E4M3_NAN)
+    return slab
+
+
+def poison_slab(w: Workload, slab, value=None):
+    """Write NaN (or ``value``, e.g. the E4M3 NaN byte) into every slab element a
+    decode must not read."""
+    import torch
+    nan = float("nan") if value is None else value
     used_rows = w.page_tokens * (w.dc + w.dr)
     if w.page_stride > used_rows:
         slab[:, used_rows:] = nan

@@ -71,3 +71,55 @@ def sample_rows(w, heads_per_token=4, seed=0):
             hs.add(int(rng.integers(0, H)))
         rows.extend(t * H + h for h in sorted(hs))
     return np.array(rows, dtype=np.int64)
+
+
+# --------------------------------------------------------------------------
+# FP8 (E4M3) pages
+# --------------------------------------------------------------------------
+
+# The FP8 decode rounds each probability to E4M3 before the value MMA (3
+# mantissa bits: relative error <= 2^-4), while the normaliser and the LSE use
+# the fp32 probabilities.  So |out - ref| may exceed the bf16 bound by at most
+# 2^-4 * sigmoid(g) * sum_t w_t |c_t| (w = the exact softmax weights, c = the
+# dequantised latent), which the oracle returns as `bound`.  The LSE bound is
+# unchanged.
+P_E4M3_REL = 2.0 ** -4
+
+
+def gpu_decode_fp8(w, d, kv_scale, *, cta_budget=0, min_splits=None, scale=SCALE):
+    ms = min_splits or w.min_splits
+    ws = api.allocate_workspace(w.num_reqs, w.n_q, w.num_heads, cta_budget, ms, "cuda",
+                                fp8=True)
+    out, lse = api.mla_decode_fp8(d["qn"], d["qr"], d["gate"], d["slab"], d["table"], d["lens"],
+                                  kv_scale=kv_scale, n_q=w.n_q, scale=scale,
+                                  cta_budget=cta_budget, min_splits=ms, workspace=ws)
+    torch.cuda.synchronize()
+    assert api.device_status(ws) == 0, "a decode pipeline wait timed out"
+    return out, lse
+
+
+def oracle_decode_fp8(w, qn, qr, gate, slab8_host, kv_scale, rows=None, scale=SCALE):
+    return oracle.mla_decode_e4m3_reference(qn, qr, gate, slab8_host, kv_scale, w.page_table,
+                                            w.seq_lens, w.n_q, w.num_heads, scale,
+                                            num_pages=w.num_pages, page_stride=w.page_stride,
+                                            page_tokens=w.page_tokens, dc=w.dc, dr=w.dr,
+                                            rows=rows, with_abs=True)
+
+
+def assert_parity_fp8(out, lse, ref_out, ref_lse, bound, rows=None, what=""):
+    o = out.float().cpu().numpy().reshape(-1, out.shape[-1]).astype(np.float64)
+    l = lse.cpu().numpy().reshape(-1).astype(np.float64)
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        o, l = o[rows], l[rows]
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    err = np.abs(o - ref_out)
+    tol = OUT_ATOL + OUT_RTOL * np.abs(ref_out) + P_E4M3_REL * bound
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} outputs out of tolerance, "
+                           f"max err {err.max():.3e}")
+    both_inf = np.isneginf(l) & np.isneginf(ref_lse)
+    with np.errstate(invalid="ignore"):
+        lerr = np.where(both_inf, 0.0, np.abs(l - ref_lse))
+    assert np.all(lerr <= LSE_ATOL), f"{what}: lse max err {np.nanmax(lerr):.3e}"
+    return float(err.max()), float(lerr.max())
