@@ -73,7 +73,7 @@ SmCalib *calib_for_current_device(bool fp8)
 }
 
 struct WorkspaceLayout {
-    size_t status, indptr, chunk, seg_count, segments, seg_req, seg_member, done, claim,
+    size_t status, calib_stage, indptr, chunk, seg_count, segments, seg_req, seg_member, done, claim,
         o_part, lse_part, q8, qexp, total;
     int32_t max_segments;
 };
@@ -124,6 +124,8 @@ WorkspaceLayout layout_for(int32_t num_reqs, const Shape &sh, bool fp8)
     w.max_segments = max_chunks < max_runs ? max_chunks : max_runs;
     size_t off = 0;
     w.status = off;
+    off = align_up(off + sizeof(int32_t));
+    w.calib_stage = off;
     off = align_up(off + sizeof(int32_t));
     w.indptr = off;
     off = align_up(off + sizeof(int32_t) * (size_t)(num_reqs + 1));
@@ -305,6 +307,7 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     plan.claim = reinterpret_cast<int32_t *>(ws + w.claim);
     plan.n_claim = sh.groups * sh.members;
     plan.calib = calib_for_current_device(fmt.fp8);
+    plan.calib_stage = reinterpret_cast<int32_t *>(ws + w.calib_stage);
     plan.q_nope = static_cast<const __nv_bfloat16 *>(q_nope_absorbed);
     plan.q_rope = static_cast<const __nv_bfloat16 *>(q_rope);
     plan.q8 = fmt.fp8 ? reinterpret_cast<uint8_t *>(ws + w.q8) : nullptr;
@@ -347,6 +350,7 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     a.done = plan.done;
     a.claim = plan.claim;
     a.calib = plan.calib;
+    a.calib_stage = plan.calib_stage;
     a.fp8 = fmt.fp8 ? 1 : 0;
     a.kv_scale = fmt.kv_scale;
     a.q8 = plan.q8;

@@ -133,7 +133,7 @@ struct Smem {
 
 // barrier offsets inside the barrier area (8 bytes each)
 constexpr int kBarFullK = 0, kBarEmptyK = 64, kBarFullV = 128, kBarEmptyV = 192;
-constexpr int kBarVtmp = 256, kBarQ = 264, kBarQe = 272, kBarS = 280, kBarSfree = 296;
+constexpr int kBarQ = 264, kBarQe = 272, kBarS = 280, kBarSfree = 296;
 constexpr int kBarP = 312, kBarPv = 320, kBarOf = 328, kBarDrainS = 336, kBarDrainPv = 344;
 constexpr int kBarPvIssued = 352;                // [4] P^T V of tile g issued, on barrier g % 4
 // S^T of tile g waits until P^T V of tile g - kLead has been issued (kLead <= 3,
@@ -602,11 +602,18 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
 // the kernel
 // ---------------------------------------------------------------------------
 
+// V boxes of 2^b token rows (b < kTailMaps) for the rows of a request's last
+// tile that lie inside its history.
+constexpr int kTailMaps = 7;
+struct TailMaps {
+    CUtensorMap m[kTailMaps];
+};
+
 template <int NG, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
-                 const DecodeArgs a)
+                 const __grid_constant__ TailMaps tail, const DecodeArgs a)
 {
     using L = Smem<NG, F8>;
     using F = Fmt<F8>;
@@ -623,7 +630,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     const uint32_t bar_empty_k = bars + kBarEmptyK;  // [NK] K slot free
     const uint32_t bar_full_v = bars + kBarFullV;    // [NV] V item ready
     const uint32_t bar_empty_v = bars + kBarEmptyV;  // [NV] V slot free
-    const uint32_t bar_vtmp = bars + kBarVtmp;       // V item of a partial tile landed (pre-mask)
     const uint32_t bar_q = bars + kBarQ;             // Q^T landed
     const uint32_t bar_qe = bars + kBarQe;           // Q^T no longer read (segment's last S^T done)
     const uint32_t bar_s = bars + kBarS;             // [2] S^T of a tile complete, per buffer
@@ -659,7 +665,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             mbar_init(bar_full_v + 8 * k, 1);
             mbar_init(bar_empty_v + 8 * k, 1);
         }
-        mbar_init(bar_vtmp, 1);
         mbar_init(bar_q, 1);
         mbar_init(bar_qe, 1);
         mbar_init(bar_s, 1);
@@ -684,6 +689,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                          smem_u32(tmem_slot)),
                      "r"(kTmemCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if (warp == kWarpVProducer) {
+        // V slots start at zero: a partial item leaves the rows past the history
+        // untouched, and they must be finite (they meet zero probabilities)
+        for (int off = 16 * lane; off < NV * kSubBytes; off += 16 * 32)
+            st_shared_v4(s_v + off, 0u, 0u, 0u, 0u);
+        fence_proxy_async();
     }
     tc_fence_before();
     __syncthreads();
@@ -789,16 +801,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         // ---------------------------------------------------------- V producer
         // bf16: V item v of a tile = latent block v / 2 (128 columns), token half
         // v % 2.  E4M3: item v = latent block v, all 128 tokens of the tile.
-        // Items of a request's last tile that reach past the history land on
-        // bar_vtmp first; the warp zeroes the rows past the history and then
-        // releases the item to the issuer.  An item entirely past the history is
-        // not loaded at all: its slot is zeroed.
+        // In a request's last tile an item loads only its rows inside the history,
+        // as boxes of power-of-two heights (the tail maps) issued together; the
+        // rows past the history keep what the slot held before -- zeros written
+        // at the start of the kernel or history rows of an earlier item, finite
+        // either way -- and their probabilities are zero.  An item wholly past the
+        // history loads nothing and is released at once.
         const uint64_t pol_once = l2_policy_evict_first();   // the tile's last read
         int slot = 0;
-        uint32_t phase = 0, vtmp_phase = 0;
+        uint32_t phase = 0;
         int issued = 0;
-        uint32_t partial_bits = 0;                   // bit b: the item issued b items ago was partial
-        bool vtmp_pending = false;                   // a partial item's copy was never seen landing
         bool ok = true;
         for (int s = seg_begin; s < seg_end && ok; ++s) {
             const int4 seg = a.segments[s];
@@ -811,57 +823,46 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 for (int v = 0; v < F::v_items; ++v) {
                     // first token of the item within the tile
                     const int toff = F8 ? 0 : 64 * (v & 1);
-                    // this item's tokens reach past the history: mask it
-                    const bool partial = t + toff + F::v_tokens > seg.z;
                     bool got = true;
                     if (lane == 0)
                         got = wait_bounded(bar_empty_v + 8 * slot, phase ^ 1, abort_flag, a.status,
                                            11);
+                    if (lane == 0 && got) {
+                        const uint32_t dst = s_v + slot * kSubBytes;
+                        const uint32_t fb = bar_full_v + 8 * slot;
+                        const int col = F8 ? 128 * v : 128 * (v >> 1), tk = tok + toff;
+                        // rows of the item inside the history
+                        const int live = seg.z - (t + toff);
+                        if (live >= F::v_tokens) {
+                            mbar_arrive_expect_tx(fb, kSubBytes);
+                            tma_load_3d_hint(dst, &tm_v, col, tk, page, fb, pol_once);
+                            if constexpr (!F8)
+                                tma_load_3d_hint(dst + kVHalf, &tm_v, col + 64, tk, page, fb,
+                                                 pol_once);
+                        } else if (live <= 0) {
+                            mbar_arrive(fb);
+                        } else {
+                            constexpr int halves = F8 ? 1 : 2;
+                            mbar_arrive_expect_tx(fb, (uint32_t)(live * 128 * halves));
+                            int r0 = 0;
+#pragma unroll
+                            for (int b = kTailMaps - 1; b >= 0; --b) {
+                                if ((live >> b) & 1) {
+                                    tma_load_3d_hint(dst + r0 * 128, &tail.m[b], col, tk + r0, page,
+                                                     fb, pol_once);
+                                    if constexpr (!F8)
+                                        tma_load_3d_hint(dst + kVHalf + r0 * 128, &tail.m[b],
+                                                         col + 64, tk + r0, page, fb, pol_once);
+                                    r0 += 1 << b;
+                                }
+                            }
+                        }
+                    }
                     if (!__shfl_sync(0xffffffffu, got ? 1 : 0, 0)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = s_v + slot * kSubBytes;
-                    const int col = F8 ? 128 * v : 128 * (v >> 1), tk = tok + toff;
-                    // all tokens of the item past the history: nothing to load
-                    const bool dead = t + toff >= seg.z;
-                    const uint32_t done_bar = partial ? bar_vtmp : bar_full_v + 8 * slot;
-                    if (lane == 0 && !dead) {
-                        mbar_arrive_expect_tx(done_bar, kSubBytes);
-                        tma_load_3d_hint(dst, &tm_v, col, tk, page, done_bar, pol_once);
-                        if constexpr (!F8)
-                            tma_load_3d_hint(dst + kVHalf, &tm_v, col + 64, tk, page, done_bar,
-                                             pol_once);
-                    }
                     ++issued;
-                    partial_bits = (partial_bits << 1) | (partial ? 1u : 0u);
-                    if (partial) {
-                        // rows r of this item hold token t + toff + r
-                        const bool landed =
-                            dead || wait_bounded(bar_vtmp, vtmp_phase, abort_flag, a.status, 12);
-                        if (!__all_sync(0xffffffffu, landed)) {
-                            vtmp_pending = true;
-                            ok = false;
-                            break;
-                        }
-                        if (!dead)
-                            vtmp_phase ^= 1;
-                        const int first_dead = seg.z - (t + toff);   // may be <= 0
-                        for (int r = lane; r < F::v_tokens; r += 32) {
-                            if (r >= first_dead) {
-#pragma unroll
-                                for (int half = 0; half < (F8 ? 1 : 2); ++half)
-#pragma unroll
-                                    for (int ch = 0; ch < 8; ++ch)
-                                        st_shared_v4(dst + half * kVHalf + r * 128 + 16 * ch, 0u,
-                                                     0u, 0u, 0u);
-                            }
-                        }
-                        fence_proxy_async();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(bar_full_v + 8 * slot);
-                    }
                     if (++slot == NV) {
                         slot = 0;
                         phase ^= 1;
@@ -870,15 +871,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             }
         }
         if (lane == 0) {
-            // copies still in flight: the last NV items that complete on their
-            // slot's barrier, and a partial item whose landing was never seen
+            // copies still in flight: at most the last NV items
             for (int back = 0; back < NV && back < issued; ++back) {
                 const int it = issued - 1 - back;
-                if (((partial_bits >> back) & 1u) == 0u)
-                    wait_drain(bar_full_v + 8 * (it % NV), (uint32_t)(it / NV) & 1u);
+                wait_drain(bar_full_v + 8 * (it % NV), (uint32_t)(it / NV) & 1u);
             }
-            if (vtmp_pending)
-                wait_drain(bar_vtmp, vtmp_phase);
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- S^T issuer
@@ -1268,18 +1265,22 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols));
     }
-    if (threadIdx.x == 0 && a.calib != nullptr && (int)sm_id < kMaxSms && *abort_flag == 0 &&
-        a.calib->cost[sm_id] < kCalibCost) {
-        // this SM's speed in the planner's cost units, from calls with real work
-        float cost = 0.f;
-        for (int s = seg_begin; s < seg_end; ++s) {
-            const int4 seg = a.segments[s];
-            cost += (float)((seg.z - seg.y + kTile - 1) / kTile +
-                            (seg.y == 0 ? kSegmentCostTiles : 0));
-        }
-        if (cost >= kCalibMinCost) {
-            atomicAdd(&a.calib->time_ns[sm_id], (float)(global_ns() - t_start));
-            atomicAdd(&a.calib->cost[sm_id], cost);
+    if (threadIdx.x == 0 && a.calib != nullptr && a.calib_stage != nullptr &&
+        (int)sm_id < kMaxSms && *abort_flag == 0) {
+        // this SM's speed in the planner's cost units, from calls with real work,
+        // into the record stage the planner named for this call
+        const int st = *a.calib_stage;
+        if (st >= 0 && st < kCalibStages && a.calib->cost[st][sm_id] < kCalibCost) {
+            float cost = 0.f;
+            for (int s = seg_begin; s < seg_end; ++s) {
+                const int4 seg = a.segments[s];
+                cost += (float)((seg.z - seg.y + kTile - 1) / kTile +
+                                (seg.y == 0 ? kSegmentCostTiles : 0));
+            }
+            if (cost >= kCalibMinCost) {
+                atomicAdd(&a.calib->time_ns[st][sm_id], (float)(global_ns() - t_start));
+                atomicAdd(&a.calib->cost[st][sm_id], cost);
+            }
         }
     }
 }
@@ -1321,60 +1322,91 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, int
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NG>
-cudaError_t make_maps_bf16(const DecodeArgs &a, CUtensorMap *maps)
+// Tensor maps over the slab (K items, V items, and the V tail boxes), kept for
+// the last slab seen by this host thread: they depend only on the slab's
+// address, page count, page stride and format.
+struct KvMaps {
+    CUtensorMap kv, v;
+    TailMaps tail;
+};
+
+bool kv_maps(const DecodeArgs &a, bool f8, KvMaps *out)
 {
-    const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const cuuint64_t kv_dims[3] = {(cuuint64_t)kRow, (cuuint64_t)kPageTokens,
-                                   (cuuint64_t)a.num_pages};
-    const cuuint64_t kv_strides[2] = {(cuuint64_t)kRow * 2, (cuuint64_t)a.page_stride * 2};
-    const cuuint32_t kv_box[3] = {64, (cuuint32_t)kTile, 1};
-    const cuuint32_t v_box[3] = {64, 64, 1};
+    thread_local struct {
+        bool valid;
+        const void *slab;
+        int64_t pages, stride;
+        bool f8;
+        KvMaps maps;
+    } cache = {};
+    if (cache.valid && cache.slab == a.slab && cache.pages == a.num_pages &&
+        cache.stride == a.page_stride && cache.f8 == f8) {
+        *out = cache.maps;
+        return true;
+    }
+    const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const cuuint64_t esize = f8 ? 1 : 2;
+    const cuuint64_t dims[3] = {(cuuint64_t)kRow, (cuuint64_t)kPageTokens, (cuuint64_t)a.num_pages};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRow * esize, (cuuint64_t)a.page_stride * esize};
+    // one box row is 128 bytes: 64 bf16 or 128 E4M3 columns
+    const cuuint32_t cols = f8 ? 128 : 64;
+    const cuuint32_t kv_box[3] = {cols, (cuuint32_t)kTile, 1};
+    const cuuint32_t v_box[3] = {cols, f8 ? (cuuint32_t)kTile : 64u, 1};
+    KvMaps m;
+    if (!make_map(&m.kv, dt, a.slab, 3, dims, strides, kv_box) ||
+        !make_map(&m.v, dt, a.slab, 3, dims, strides, v_box))
+        return false;
+    for (int b = 0; b < kTailMaps; ++b) {
+        const cuuint32_t rows = 1u << b;
+        const cuuint32_t box[3] = {cols, rows < v_box[1] ? rows : v_box[1], 1};
+        if (!make_map(&m.tail.m[b], dt, a.slab, 3, dims, strides, box))
+            return false;
+    }
+    cache.valid = true;
+    cache.slab = a.slab;
+    cache.pages = a.num_pages;
+    cache.stride = a.page_stride;
+    cache.f8 = f8;
+    cache.maps = m;
+    *out = m;
+    return true;
+}
+
+// Query maps: bf16 q_nope (64-column boxes) and q_rope, or the quantised E4M3
+// rows [R*n_q*H, 576] (128-column boxes; the second map is then unused).
+template <int NG>
+bool q_maps(const DecodeArgs &a, bool f8, CUtensorMap *qn, CUtensorMap *qr)
+{
     const cuuint64_t rows = (cuuint64_t)a.num_reqs * a.rows_per_req;
+    if (f8) {
+        const cuuint64_t q_dims[2] = {(cuuint64_t)kRow, rows};
+        const cuuint64_t q_strides[1] = {(cuuint64_t)kRow};
+        const cuuint32_t q_box[2] = {128, (cuuint32_t)NG};
+        if (!make_map(qn, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q8, 2, q_dims, q_strides, q_box))
+            return false;
+        *qr = *qn;
+        return true;
+    }
+    const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const cuuint64_t qn_dims[2] = {(cuuint64_t)kLatent, rows};
     const cuuint64_t qn_strides[1] = {(cuuint64_t)kLatent * 2};
     const cuuint64_t qr_dims[2] = {(cuuint64_t)kRope, rows};
     const cuuint64_t qr_strides[1] = {(cuuint64_t)kRope * 2};
     const cuuint32_t q_box[2] = {64, (cuuint32_t)NG};
-    if (!make_map(&maps[0], bf16, a.slab, 3, kv_dims, kv_strides, kv_box) ||
-        !make_map(&maps[1], bf16, a.slab, 3, kv_dims, kv_strides, v_box) ||
-        !make_map(&maps[2], bf16, a.q_nope, 2, qn_dims, qn_strides, q_box) ||
-        !make_map(&maps[3], bf16, a.q_rope, 2, qr_dims, qr_strides, q_box))
-        return cudaErrorInvalidValue;
-    return cudaSuccess;
-}
-
-// E4M3 pages: byte tensors; K and V items use the same 128 x 128 box, and the
-// queries are the quantised rows [R*n_q*H, 576] (the fourth map is unused).
-template <int NG>
-cudaError_t make_maps_e4m3(const DecodeArgs &a, CUtensorMap *maps)
-{
-    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    const cuuint64_t kv_dims[3] = {(cuuint64_t)kRow, (cuuint64_t)kPageTokens,
-                                   (cuuint64_t)a.num_pages};
-    const cuuint64_t kv_strides[2] = {(cuuint64_t)kRow, (cuuint64_t)a.page_stride};
-    const cuuint32_t kv_box[3] = {128, (cuuint32_t)kTile, 1};
-    const cuuint64_t rows = (cuuint64_t)a.num_reqs * a.rows_per_req;
-    const cuuint64_t q_dims[2] = {(cuuint64_t)kRow, rows};
-    const cuuint64_t q_strides[1] = {(cuuint64_t)kRow};
-    const cuuint32_t q_box[2] = {128, (cuuint32_t)NG};
-    if (!make_map(&maps[0], u8, a.slab, 3, kv_dims, kv_strides, kv_box) ||
-        !make_map(&maps[2], u8, a.q8, 2, q_dims, q_strides, q_box))
-        return cudaErrorInvalidValue;
-    maps[1] = maps[0];
-    maps[3] = maps[2];
-    return cudaSuccess;
+    return make_map(qn, bf16, a.q_nope, 2, qn_dims, qn_strides, q_box) &&
+           make_map(qr, bf16, a.q_rope, 2, qr_dims, qr_strides, q_box);
 }
 
 template <int NG, bool F8>
 cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
 {
-    CUtensorMap maps[4];
-    cudaError_t err = F8 ? make_maps_e4m3<NG>(a, maps) : make_maps_bf16<NG>(a, maps);
-    if (err != cudaSuccess)
-        return err;
+    KvMaps kv;
+    CUtensorMap qn, qr;
+    if (!kv_maps(a, F8, &kv) || !q_maps<NG>(a, F8, &qn, &qr))
+        return cudaErrorInvalidValue;
     constexpr int smem = Smem<NG, F8>::alloc;
-    err = cudaFuncSetAttribute(decode_tc_kernel<NG, F8>,
+    cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<NG, F8>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess)
         return err;
@@ -1388,8 +1420,7 @@ cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NG, F8>, maps[0], maps[1], maps[2], maps[3],
-                              a);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NG, F8>, kv.kv, kv.v, qn, qr, kv.tail, a);
 }
 
 }  // namespace

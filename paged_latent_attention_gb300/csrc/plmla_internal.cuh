@@ -31,15 +31,19 @@ constexpr float kCalibMinCost = 16.f;   // a call adds to the record only with t
 // summed over calls in which the SM's CTA had at least kCalibMinCost of work,
 // until kCalibCost units are measured.  SMs of one chip run the same code at
 // repeatably different speeds (some TPCs sit closer to their GPC's crossbar
-// port, some GPCs have fewer TPCs), so once every SM of the grid is measured
-// the planner gives each CTA a share of the work proportional to its SM's
-// speed; until then, and for ever after, the shares are fixed.
+// port, some GPCs have fewer TPCs), so the planner gives each CTA a share of
+// the work proportional to its SM's measured speed.  The record has stages:
+// stage 0 is measured under equal shares, stage k under the shares computed from
+// stage k - 1.  Equal shares let the fast SMs idle at the end, and the slow ones
+// then run alone and faster, so one stage under-corrects; a later stage
+// measures every SM busy for the whole kernel.  Once every stage is complete the
+// shares stay fixed (results are then bit-stable from call to call).
+constexpr int kCalibStages = 3;
 struct SmCalib {
-    float cost[kMaxSms];
-    float time_ns[kMaxSms];
-    // the planner's member weight prefix for one grid shape, computed once all
-    // of that grid's SMs are measured (their records no longer change)
-    int32_t cache_members, cache_teams;
+    float cost[kCalibStages][kMaxSms];
+    float time_ns[kCalibStages][kMaxSms];
+    // the planner's member weight prefix for one grid shape and stage
+    int32_t cache_members, cache_teams, cache_stage;
     float cache_wprefix[kMaxSms + 1];
 };
 
@@ -57,6 +61,7 @@ struct PlanBuffers {
     int32_t *claim;             // [n_claim] CTA-index claims of the decode grid, zeroed here
     int32_t n_claim;
     SmCalib *calib;             // per-device speed record (null: equal shares)
+    int32_t *calib_stage;       // [1] written: the record stage this call's decode fills (-1: none)
     // FP8 decode: extra CTAs of the plan grid quantise the queries (null: none)
     const __nv_bfloat16 *q_nope; // [q_rows, 512]
     const __nv_bfloat16 *q_rope; // [q_rows, 64]
@@ -89,6 +94,7 @@ struct DecodeArgs {
     int32_t *done;                 // [groups * R] segments of (team, request) written
     int32_t *claim;                // [groups * members] CTA indices taken (zeroed by the plan)
     SmCalib *calib;                // per-device speed record, or null
+    const int32_t *calib_stage;    // stage of the record to add this call's timing to (-1: none)
     // FP8 pages: slab holds E4M3 bytes (value = kv_scale * byte), the queries are
     // read as E4M3 codes q8 with per-row exponents qexp (written by the plan grid)
     int32_t fp8;

@@ -260,10 +260,19 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     const int teams = n_cta / max(members, 1);
     int cache_hit = 0;
     float cached_w = 0.f;
+    bool rec_done[kCalibStages];                // this thread's SM finished each record stage
+#pragma unroll
+    for (int k = 0; k < kCalibStages; ++k)
+        rec_done[k] = true;
     if (cal != nullptr) {
         cache_hit = cal->cache_members == members && cal->cache_teams == teams;
         if (tid <= kMaxSms)
             cached_w = cal->cache_wprefix[tid];
+        if (tid < n_cta && n_cta <= kMaxSms) {
+#pragma unroll
+            for (int k = 0; k < kCalibStages; ++k)
+                rec_done[k] = cal->cost[k][tid] >= kCalibCost && cal->time_ns[k][tid] > 0.f;
+        }
     }
     // finished-segment counters and CTA claims of this call's decode start from zero
     if (plan.done != nullptr)
@@ -382,9 +391,20 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     }
 
     // ---- member shares: CTA c of the decode grid runs on the SM with id c when
-    // it can (it claims that index), so once every such SM's speed is measured,
-    // member m of every team gets a share of the cost proportional to the mean
-    // speed of SMs team*members + m; until then the shares are equal
+    // it can (it claims that index).  `stage` = the number of record stages that
+    // every such SM has completed; with stage >= 1, member m of every team gets a
+    // share of the cost proportional to the mean speed of SMs team*members + m
+    // in record stage - 1, otherwise the shares are equal.  This call's decode
+    // adds its timing to record `stage` (if any is left).
+    const bool usable = cal != nullptr && teams >= 1 && n_cta <= kMaxSms;
+    int stage = 0;
+#pragma unroll
+    for (int k = 0; k < kCalibStages; ++k)
+        if (__syncthreads_and(usable && rec_done[k]) && stage == k)
+            stage = k + 1;
+    if (tid == 0 && plan.calib_stage != nullptr)
+        *plan.calib_stage = usable && stage < kCalibStages ? stage : -1;
+    cache_hit = cache_hit && stage >= 1 && cal->cache_stage == stage;
     if (cache_hit) {
         if (tid <= members)
             sm.wprefix[tid] = cached_w;
@@ -392,14 +412,11 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
             sm.weighted = 1;
         __syncthreads();
     } else {
-        const bool usable = cal != nullptr && teams >= 1 && n_cta <= kMaxSms;
-        bool measured = true;
-        if (usable && tid < n_cta) {
-            const float c = cal->cost[tid], t = cal->time_ns[tid];
-            measured = c >= kCalibCost && t > 0.f;
-            sm.wrate[tid] = measured ? c / t : 0.f;
+        if (usable && stage >= 1 && tid < n_cta) {
+            const float c = cal->cost[stage - 1][tid], t = cal->time_ns[stage - 1][tid];
+            sm.wrate[tid] = c / t;
         }
-        const int ready = __syncthreads_and(usable && measured);
+        const int ready = __syncthreads_or(stage >= 1);
         if (ready && tid < 32) {
             // member rate (mean over teams), then an inclusive prefix in warp 0:
             // lane l owns members [8l, 8l + 8)
@@ -439,7 +456,8 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
             sm.weighted = ready ? 1 : 0;
         __syncthreads();
         if (ready) {
-            // the records of this grid's SMs are final: keep the prefix for later calls
+            // the record stage this prefix comes from is complete: keep it for
+            // later calls of this grid shape until the next stage completes
             SmCalib *wcal = plan.calib;
             if (tid <= members)
                 wcal->cache_wprefix[tid] = sm.wprefix[tid];
@@ -448,6 +466,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
             if (tid == 0) {
                 wcal->cache_teams = teams;
                 wcal->cache_members = members;
+                wcal->cache_stage = stage;
             }
         }
     }
