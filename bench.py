@@ -57,7 +57,7 @@ def parse_args(argv=None):
                     help="cache format: bf16 pages (the default workload) or E4M3 pages "
                          "(the deployment's FP8 cache, 576 bytes per token row)")
     ap.add_argument("--workload", default="steady",
-                    choices=["tiny", "steady", "agentic", "spec", "long"])
+                    choices=["tiny", "steady", "agentic", "spec", "long", "extend"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -250,18 +250,32 @@ def oracle_sample(w, qn, qr, gate, slab_dev, req_ids):
             len(phys))
 
 
-def run_oracle(w, sample, kv_scale=None):
+def row_sample(w, n_reqs):
+    """Output rows the oracle computes for a sample of n_reqs requests, and the
+    fraction of the requests' rows they are.  Workloads with many query rows per
+    request (a chunked extend) take the first, middle and last new token, four
+    heads each; the others take every row."""
+    rows_per_req = w.n_q * w.num_heads
+    if rows_per_req <= 256:
+        return None, 1.0
+    toks = sorted({0, w.n_q // 2, w.n_q - 1})
+    heads = range(min(4, w.num_heads))
+    rows = [(i * w.n_q + j) * w.num_heads + h for i in range(n_reqs) for j in toks for h in heads]
+    return rows, len(toks) * len(heads) / rows_per_req
+
+
+def run_oracle(w, sample, kv_scale=None, rows=None):
     import oracle
     qn, qr, gate, slab, table, lens, npages = sample
     t = time.perf_counter()
     if kv_scale is None:
         oracle.mla_decode_reference(qn, qr, gate, slab, table, lens, w.n_q, w.num_heads,
                                     1.0 / math.sqrt(192.0), num_pages=npages,
-                                    page_stride=w.page_stride)
+                                    page_stride=w.page_stride, rows=rows)
     else:
         oracle.mla_decode_e4m3_reference(qn, qr, gate, slab, kv_scale, table, lens, w.n_q,
                                          w.num_heads, 1.0 / math.sqrt(192.0), num_pages=npages,
-                                         page_stride=w.page_stride)
+                                         page_stride=w.page_stride, rows=rows)
     return time.perf_counter() - t
 
 
@@ -274,19 +288,24 @@ def cpu_baseline(w, qn, qr, gate, slab_dev, target_s, kv_scale=None):
     cores = oracle.oracle.default_threads()
     order = list(range(w.num_reqs))
     one = oracle_sample(w, qn, qr, gate, slab_dev, order[:1])
-    t1 = run_oracle(w, one, kv_scale)
+    t1 = run_oracle(w, one, kv_scale, row_sample(w, 1)[0])
     n = max(1, min(w.num_reqs, int(target_s / max(t1, 1e-3))))
     sample = oracle_sample(w, qn, qr, gate, slab_dev, order[:n])
+    rows, frac = row_sample(w, n)
     elapsed, reps = 0.0, 0
     while elapsed < 0.5 * target_s or reps == 0:
-        elapsed += run_oracle(w, sample, kv_scale)
+        elapsed += run_oracle(w, sample, kv_scale, rows)
         reps += 1
+    # KV bytes credited in proportion to the rows computed
     kv = int(sum(int(w.seq_lens[r]) for r in order[:n])) * kv_row_bytes(w, kv_scale is not None)
-    gbs = kv * reps / elapsed / 1e9
+    gbs = frac * kv * reps / elapsed / 1e9
+    what = ("all {} heads".format(w.num_heads) if rows is None else
+            f"{frac:.4f} of the rows (first, middle and last new token, 4 heads)")
     return {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {w.num_reqs} requests x all {w.num_heads} heads, {reps} pass(es), "
-                      f"{elapsed:.1f} s of double-precision oracle time",
-            "request_steps_per_s": n * reps / elapsed}
+            "sample": f"{n} of {w.num_reqs} requests x {what}, {reps} pass(es), "
+                      f"{elapsed:.1f} s of double-precision oracle time, KV bytes credited "
+                      f"in proportion to the rows",
+            "request_steps_per_s": frac * n * reps / elapsed}
 
 
 # --------------------------------------------------------------------------
@@ -407,7 +426,7 @@ def run_gpu(args):
     if fp8:
         # E4M3 MMAs run at twice the bf16 rate (nominal 4.5 vs 2.25 PFLOP/s dense)
         tpeak, tpeak_src = 2.0 * tpeak, tpeak_src + " x 2 (nominal E4M3 / bf16 ratio)"
-    flops_layer = 2.0 * (w.dc + w.dr + w.dc) * w.n_q * w.num_heads * w.kv_tokens
+    flops_layer = 2.0 * (w.dc + w.dr + w.dc) * w.visible_pairs
     intensity = flops_layer / kv_bytes_layer
     ridge = tpeak * 1e12 / (peak * 1e9)
     if intensity > ridge:
@@ -739,19 +758,23 @@ def run_reference(args):
     total = args.steps + args.warmup
     budget_s = 150.0
     one = oracle_sample(w, qn, qr, gate, slab, [0])
-    t1 = run_oracle(w, one, kv_scale)
+    t1 = run_oracle(w, one, kv_scale, row_sample(w, 1)[0])
     per_step = max(1, min(w.num_reqs, int(budget_s / total / max(t1, 1e-3))))
+    rows, frac = row_sample(w, per_step)
     times, kv = [], []
     for s in range(total):
         ids = [(s * per_step + i) % w.num_reqs for i in range(per_step)]
         sample = oracle_sample(w, qn, qr, gate, slab, ids)
-        dt = run_oracle(w, sample, kv_scale)
+        dt = run_oracle(w, sample, kv_scale, rows)
         if s >= args.warmup:
             times.append(dt)
-            kv.append(sum(int(w.seq_lens[r]) for r in ids) * kv_row_bytes(w, fp8))
+            kv.append(frac * sum(int(w.seq_lens[r]) for r in ids) * kv_row_bytes(w, fp8))
     elapsed = sum(times)
     value = sum(kv) / elapsed / 1e9
-    desc = (f"{per_step} of {w.num_reqs} requests x all {w.num_heads} heads per step "
+    what = (f"all {w.num_heads} heads" if rows is None else
+            f"{frac:.4f} of the rows (first, middle and last new token, 4 heads; KV bytes "
+            f"credited in proportion)")
+    desc = (f"{per_step} of {w.num_reqs} requests x {what} per step "
             f"(requests taken in rotation), double-precision oracle")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,

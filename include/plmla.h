@@ -141,7 +141,10 @@ plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_reqs, int32_t 
  * page_table       int32, row r at page_table + r*page_table_ld (row stride honoured)
  * page_table_ld    >= ceil(max_r L_r / 1536)
  * seq_lens         int32 [num_reqs], device (history incl. the n_q drafts)
- * num_reqs         1 .. 1024;  n_q_per_req 1 .. 16;  num_heads multiple of 16, <= 128
+ * num_reqs         1 .. 1024;  n_q_per_req 1 .. 256 (draft tokens of a verify step,
+ *                  or a chunk of new tokens: a chunked extend / prefill over the
+ *                  pages, whose KV rows were appended before the call);
+ *                  num_heads multiple of 16, <= 128
  * scale            softmax scale (1/sqrt(192) for a 128+64 head)
  * out              bf16 [num_reqs*n_q_per_req, num_heads, 512], written
  * lse              fp32 [num_reqs*n_q_per_req, num_heads], written (may be NULL)

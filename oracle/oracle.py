@@ -92,6 +92,23 @@ def _as_f64(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float64)
 
 
+def _rows_f64(q, rows, width) -> np.ndarray:
+    """[total rows, width] float64 holding the listed rows of q (the rest zero)."""
+    if hasattr(q, "detach"):
+        import torch
+        flat = q.detach().reshape(-1, width)
+        total = flat.shape[0]
+        idx = torch.as_tensor(rows, dtype=torch.long, device=flat.device)
+        picked = _as_f64(flat.index_select(0, idx).contiguous())
+    else:
+        flat = np.asarray(q).reshape(-1, width)
+        total = flat.shape[0]
+        picked = _as_f64(np.ascontiguousarray(flat[rows]))
+    out = np.zeros((total, width), dtype=np.float64)
+    out[rows] = picked
+    return out
+
+
 def _i32(a) -> np.ndarray:
     if hasattr(a, "cpu"):
         a = a.detach().cpu().numpy()
@@ -124,7 +141,12 @@ def attend_rows(q_nope, q_rope, slab, page_table, seq_lens, n_q, num_heads, scal
     E4M3 bytes and an element's value is kv_scale times the decoded byte.
     """
     lib = _load()
-    qn, qr = _as_f64(q_nope), _as_f64(q_rope)
+    if rows is None:
+        qn, qr = _as_f64(q_nope), _as_f64(q_rope)
+    else:
+        # only the requested rows are widened; the others are never read
+        sel = np.asarray(rows, dtype=np.int64)
+        qn, qr = _rows_f64(q_nope, sel, dc), _rows_f64(q_rope, sel, dr)
     if kv_format == "bf16":
         sl, fp8 = _u16(slab), 0
     elif kv_format == "e4m3":

@@ -136,9 +136,12 @@ constexpr int kBarFullK = 0, kBarEmptyK = 64, kBarFullV = 128, kBarEmptyV = 192;
 constexpr int kBarQ = 264, kBarQe = 272, kBarS = 280, kBarSfree = 296;
 constexpr int kBarP = 312, kBarPv = 320, kBarOf = 328, kBarDrainS = 336, kBarDrainPv = 344;
 constexpr int kBarPvIssued = 352;                // [4] P^T V of tile g issued, on barrier g % 4
-// S^T of tile g waits until P^T V of tile g - kLead has been issued (kLead <= 3,
-// so that the next phase of that barrier, tile g - kLead + 4, cannot complete first)
-constexpr int kLead = 2;
+// S^T of tile g waits until P^T V of tile g - lead has been issued (lead <= 3,
+// so that the next phase of that barrier, tile g - lead + 4, cannot complete
+// first): two tiles for bf16 pages, three for E4M3 pages, whose tiles are half
+// the bytes (measured best for each).
+template <bool F8>
+constexpr int kLead = F8 ? 3 : 2;
 
 // ---------------------------------------------------------------------------
 // PTX wrappers
@@ -898,16 +901,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 for (int i = 0; i < n_tiles; ++i, ++g) {
                     const uint32_t b = g & 1;
                     // the softmax of tile g - 2 must be done with this S^T buffer, and
-                    // S^T runs at most kLead tiles ahead of P^T V, so that a tile's
+                    // S^T runs at most kLead<F8> tiles ahead of P^T V, so that a tile's
                     // latent blocks are still in L2 when they are read again as V items
                     if (g >= 2 && !wait_bounded(bar_sfree + 8 * b, ((g - 2) >> 1) & 1, abort_flag,
                                                 a.status, 13)) {
                         ok = false;
                         break;
                     }
-                    if (g >= kLead &&
-                        !wait_bounded(bars + kBarPvIssued + 8 * ((g - kLead) & 3),
-                                      ((g - kLead) >> 2) & 1, abort_flag, a.status, 10)) {
+                    constexpr int lead = kLead<F8>;
+                    static_assert(lead >= 1 && lead <= 3, "lead");
+                    if (g >= lead &&
+                        !wait_bounded(bars + kBarPvIssued + 8 * ((g - lead) & 3),
+                                      ((g - lead) >> 2) & 1, abort_flag, a.status, 10)) {
                         ok = false;
                         break;
                     }

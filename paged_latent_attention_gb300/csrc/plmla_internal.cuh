@@ -14,7 +14,9 @@ constexpr int kRow = kLatent + kRope;
 constexpr int kPageTokens = 1536; // token rows per MLA page
 constexpr int kTile = 128;        // KV tokens per decode tile; chunks are multiples of it
 constexpr int kMaxReqs = 1024;
-constexpr int kMaxNq = 16;
+// query tokens per request: draft tokens of a verify step (4) up to a chunk of
+// new tokens of an extend (prefill) step, causal among themselves
+constexpr int kMaxNq = 256;
 constexpr int kMaxPlanSplits = 4096;  // chunks the device planner can schedule
 constexpr int kChunksPerMember = 26;  // default chunk budget per persistent CTA
 // Planner cost of starting a segment, in 128-token tiles: a request's first

@@ -20,6 +20,10 @@ Workloads (history-length mixes, pool sizes and seeds):
   long     4 x 1 at 1,000,000 tokens, 64 heads, 24 slabs (one per MLA layer)
            sharing one table of 652 pages per request, >= 128 splits per
            request, seed 4
+  extend   4 requests x 128 new tokens (a chunked extend: causal among the
+           new tokens, whose rows are the history's last 128), 64 heads,
+           histories uniform in [8192, 32768], pool = pages needed + 10%,
+           seed 5
 
 Values: q, KV rows and gate logits are N(0, 1) rounded to bf16.  Tail rows of a
 request's last page and free pages may be poisoned with NaN (reused pages can
@@ -72,6 +76,15 @@ class Workload:
     @property
     def kv_bytes_per_layer(self) -> int:
         return self.kv_tokens * (self.dc + self.dr) * 2
+
+    @property
+    def visible_pairs(self) -> int:
+        """(query row, KV token) pairs of one layer: draft/new token j of request
+        r sees seq_lens[r] - (n_q - 1 - j) tokens, for each of the heads."""
+        L = np.asarray(self.seq_lens, dtype=np.int64)
+        j = np.arange(self.n_q, dtype=np.int64)
+        vis = np.maximum(0, L[:, None] - (self.n_q - 1 - j[None, :]))
+        return int(vis.sum()) * self.num_heads
 
 
 def _pages_for(lengths, page_tokens):
@@ -128,6 +141,13 @@ def make_workload(name: str) -> Workload:
         pages = need + -(-need // 10)
         table = _assign_pages(rng, lens, pages, PAGE_TOKENS)
         return Workload("spec", 128, 4, 64, lens, table, pages, seed=3)
+    if name == "extend":
+        rng = np.random.Generator(np.random.PCG64(5))
+        lens = rng.integers(8192, 32768, size=4, endpoint=True).astype(np.int32)
+        need = sum(_pages_for(lens, PAGE_TOKENS))
+        pages = need + -(-need // 10)
+        table = _assign_pages(rng, lens, pages, PAGE_TOKENS)
+        return Workload("extend", 4, 128, 64, lens, table, pages, seed=5)
     if name == "long":
         rng = np.random.Generator(np.random.PCG64(4))
         lens = np.full(4, 1_000_000, dtype=np.int32)
@@ -137,7 +157,7 @@ def make_workload(name: str) -> Workload:
     raise KeyError(name)
 
 
-WORKLOAD_NAMES = ("tiny", "steady", "agentic", "spec", "long")
+WORKLOAD_NAMES = ("tiny", "steady", "agentic", "spec", "long", "extend")
 
 
 def custom_workload(lengths, n_q, num_heads, *, seed=0, spare_pages=2, page_tokens=PAGE_TOKENS,

@@ -94,3 +94,27 @@ def test_more_than_256_ctas_per_row_group_is_rejected(lib):
     assert lib.mla_workspace_size(64, 1, 64, 257, 1) == 0
     # four row groups: 1024 slots give 256 CTAs per group
     assert lib.mla_split_budget(8, 4, 64, 1024, 1) > 0
+
+
+def test_query_token_limit_and_fp8_arguments(lib):
+    # up to 256 query tokens per request (a chunk of new tokens), not more
+    assert lib.mla_split_budget(4, 256, 64, 152, 1) > 0
+    assert lib.mla_split_budget(4, 257, 64, 152, 1) == -1
+    assert lib.mla_workspace_size_fp8(4, 257, 64, 152, 1) == 0
+    # the FP8 workspace adds the quantised queries: 576 bytes and an exponent per row
+    extra = lib.mla_workspace_size_fp8(64, 1, 64, 152, 1) - lib.mla_workspace_size(64, 1, 64, 152, 1)
+    assert extra >= 64 * 64 * (576 + 4)
+    fake = 1 << 20
+
+    def fp8(stride=1536 * 576, kv_scale=0.5):
+        return lib.mla_decode_fp8(fake, fake, fake, fake, 8, stride, ctypes.c_float(kv_scale), fake,
+                                  1, fake, 2, 1, 16, ctypes.c_float(0.07), fake, None, fake, 1 << 30,
+                                  152, 1, None)
+    assert fp8(stride=1536 * 576 + 8) == 1       # E4M3 page stride not a multiple of 16 bytes
+    assert fp8(kv_scale=0.0) == 1
+    assert fp8(kv_scale=float("inf")) == 1
+    assert fp8(kv_scale=-1.0) == 1
+    assert lib.mla_kv_append_fp8(fake, fake, fake, 8, 1536 * 576, ctypes.c_float(0.0), fake, 1,
+                                 fake, 1, 1, None, None) == 1
+    assert lib.mla_quantize_queries_fp8(fake + 4, fake, 4, fake, fake, None) == 1
+    assert lib.mla_quantize_queries_fp8(None, None, 0, None, None, None) == 0
