@@ -106,10 +106,14 @@ struct Smem {
     static constexpr int pn = F8 && NG < 32 ? 32 : NG;      // P^T columns (MMA N of P^T V)
     static constexpr int p_row = F8 ? pn : 2 * NG;          // bytes per token row of P^T
     static constexpr int q_chunk = NG * 128;                // one 128-byte column block of Q^T
+    // Q^T: bf16 nine 128-byte blocks; E4M3 four 128-byte latent blocks and the rope
+    // block of 64 bytes per row (64-byte swizzle)
+    static constexpr int q_rope_bytes = F8 ? NG * 64 : q_chunk;
+    static constexpr int q_bytes = (F::sub - 1) * q_chunk + q_rope_bytes;
     static constexpr int p_bytes = kTile * p_row;           // P^T
     static constexpr int bar_bytes = 512;
     static constexpr int misc_bytes = bar_bytes + 4 * 64 * 4 + 4 * 64 * 4 + 32;
-    static constexpr int fixed = p_bytes + F::sub * q_chunk + misc_bytes + 1024;
+    static constexpr int fixed = p_bytes + q_bytes + misc_bytes + 1024;
     static constexpr int slots_fit = (kMaxDynSmem - fixed) / kSubBytes;
     // bf16: half of the slots for each ring; E4M3: one tile of V items, the rest K
     static constexpr int v_slots = F8 ? 4 : (slots_fit / 2 < kMaxV ? slots_fit / 2 : kMaxV);
@@ -117,7 +121,7 @@ struct Smem {
     static constexpr int v_off = k_slots * kSubBytes;
     static constexpr int p_off = v_off + v_slots * kSubBytes;
     static constexpr int q_off = p_off + p_bytes;            // 1024-aligned
-    static constexpr int bar_off = q_off + F::sub * q_chunk; // 1024-aligned
+    static constexpr int bar_off = q_off + q_bytes;          // 1024-aligned
     static constexpr int red_off = bar_off + bar_bytes;      // float red[4][64]
     static constexpr int fin_off = red_off + 4 * 64 * 4;     // float fin[64]
     static constexpr int m_off = fin_off + 64 * 4;           // float m[64]   (log2 units)
@@ -127,7 +131,8 @@ struct Smem {
     static constexpr int bytes = misc_off + 32;
     static constexpr int alloc = bytes + 1024;               // slack for 1024-B alignment
     static_assert(k_slots >= 2 && v_slots >= 2, "ring depth");
-    static_assert(p_bytes % 1024 == 0 && q_chunk % 1024 == 0, "swizzle atom alignment");
+    static_assert(p_bytes % 1024 == 0 && q_chunk % 1024 == 0 && q_bytes % 1024 == 0,
+                  "swizzle atom alignment");
     static_assert(alloc <= kMaxDynSmem, "shared memory budget");
 };
 
@@ -757,12 +762,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     break;
                 }
                 const int qrow = seg.x * a.rows_per_req + row0;
-                mbar_arrive_expect_tx(bar_q, F::sub * L::q_chunk);
+                mbar_arrive_expect_tx(bar_q, L::q_bytes);
                 if constexpr (F8) {
-                    // E4M3 rows of 576 bytes: four latent blocks and the rope block
-                    // (its columns past 576 are zero-filled)
-                    for (int k = 0; k < F::sub; ++k)
+                    // E4M3 rows of 576 bytes: four latent blocks, then the 64-byte rope
+                    // block through its own map
+                    for (int k = 0; k < F::sub - 1; ++k)
                         tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 128 * k, qrow, bar_q);
+                    tma_load_2d(s_q + (F::sub - 1) * L::q_chunk, &tm_qr, kLatent, qrow, bar_q);
                 } else {
                     for (int k = 0; k < F::sub - 1; ++k)
                         tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 64 * k, qrow, bar_q);
@@ -887,6 +893,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             constexpr uint32_t idesc_s = idesc_for<F8>(128, NG, false, false);
             const uint64_t dk0 = sdesc(s_k, 16, 1024, kSw128);
             const uint64_t dq0 = sdesc(s_q, 16, 1024, kSw128);
+            const uint64_t dq_rope =
+                sdesc(s_q + (F::sub - 1) * L::q_chunk, 16, F8 ? 512 : 1024, F8 ? kSw64 : kSw128);
             int slot = 0;
             uint32_t phase = 0;
             int g = 0;                               // tiles so far (all segments)
@@ -931,10 +939,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                         const int n_mma = k == F::sub - 1 ? last_mmas : 4;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            if (kk < n_mma)
-                                mma<F8>(d_s, da + 2 * kk,
-                                        dq0 + (uint64_t)(k * (L::q_chunk >> 4) + 2 * kk), idesc_s,
-                                        (k | kk) != 0);
+                            if (kk < n_mma) {
+                                // the E4M3 rope block of Q^T has 64-byte rows
+                                const uint64_t db =
+                                    (F8 && k == F::sub - 1) ? dq_rope + 2 * kk
+                                                            : dq0 + (uint64_t)(k * (L::q_chunk >> 4) + 2 * kk);
+                                mma<F8>(d_s, da + 2 * kk, db, idesc_s, (k | kk) != 0);
+                            }
                         mma_commit(bar_empty_k + 8 * slot);
                         issued = true;
                         if (++slot == NK) {
@@ -1315,7 +1326,8 @@ EncodeTiledFn encode_fn()
 }
 
 bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, int rank,
-              const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box)
+              const cuuint64_t *dims, const cuuint64_t *strides, const cuuint32_t *box,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
     EncodeTiledFn fn = encode_fn();
     if (fn == nullptr)
@@ -1323,8 +1335,8 @@ bool make_map(CUtensorMap *map, CUtensorMapDataType dtype, const void *base, int
     const cuuint32_t estr[3] = {1, 1, 1};
     // out-of-range elements (the E4M3 rope block's columns past 576) read as zero
     return fn(map, dtype, rank, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Tensor maps over the slab (K items, V items, and the V tail boxes), kept for
@@ -1379,7 +1391,8 @@ bool kv_maps(const DecodeArgs &a, bool f8, KvMaps *out)
 }
 
 // Query maps: bf16 q_nope (64-column boxes) and q_rope, or the quantised E4M3
-// rows [R*n_q*H, 576] (128-column boxes; the second map is then unused).
+// rows [R*n_q*H, 576]: 128-byte boxes for the latent, a 64-byte box (64-byte
+// swizzle) for the rope.
 template <int NG>
 bool q_maps(const DecodeArgs &a, bool f8, CUtensorMap *qn, CUtensorMap *qr)
 {
@@ -1388,10 +1401,10 @@ bool q_maps(const DecodeArgs &a, bool f8, CUtensorMap *qn, CUtensorMap *qr)
         const cuuint64_t q_dims[2] = {(cuuint64_t)kRow, rows};
         const cuuint64_t q_strides[1] = {(cuuint64_t)kRow};
         const cuuint32_t q_box[2] = {128, (cuuint32_t)NG};
-        if (!make_map(qn, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q8, 2, q_dims, q_strides, q_box))
-            return false;
-        *qr = *qn;
-        return true;
+        const cuuint32_t r_box[2] = {64, (cuuint32_t)NG};
+        return make_map(qn, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q8, 2, q_dims, q_strides, q_box) &&
+               make_map(qr, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.q8, 2, q_dims, q_strides, r_box,
+                        CU_TENSOR_MAP_SWIZZLE_64B);
     }
     const CUtensorMapDataType bf16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const cuuint64_t qn_dims[2] = {(cuuint64_t)kLatent, rows};
