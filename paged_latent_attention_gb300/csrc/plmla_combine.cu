@@ -70,6 +70,9 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
                int num_heads, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
                const int32_t *__restrict__ done, int32_t *status)
 {
+    // The next kernel on the stream may launch now (the decode step's planner
+    // waits on entry for this grid to complete).
+    asm volatile("griddepcontrol.launch_dependents;");
     // Without counters: launched as a programmatic dependent of the decode
     // kernel (or on its own), wait for the previous grid's partial states.
     if (done == nullptr)

@@ -232,6 +232,10 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     extern __shared__ __align__(16) unsigned char plan_smem_raw[];
     PlanSmem &sm = *reinterpret_cast<PlanSmem *>(plan_smem_raw);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // Launched as a programmatic dependent of whatever ran before it on the
+    // stream: wait for that grid (it may have written seq_lens or the queries,
+    // or still read this workspace) before touching memory.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // the decode kernel may start its prologue now; it waits for this grid's
     // completion before reading the plan (and the FP8 queries)
     asm volatile("griddepcontrol.launch_dependents;");
@@ -648,9 +652,19 @@ cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int m
         return err;
     const int qctas =
         plan.q8 != nullptr ? (plan.q_rows + kQuantRowsPerCta - 1) / kQuantRowsPerCta : 0;
-    plan_kernel<<<1 + qctas, kPlanThreads, smem, stream>>>(seq_lens, num_reqs, budget, members,
-                                                            plan);
-    return cudaGetLastError();
+    // programmatic stream serialization: the launch overlaps the tail of the
+    // previous kernel, whose completion the kernel waits for on entry
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(1 + qctas));
+    cfg.blockDim = dim3(kPlanThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, num_reqs, budget, members, plan);
 }
 
 }  // namespace plmla
