@@ -30,7 +30,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "liboracle_plmla.so")
 _lib = None
 
-DC = 512          # latent width (BASELINE workload)
+DC = 512          # compressed latent width of the MLA cache rows
 DR = 64           # rope width
 PAGE_TOKENS = 1536  # tokens per MLA page (flat KV layout section)
 
