@@ -89,14 +89,30 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     const int gi = rw % group_rows;              // row inside the group's partials
     const int base = seg_stride != nullptr ? g * __ldcg(seg_stride) : 0;
     const int s0 = base + __ldcg(indptr + r), s1 = base + __ldcg(indptr + r + 1);
+    // the gate logits are an input of the step: read them before waiting
+    const uint2 *gp = reinterpret_cast<const uint2 *>(gate + row * kLatent);
+    uint2 graw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        graw[k] = gp[lane + 32 * k];
     // With counters: this request's partial states are complete once all its
     // segments of this team are published (other requests may still run).
     if (done != nullptr && !wait_segments(done + g * num_reqs + r, s1 - s0, status))
         return;
 
+    // The segments' log-sum-exps are read by the lanes in parallel, 32 at a
+    // time (one round trip instead of one per segment); the maximum and the
+    // weights follow with warp shuffles, and the weighted rows are read with
+    // several segments' loads in flight.  The order of every sum is fixed.
     float m = -INFINITY;
-    for (int s = s0; s < s1; ++s)
-        m = fmaxf(m, __ldcg(lse_part + (int64_t)s * group_rows + gi));
+    for (int b = s0; b < s1; b += 32) {
+        const int s = b + lane;
+        if (s < s1)
+            m = fmaxf(m, __ldcg(lse_part + (int64_t)s * group_rows + gi));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
 
     float4 acc[4];
 #pragma unroll
@@ -104,32 +120,41 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
         acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (m != -INFINITY) {
-        for (int s = s0; s < s1; ++s) {
-            const float l = __ldcg(lse_part + (int64_t)s * group_rows + gi);
-            if (l == -INFINITY)
-                continue;
-            const float w = expf(l - m);
-            wsum += w;
-            const float4 *src = reinterpret_cast<const float4 *>(
-                o_part + ((int64_t)s * group_rows + gi) * kLatent);
+        for (int b = s0; b < s1; b += 32) {
+            const int s = b + lane;
+            const float l = s < s1 ? __ldcg(lse_part + (int64_t)s * group_rows + gi) : -INFINITY;
+            const float wl = l == -INFINITY ? 0.f : expf(l - m);   // this lane's segment weight
+            wsum += wl;
+            const int n = min(32, s1 - b);
+            const float4 *src0 = reinterpret_cast<const float4 *>(
+                o_part + ((int64_t)b * group_rows + gi) * kLatent);
+            const int64_t seg_step = (int64_t)group_rows * kLatent / 4;   // float4 per segment
+#pragma unroll 4
+            for (int k = 0; k < n; ++k) {
+                const float w = __shfl_sync(0xffffffffu, wl, k);
+                if (w == 0.f)
+                    continue;                    // warp-uniform: an empty segment
+                const float4 *src = src0 + k * seg_step;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float4 v = __ldcg(src + lane + 32 * k);
-                acc[k].x = fmaf(w, v.x, acc[k].x);
-                acc[k].y = fmaf(w, v.y, acc[k].y);
-                acc[k].z = fmaf(w, v.z, acc[k].z);
-                acc[k].w = fmaf(w, v.w, acc[k].w);
+                for (int j = 0; j < 4; ++j) {
+                    const float4 v = __ldcg(src + lane + 32 * j);
+                    acc[j].x = fmaf(w, v.x, acc[j].x);
+                    acc[j].y = fmaf(w, v.y, acc[j].y);
+                    acc[j].z = fmaf(w, v.z, acc[j].z);
+                    acc[j].w = fmaf(w, v.w, acc[j].w);
+                }
             }
         }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    const uint2 *gp = reinterpret_cast<const uint2 *>(gate + row * kLatent);
     uint2 *dst = reinterpret_cast<uint2 *>(out + row * kLatent);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        const uint2 graw = gp[lane + 32 * k];
-        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw.x));
-        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw.y));
+        const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw[k].x));
+        const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw[k].y));
         const float o0 = acc[k].x * inv / (1.f + expf(-g01.x));
         const float o1 = acc[k].y * inv / (1.f + expf(-g01.y));
         const float o2 = acc[k].z * inv / (1.f + expf(-g23.x));
