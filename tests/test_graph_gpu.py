@@ -60,3 +60,46 @@ def test_captured_step_follows_new_lengths_and_queries(n_q, H):
         rows = sample_rows(w2, heads_per_token=4, seed=trial)
         ref_out, ref_lse = oracle_decode(w2, nq, nr, ng, slab, rows=rows)
         assert_parity(out, lse, ref_out, ref_lse, rows=rows, what=f"graph replay {trial}")
+
+
+def test_captured_fp8_step_follows_new_queries():
+    """The E4M3 step (its plan grid also quantises the queries) replays the same way."""
+    from helpers import assert_parity_fp8, oracle_decode_fp8
+    kvs = inputs.KV_SCALE_E4M3
+    w = inputs.custom_workload([12000, 3000, 25000], 1, 64, seed=77, spare_pages=3)
+    qn, qr, gate = inputs.make_queries(w, "cpu")
+    slab = inputs.make_slab_e4m3(w, "cpu", poison_nan=False, kv_scale=kvs)
+    d = to_device(w, qn, qr, gate, slab)
+    ws = api.allocate_workspace(w.num_reqs, 1, 64, 0, 1, "cuda", fp8=True)
+    out = torch.empty_like(d["qn"])
+    lse = torch.empty(d["qn"].shape[0], 64, dtype=torch.float32, device="cuda")
+
+    def step():
+        api.mla_decode_fp8(d["qn"], d["qr"], d["gate"], d["slab"], d["table"], d["lens"],
+                           kv_scale=kvs, n_q=1, scale=SCALE, out=out, lse=lse, workspace=ws)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    rng = np.random.Generator(np.random.PCG64(9))
+    for trial in range(2):
+        new_lens = np.array([rng.integers(1, L + 1) for L in w.seq_lens], dtype=np.int32)
+        g = torch.Generator().manual_seed(200 + trial)
+        nq = torch.randn(qn.shape, generator=g).bfloat16()
+        nr = torch.randn(qr.shape, generator=g).bfloat16()
+        ng = torch.randn(gate.shape, generator=g).bfloat16()
+        d["qn"].copy_(nq)
+        d["qr"].copy_(nr)
+        d["gate"].copy_(ng)
+        d["lens"].copy_(torch.as_tensor(new_lens))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert api.device_status(ws) == 0, "a decode pipeline wait timed out"
+        w2 = copy.copy(w)
+        w2.seq_lens = new_lens
+        rows = sample_rows(w2, heads_per_token=4, seed=trial)
+        ref_out, ref_lse, bound = oracle_decode_fp8(w2, nq, nr, ng, slab, kvs, rows=rows)
+        assert_parity_fp8(out, lse, ref_out, ref_lse, bound, rows=rows, what=f"fp8 replay {trial}")
