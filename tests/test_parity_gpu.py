@@ -145,6 +145,23 @@ def test_split_and_unsplit_agree():
         assert_parity(out, lse, ref_out, ref_lse, what=f"budget={budget} min={min_splits}")
 
 
+@pytest.mark.parametrize("min_splits", [1, 4])
+def test_largest_batch_of_1024_requests(min_splits):
+    """The planner's request limit: 1,024 requests (four per planner thread), short
+    ragged histories including empty ones, 4,096 chunks when each request must
+    get 4 (the planner's chunk limit)."""
+    rng = np.random.Generator(np.random.PCG64(12))
+    lengths = rng.integers(0, 1500, size=1024)       # one page each: a 1.8 GB pool
+    lengths[::97] = 0
+    lengths[5] = 1
+    w, qn, qr, gate, slab = _problem(lengths.tolist(), 1, 16, seed=12, spare=4)
+    d = to_device(w, qn, qr, gate, slab)
+    out, lse = gpu_decode(w, d, min_splits=min_splits)
+    rows = np.concatenate([np.arange(0, 1024 * 16, 7), [1024 * 16 - 1]])
+    ref_out, ref_lse = oracle_decode(w, qn, qr, gate, slab, rows=rows)
+    assert_parity(out, lse, ref_out, ref_lse, rows=rows, what=f"1024 requests min={min_splits}")
+
+
 def test_causal_drafts_match_single_token_runs():
     lengths = [3000, 130]
     w, qn, qr, gate, slab = _problem(lengths, 4, 16, seed=11)
