@@ -484,10 +484,13 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
             firstc = 0;
         } else if (m < members) {
             // a doubled midpoint v reaches member m's boundary when
-            // v >= 2 * total_cost * share(m): an integer threshold
+            // v >= 2 * total_cost * share(m): an integer threshold.  Single
+            // precision is enough: every step rounds monotonically, so the
+            // thresholds still rise with m and each chunk has one member (and
+            // this GPU's double-precision rate is a small fraction of fp32's).
             const long long thr =
-                weighted ? (long long)ceil(2.0 * total_cost * (double)sm.wprefix[m] /
-                                           (double)sm.wprefix[members])
+                weighted ? (long long)ceilf(2.f * (float)total_cost *
+                                            (sm.wprefix[m] / sm.wprefix[members]))
                          : (2LL * total_cost * m + members - 1) / members;
             auto reaches = [&](int v) -> bool { return (long long)v >= thr; };
             // the first request whose last chunk reaches it (lastm is a running
