@@ -328,6 +328,27 @@ plmla_status mla_split_combine(const float *o_part, const float *lse_part,
                                void *stream);
 
 /*
+ * mla_merge_partials -- the exchange step of decode context parallelism [AX,
+ * "AgentX benchmark results": ranks combine partial attention results]: each
+ * of `world` ranks decoded (with mla_decode) a disjoint part of every request's
+ * history -- its own pages -- and the gathered results are merged.  The gate is
+ * elementwise and the same for every part, so gated parts merge directly:
+ *
+ *   lse = ln sum_k exp(lse_parts[k]);  out = bf16_rn(sum_k exp(lse_parts[k] - lse) * out_parts[k])
+ *
+ * out_parts  bf16 [world, rows, 512], 16-byte aligned: rank k's gated output
+ *            (rows = num_reqs * n_q * num_heads, the order of mla_decode's out)
+ * lse_parts  fp32 [world, rows], natural log; -inf where rank k's part is empty
+ * world      1 .. 4096;  rows >= 0
+ * out        bf16 [rows, 512], written;  lse fp32 [rows], written (may be NULL);
+ *            a row that no rank saw gives 0 and -inf
+ * Ranks are merged in a fixed order, so the result does not depend on timing.
+ * The bf16 rounding of each part adds at most 2^-9 relative error per part.
+ */
+plmla_status mla_merge_partials(const void *out_parts, const float *lse_parts, int32_t world,
+                                int64_t rows, void *out, float *lse, void *stream);
+
+/*
  * mla_kv_append -- write each request's new latent and rope rows into the flat
  * page pool, the step before attention: under MLA a new token's rows are
  * appended after the request's history and no earlier row changes (vLLM blog

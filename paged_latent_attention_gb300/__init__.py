@@ -11,6 +11,7 @@ from .api import (  # noqa: F401
     mla_decode_fp8,
     mla_kv_append,
     mla_kv_append_fp8,
+    mla_merge_partials,
     mla_plan_splits,
     mla_quantize_queries_fp8,
     mla_split_budget,

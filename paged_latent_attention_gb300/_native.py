@@ -39,6 +39,7 @@ SIGNATURES = {
     "mla_kv_append_fp8": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _f, _p, _i64, _p, _i32, _i32,
                                          _p, _p]),
     "mla_quantize_queries_fp8": (ctypes.c_int, [_p, _p, _i64, _p, _p, _p]),
+    "mla_merge_partials": (ctypes.c_int, [_p, _p, _i32, _i64, _p, _p, _p]),
 }
 
 _lib = None

@@ -239,6 +239,33 @@ def mla_split_combine(o_part, lse_part, split_indptr, gate, *, n_q=1, out=None, 
     return out, lse
 
 
+def mla_merge_partials(out_parts, lse_parts, *, out=None, lse=None, stream=None, with_lse=True):
+    """Merge the gated outputs of ranks that each decoded a disjoint part of the
+    histories (decode context parallelism).  out_parts is bf16 [world, T, H, 512]
+    (rank k's mla_decode output), lse_parts fp32 [world, T, H]; returns the
+    merged (out [T, H, 512] bf16, lse [T, H] fp32)."""
+    _require(out_parts.is_cuda and out_parts.dtype == torch.bfloat16 and out_parts.is_contiguous()
+             and out_parts.dim() == 4 and out_parts.shape[-1] == LATENT,
+             "out_parts must be contiguous CUDA bf16 [world, T, H, 512]")
+    world, T, H, _ = out_parts.shape
+    _require(lse_parts.is_cuda and lse_parts.dtype == torch.float32 and lse_parts.is_contiguous()
+             and tuple(lse_parts.shape) == (world, T, H),
+             "lse_parts must be contiguous CUDA fp32 [world, T, H]")
+    if out is None:
+        out = torch.empty(T, H, LATENT, dtype=torch.bfloat16, device=out_parts.device)
+    _check_bf16(out, "out", (T, H, LATENT))
+    if lse is None and with_lse:
+        lse = torch.empty(T, H, dtype=torch.float32, device=out_parts.device)
+    if lse is not None:
+        _require(lse.is_cuda and lse.dtype == torch.float32 and lse.is_contiguous()
+                 and tuple(lse.shape) == (T, H), "lse must be a contiguous CUDA fp32 [T, H]")
+    status = _native.lib().mla_merge_partials(
+        out_parts.data_ptr(), lse_parts.data_ptr(), world, T * H, out.data_ptr(),
+        lse.data_ptr() if lse is not None else None, _stream_ptr(stream, out_parts.device))
+    _native.check(status, "mla_merge_partials")
+    return out, lse
+
+
 def mla_kv_append_fp8(latent_new, rope_new, slab, page_table, seq_lens, n_new, *, kv_scale,
                       status=None, stream=None):
     """mla_kv_append into E4M3 pages (slab uint8 or float8_e4m3fn [num_pages,

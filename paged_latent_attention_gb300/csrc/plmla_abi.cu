@@ -13,6 +13,13 @@
 
 using namespace plmla;
 
+namespace plmla {
+// plmla_combine.cu: merge of G ranks' gated partial outputs and LSEs.
+cudaError_t launch_merge_partials(const __nv_bfloat16 *parts, const float *lse_parts, int world,
+                                  int64_t rows, __nv_bfloat16 *out, float *lse,
+                                  cudaStream_t stream);
+}  // namespace plmla
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -214,6 +221,23 @@ extern "C" plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_req
     plan.chunk = split_chunk;
     cudaError_t err = launch_plan(seq_lens, num_reqs, split_budget, 1, plan,
                                   static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
+}
+
+extern "C" plmla_status mla_merge_partials(const void *out_parts, const float *lse_parts,
+                                           int32_t world, int64_t rows, void *out, float *lse,
+                                           void *stream)
+{
+    if (out_parts == nullptr || lse_parts == nullptr || out == nullptr || world < 1 ||
+        world > 4096 || rows < 0 || rows > (int64_t)kMaxReqs * kMaxNq * 128)
+        return PLMLA_INVALID_ARGUMENT;
+    if (!aligned(out_parts, 16) || !aligned(lse_parts, 4) || !aligned(out, 16) ||
+        (lse != nullptr && !aligned(lse, 4)))
+        return PLMLA_INVALID_ARGUMENT;
+    cudaError_t err = launch_merge_partials(static_cast<const __nv_bfloat16 *>(out_parts),
+                                            lse_parts, world, rows,
+                                            static_cast<__nv_bfloat16 *>(out), lse,
+                                            static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
 }
 

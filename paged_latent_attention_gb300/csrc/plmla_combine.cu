@@ -170,7 +170,89 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
         lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
+// Decode context parallelism: G ranks each decoded a disjoint part of every
+// request's history (its pages), giving a gated bf16 output and the LSE of
+// its part; merge them.  The gate is elementwise and the same for every part,
+// so the merged gated row is the LSE-weighted sum of the gated parts:
+//   lse = ln sum_k e^{lse_k},   out = sum_k e^{lse_k - lse} out_k
+// (AgentX post, "AgentX benchmark results": decode context parallelism, ranks
+// combine partial attention results; the merge rule is the split merge above).
+// One warp per row, ranks in a fixed order; a row no rank saw gives 0, -inf.
+__global__ void __launch_bounds__(kThreads)
+merge_partials_kernel(const __nv_bfloat16 *__restrict__ parts, const float *__restrict__ lse_parts,
+                      int world, int64_t rows, __nv_bfloat16 *__restrict__ out,
+                      float *__restrict__ lse)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    if (row >= rows)
+        return;
+    float m = -INFINITY;
+    for (int k0 = 0; k0 < world; k0 += 32) {
+        const int k = k0 + lane;
+        if (k < world)
+            m = fmaxf(m, __ldg(lse_parts + (int64_t)k * rows + row));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float acc[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        acc[i] = 0.f;
+    float wsum = 0.f;
+    if (m != -INFINITY) {
+        for (int k = 0; k < world; ++k) {
+            const float l = __ldg(lse_parts + (int64_t)k * rows + row);
+            if (l == -INFINITY)
+                continue;
+            const float w = expf(l - m);
+            wsum += w;
+            // lane owns columns [8 lane, 8 lane + 8) and [256 + 8 lane, 256 + 8 lane + 8)
+            const uint4 *src = reinterpret_cast<const uint4 *>(parts + ((int64_t)k * rows + row) * kLatent);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint4 v = __ldg(src + lane + 32 * h);
+                const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&wd[e]));
+                    acc[8 * h + 2 * e] = fmaf(w, f.x, acc[8 * h + 2 * e]);
+                    acc[8 * h + 2 * e + 1] = fmaf(w, f.y, acc[8 * h + 2 * e + 1]);
+                }
+            }
+        }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint4 *dst = reinterpret_cast<uint4 *>(out + row * kLatent);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        uint32_t wd[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const __nv_bfloat162 p =
+                __floats2bfloat162_rn(acc[8 * h + 2 * e] * inv, acc[8 * h + 2 * e + 1] * inv);
+            wd[e] = *reinterpret_cast<const uint32_t *>(&p);
+        }
+        dst[lane + 32 * h] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    }
+    if (lse != nullptr && lane == 0)
+        lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
+}
+
 }  // namespace
+
+cudaError_t launch_merge_partials(const __nv_bfloat16 *parts, const float *lse_parts, int world,
+                                  int64_t rows, __nv_bfloat16 *out, float *lse,
+                                  cudaStream_t stream)
+{
+    if (rows <= 0)
+        return cudaSuccess;
+    const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
+    merge_partials_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(parts, lse_parts, world, rows,
+                                                                   out, lse);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const float *o_part, const float *lse_part, const int32_t *indptr,
                            const int32_t *seg_stride, int group_rows,

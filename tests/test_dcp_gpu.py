@@ -1,0 +1,56 @@
+"""Decode context parallelism on one GPU: the ranks' parts run one after the
+other here (each is an ordinary mla_decode on its column view of the page table;
+no kernel waits on another), then mla_merge_partials merges them as the
+exchange step would.  The merged result must match the oracle on the whole
+history, and mla_decode on the whole history."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import SCALE, assert_parity, gpu_decode, oracle_decode, to_device
+from paged_latent_attention_gb300 import api, dcp, inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _parts(w, d, world):
+    outs, lses = [], []
+    for rank in range(world):
+        table_k, lens_k = dcp.shard_view(d["table"], d["lens"], rank, world)
+        out, lse = api.mla_decode(d["qn"], d["qr"], d["gate"], d["slab"], table_k, lens_k,
+                                  n_q=1, scale=SCALE)
+        outs.append(out)
+        lses.append(lse)
+    return torch.stack(outs).contiguous(), torch.stack(lses).contiguous()
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 5])
+def test_ranks_parts_merge_to_the_whole_history(world):
+    # histories of 0, 1, a few pages, and ones that end inside a rank's first page
+    lengths = [7000, 0, 1, 1536 * 3, 20000, 1537, 12345]
+    w = inputs.custom_workload(lengths, 1, 64, seed=80 + world, spare_pages=3)
+    qn, qr, gate = inputs.make_queries(w, "cpu")
+    slab = inputs.make_slab(w, "cpu", poison_nan=True)
+    d = to_device(w, qn, qr, gate, slab)
+    out_parts, lse_parts = _parts(w, d, world)
+    out, lse = api.mla_merge_partials(out_parts, lse_parts)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle_decode(w, qn, qr, gate, slab)
+    assert_parity(out, lse, ref_out, ref_lse, what=f"dcp world={world}")
+    whole_out, whole_lse = gpu_decode(w, d)
+    torch.testing.assert_close(out.float(), whole_out.float(), atol=2e-2, rtol=2e-2)
+    finite = torch.isfinite(whole_lse)
+    assert torch.equal(finite, torch.isfinite(lse))
+    torch.testing.assert_close(lse[finite], whole_lse[finite], atol=1e-3, rtol=0)
+
+
+def test_merge_of_one_part_is_that_part_and_no_part_is_empty():
+    T, H = 3, 16
+    g = torch.Generator(device="cuda").manual_seed(4)
+    part = torch.randn(1, T, H, 512, device="cuda", generator=g).bfloat16()
+    lse1 = torch.randn(1, T, H, device="cuda", generator=g)
+    out, lse = api.mla_merge_partials(part, lse1)
+    assert torch.equal(out, part[0]) and torch.equal(lse, lse1[0])
+    empty = torch.full((2, T, H), float("-inf"), device="cuda")
+    out, lse = api.mla_merge_partials(torch.stack([part[0], part[0]]).contiguous(), empty)
+    assert torch.equal(out, torch.zeros_like(out)) and bool(torch.isneginf(lse).all())
