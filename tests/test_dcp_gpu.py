@@ -54,3 +54,28 @@ def test_merge_of_one_part_is_that_part_and_no_part_is_empty():
     empty = torch.full((2, T, H), float("-inf"), device="cuda")
     out, lse = api.mla_merge_partials(torch.stack([part[0], part[0]]).contiguous(), empty)
     assert torch.equal(out, torch.zeros_like(out)) and bool(torch.isneginf(lse).all())
+
+
+def test_dcp_decode_through_a_one_rank_process_group():
+    """dcp_decode end to end (view, decode, all-gather, merge) in a one-rank NCCL
+    group: the collective path runs, and equals mla_decode on the whole history."""
+    import socket
+
+    import torch.distributed as dist
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    store = dist.TCPStore("127.0.0.1", port, 1, True)
+    dist.init_process_group("nccl", store=store, rank=0, world_size=1)
+    try:
+        w = inputs.custom_workload([9000, 2, 4000], 1, 16, seed=85, spare_pages=2)
+        qn, qr, gate = inputs.make_queries(w, "cpu")
+        slab = inputs.make_slab(w, "cpu", poison_nan=True)
+        d = to_device(w, qn, qr, gate, slab)
+        out, lse = dcp.dcp_decode(d["qn"], d["qr"], d["gate"], d["slab"], d["table"], d["lens"],
+                                  scale=SCALE)
+        torch.cuda.synchronize()
+        ref_out, ref_lse = oracle_decode(w, qn, qr, gate, slab)
+        assert_parity(out, lse, ref_out, ref_lse, what="dcp_decode one rank")
+    finally:
+        dist.destroy_process_group()
