@@ -97,6 +97,18 @@ size_t mla_workspace_size(int32_t num_reqs, int32_t n_q, int32_t num_heads, int3
                           int32_t min_splits_per_req);
 
 /*
+ * mla_set_page_checks -- process-wide switch (not part of the method) for a
+ * check of the page table after every mla_decode / mla_decode_fp8 step: one
+ * extra kernel reads each request's table entries 0 .. ceil(L / 1536) - 1 and
+ * sets the step's status word to 40 if any lies outside [0, num_pages), or to 41
+ * if a history needs more than page_table_ld columns.  Off by
+ * default; the environment variable PLMLA_CHECK_PAGES (any value but "0") turns
+ * it on when the library loads.  mla_get_page_checks returns the setting.
+ */
+void mla_set_page_checks(int32_t on);
+int32_t mla_get_page_checks(void);
+
+/*
  * mla_plan_splits -- per-request KV split plan [AX, Figure 4], on the device.
  *
  *   chunk     = ceil(sum_r L_r / split_budget) rounded up to a multiple of 128,
@@ -151,7 +163,8 @@ plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_reqs, int32_t 
  * workspace        device scratch of workspace_bytes >= mla_workspace_size(...),
  *                  256-byte aligned; contents on entry are irrelevant.  After the
  *                  step, its first 4 bytes hold the device status word (int32):
- *                  0 = ok; nonzero = a pipeline wait inside the decode kernel
+ *                  0 = ok; 40 = a used page ID out of range, 41 = a history
+ *                  longer than the table row (both with page checks on); another nonzero value = a pipeline wait inside the decode kernel
  *                  gave up after its time bound and the outputs are invalid
  *                  (the kernel never traps or spins forever)
  * cta_budget       concurrent CTA slots for the split budget (0 = SM count)
@@ -161,7 +174,12 @@ plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_reqs, int32_t 
  *
  * Enqueues: plan kernel (split plan + persistent schedule) -> split-decode
  * kernel (one persistent CTA per SM and row group) -> combine/gate kernel.
- * Page IDs are trusted: an ID outside [0, num_pages) is undefined behaviour.
+ * Page IDs are not checked on the hot path: an ID outside [0, num_pages) is a
+ * tensor-map coordinate out of range, which the TMA unit reads as zeros (no
+ * fault), so the affected rows come out wrong.  With page checks on (see
+ * mla_set_page_checks) a small kernel after the step checks every table entry
+ * a history uses and writes status 40 into the status word if one is out of
+ * range.
  */
 plmla_status mla_decode(const void *q_nope_absorbed, const void *q_rope, const void *gate,
                         const void *slab_base, int64_t num_pages, int64_t page_stride_elems,

@@ -7,6 +7,7 @@ from .api import (  # noqa: F401
     DEFAULT_SCALE,
     allocate_workspace,
     device_status,
+    get_page_checks,
     mla_decode,
     mla_decode_fp8,
     mla_kv_append,
@@ -18,4 +19,5 @@ from .api import (  # noqa: F401
     mla_split_combine,
     mla_workspace_size,
     mla_workspace_size_fp8,
+    set_page_checks,
 )

@@ -40,6 +40,8 @@ SIGNATURES = {
                                          _p, _p]),
     "mla_quantize_queries_fp8": (ctypes.c_int, [_p, _p, _i64, _p, _p, _p]),
     "mla_merge_partials": (ctypes.c_int, [_p, _p, _i32, _i64, _p, _p, _p]),
+    "mla_set_page_checks": (None, [_i32]),
+    "mla_get_page_checks": (_i32, []),
 }
 
 _lib = None

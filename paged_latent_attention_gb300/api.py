@@ -192,6 +192,16 @@ def mla_quantize_queries_fp8(q_nope_absorbed, q_rope, stream=None):
     return codes, exps
 
 
+def set_page_checks(on: bool) -> None:
+    """Process-wide: check every page-table entry a decode step uses after the
+    step (status 40 in the workspace's status word if one is out of range)."""
+    _native.lib().mla_set_page_checks(1 if on else 0)
+
+
+def get_page_checks() -> bool:
+    return bool(_native.lib().mla_get_page_checks())
+
+
 def device_status(workspace) -> int:
     """The decode kernel's status word from the workspace of the last step
     (0 = ok).  Reads device memory: synchronises with the workspace's stream."""

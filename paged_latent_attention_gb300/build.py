@@ -28,6 +28,7 @@ SOURCES = [
     "plmla_decode_tc.cu",
     "plmla_static_scratch.cu",
     "plmla_append.cu",
+    "plmla_check.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

@@ -5,6 +5,7 @@
 // allocates device memory, synchronises, or reads device data back.
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include <mutex>
 
@@ -14,6 +15,10 @@
 using namespace plmla;
 
 namespace plmla {
+// plmla_check.cu: the opt-in page-table check after a decode step.
+cudaError_t launch_check_pages(const int32_t *seq_lens, int num_reqs, const int32_t *page_table,
+                               int64_t table_ld, int64_t num_pages, int32_t *status,
+                               cudaStream_t stream);
 // plmla_combine.cu: merge of G ranks' gated partial outputs and LSEs.
 cudaError_t launch_merge_partials(const __nv_bfloat16 *parts, const float *lse_parts, int world,
                                   int64_t rows, __nv_bfloat16 *out, float *lse,
@@ -23,6 +28,15 @@ cudaError_t launch_merge_partials(const __nv_bfloat16 *parts, const float *lse_p
 namespace {
 
 constexpr size_t kAlign = 256;
+
+// Page-table checks after each decode step: off unless PLMLA_CHECK_PAGES is set
+// to something other than "0" in the environment, or mla_set_page_checks(1).
+int initial_page_checks()
+{
+    const char *v = getenv("PLMLA_CHECK_PAGES");
+    return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
+}
+int g_page_checks = initial_page_checks();
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -224,6 +238,10 @@ extern "C" plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_req
     return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
 }
 
+extern "C" void mla_set_page_checks(int32_t on) { g_page_checks = on != 0 ? 1 : 0; }
+
+extern "C" int32_t mla_get_page_checks(void) { return g_page_checks; }
+
 extern "C" plmla_status mla_merge_partials(const void *out_parts, const float *lse_parts,
                                            int32_t world, int64_t rows, void *out, float *lse,
                                            void *stream)
@@ -388,6 +406,9 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
                          num_heads, static_cast<__nv_bfloat16 *>(out), lse, plan.done,
                          plan.status, s);
     if (err != cudaSuccess || record(ev.combine_end, s) != cudaSuccess)
+        return PLMLA_CUDA_ERROR;
+    if (g_page_checks && launch_check_pages(seq_lens, num_reqs, page_table, page_table_ld,
+                                            num_pages, plan.status, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
     return PLMLA_OK;
 }
