@@ -54,17 +54,32 @@ def shard_view(page_table, seq_lens, rank: int, world: int, page_tokens: int = P
     return table_k, lens_k
 
 
+def decode_shard(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, rank, world, *,
+                 kv_scale=None, scale=api.DEFAULT_SCALE, workspace=None, stream=None):
+    """Rank `rank`'s gated part (out_k, lse_k): mla_decode (mla_decode_fp8 when
+    `kv_scale` is given and the slab holds E4M3 codes) on its column view."""
+    table_k, lens_k = shard_view(page_table, seq_lens, rank, world)
+    if kv_scale is None:
+        return api.mla_decode(q_nope_absorbed, q_rope, gate, slab, table_k, lens_k, n_q=1,
+                              scale=scale, workspace=workspace, stream=stream)
+    return api.mla_decode_fp8(q_nope_absorbed, q_rope, gate, slab, table_k, lens_k,
+                              kv_scale=kv_scale, n_q=1, scale=scale, workspace=workspace,
+                              stream=stream)
+
+
 def dcp_decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *, group=None,
-               scale=api.DEFAULT_SCALE, workspace=None, stream=None):
+               kv_scale=None, scale=api.DEFAULT_SCALE, workspace=None, stream=None):
     """mla_decode of single-token requests with every history split across the
-    ranks of `group` (torch.distributed); every rank returns the full (out, lse)."""
+    ranks of `group` (torch.distributed); every rank returns the full (out, lse).
+    With `kv_scale`, the slab holds E4M3 pages (the merge is the same: each part
+    is a gated output with its LSE, whatever the page format)."""
     import torch.distributed as dist
 
     world = dist.get_world_size(group)
     rank = dist.get_rank(group)
-    table_k, lens_k = shard_view(page_table, seq_lens, rank, world)
-    out_k, lse_k = api.mla_decode(q_nope_absorbed, q_rope, gate, slab, table_k, lens_k, n_q=1,
-                                  scale=scale, workspace=workspace, stream=stream)
+    out_k, lse_k = decode_shard(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, rank,
+                                world, kv_scale=kv_scale, scale=scale, workspace=workspace,
+                                stream=stream)
     out_parts = torch.empty((world,) + tuple(out_k.shape), dtype=out_k.dtype, device=out_k.device)
     lse_parts = torch.empty((world,) + tuple(lse_k.shape), dtype=lse_k.dtype, device=lse_k.device)
     dist.all_gather_into_tensor(out_parts, out_k, group=group)

@@ -44,6 +44,31 @@ def test_ranks_parts_merge_to_the_whole_history(world):
     torch.testing.assert_close(lse[finite], whole_lse[finite], atol=1e-3, rtol=0)
 
 
+@pytest.mark.parametrize("world", [2, 3])
+def test_fp8_pages_parts_merge_to_the_whole_history(world):
+    """E4M3 pages: each rank's part carries the E4M3 probability rounding of its
+    own tokens; weighted by exp(lse_k - lse), those errors add up to the same
+    bound as one decode over the whole history."""
+    from helpers import assert_parity_fp8, oracle_decode_fp8
+    kvs = inputs.KV_SCALE_E4M3
+    lengths = [9000, 1, 1536 * 2, 16000, 0]
+    w = inputs.custom_workload(lengths, 1, 64, seed=90 + world, spare_pages=3)
+    qn, qr, gate = inputs.make_queries(w, "cpu")
+    slab = inputs.make_slab_e4m3(w, "cpu", poison_nan=True, kv_scale=kvs)
+    d = to_device(w, qn, qr, gate, slab)
+    outs, lses = [], []
+    for rank in range(world):
+        o, l = dcp.decode_shard(d["qn"], d["qr"], d["gate"], d["slab"], d["table"], d["lens"],
+                                rank, world, kv_scale=kvs, scale=SCALE)
+        outs.append(o)
+        lses.append(l)
+    out, lse = api.mla_merge_partials(torch.stack(outs).contiguous(),
+                                      torch.stack(lses).contiguous())
+    torch.cuda.synchronize()
+    ref_out, ref_lse, bound = oracle_decode_fp8(w, qn, qr, gate, slab, kvs)
+    assert_parity_fp8(out, lse, ref_out, ref_lse, bound, what=f"fp8 dcp world={world}")
+
+
 def test_merge_of_one_part_is_that_part_and_no_part_is_empty():
     T, H = 3, 16
     g = torch.Generator(device="cuda").manual_seed(4)
