@@ -254,6 +254,15 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// Prefetch one box of a tiled tensor into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_policy_evict_last()
 {
     uint64_t p;
@@ -781,6 +790,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     const int t = seg.y + i * kTile;
                     const int page = trow[t / kPageTokens];
                     const int tok = t % kPageTokens;
+                    if constexpr (!F8) {
+                        // Entering a page: warm the address translations of the next page
+                        // this CTA reads (the segment's next page, else the next segment's
+                        // first) with one-row L2 prefetches of its first row and of the first
+                        // row past a 2 MiB boundary inside it, a page's worth of tiles before
+                        // the ring reaches it.  Measured: ~2% off the steady step.
+                        if (i == 0 || tok == 0) {
+                            const int tn = (t / kPageTokens + 1) * kPageTokens;
+                            int np = -1, nt0 = 0;
+                            if (tn < seg.z) {
+                                np = trow[tn / kPageTokens];
+                            } else if (s + 1 < seg_end) {
+                                const int4 nx = a.segments[s + 1];
+                                np = a.page_table[(int64_t)nx.x * a.table_ld + nx.y / kPageTokens];
+                                nt0 = nx.y % kPageTokens;
+                            }
+                            if (np >= 0) {
+                                tma_prefetch_3d(&tail.m[0], 0, nt0, np);
+                                const uint64_t pa = reinterpret_cast<uint64_t>(a.slab) +
+                                                    (uint64_t)np * (uint64_t)a.page_stride * 2u;
+                                const uint64_t nb = ((pa >> 21) + 1) << 21;
+                                const uint64_t rb = (uint64_t)kRow * 2u;
+                                const int tb = (int)((nb - pa + rb - 1) / rb);
+                                if (tb > nt0 && tb < kPageTokens)
+                                    tma_prefetch_3d(&tail.m[0], 0, tb, np);
+                            }
+                        }
+                    }
                     for (int k = 0; k < F::sub; ++k) {
                         if (!wait_bounded(bar_empty_k + 8 * slot, phase ^ 1, abort_flag, a.status,
                                           2)) {
