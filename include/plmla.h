@@ -102,8 +102,8 @@ size_t mla_workspace_size(int32_t num_reqs, int32_t n_q, int32_t num_heads, int3
  * extra kernel reads each request's table entries 0 .. ceil(L / 1536) - 1 and
  * sets the step's status word to 40 if any lies outside [0, num_pages), or to 41
  * if a history needs more than page_table_ld columns.  Off by
- * default; the environment variable PLMLA_CHECK_PAGES (any value but "0") turns
- * it on when the library loads.  mla_get_page_checks returns the setting.
+ * default; the environment variable PLMLA_CHECK_PAGES or PLMLA_DEBUG (any value
+ * but "0") turns it on when the library loads.  mla_get_page_checks returns the setting.
  */
 void mla_set_page_checks(int32_t on);
 int32_t mla_get_page_checks(void);

@@ -29,13 +29,15 @@ namespace {
 
 constexpr size_t kAlign = 256;
 
-// Page-table checks after each decode step: off unless PLMLA_CHECK_PAGES is set
-// to something other than "0" in the environment, or mla_set_page_checks(1).
-int initial_page_checks()
+// Page-table checks after each decode step: off unless PLMLA_CHECK_PAGES (or the
+// general debug switch PLMLA_DEBUG) is set to something other than "0" in the
+// environment, or mla_set_page_checks(1).
+bool env_on(const char *name)
 {
-    const char *v = getenv("PLMLA_CHECK_PAGES");
+    const char *v = getenv(name);
     return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
 }
+int initial_page_checks() { return env_on("PLMLA_CHECK_PAGES") || env_on("PLMLA_DEBUG"); }
 int g_page_checks = initial_page_checks();
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }

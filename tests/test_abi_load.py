@@ -118,3 +118,22 @@ def test_query_token_limit_and_fp8_arguments(lib):
                                  fake, 1, 1, None, None) == 1
     assert lib.mla_quantize_queries_fp8(fake + 4, fake, 4, fake, fake, None) == 1
     assert lib.mla_quantize_queries_fp8(None, None, 0, None, None, None) == 0
+
+
+@pytest.mark.parametrize("env,expect", [({}, 0), ({"PLMLA_CHECK_PAGES": "1"}, 1),
+                                        ({"PLMLA_DEBUG": "1"}, 1), ({"PLMLA_CHECK_PAGES": "0"}, 0),
+                                        ({"PLMLA_DEBUG": ""}, 0)])
+def test_page_check_switch_reads_the_environment_at_load(lib, env, expect):
+    """Host logic only: the switch's initial value comes from the environment of
+    the process that loads the library, and the setter overrides it."""
+    import os
+    import subprocess
+    import sys
+    clean = {k: v for k, v in os.environ.items() if k not in ("PLMLA_CHECK_PAGES", "PLMLA_DEBUG")}
+    code = ("from paged_latent_attention_gb300 import _native; l = _native.lib(); "
+            "a = l.mla_get_page_checks(); l.mla_set_page_checks(1 - a); "
+            "print(a, l.mla_get_page_checks())")
+    out = subprocess.run([sys.executable, "-c", code], env={**clean, **env}, capture_output=True,
+                         text=True, timeout=120, cwd=os.path.dirname(os.path.dirname(__file__)))
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == [str(expect), str(1 - expect)]
