@@ -7,6 +7,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "plmla.h"
@@ -38,7 +39,7 @@ bool env_on(const char *name)
     return v != nullptr && v[0] != '\0' && !(v[0] == '0' && v[1] == '\0');
 }
 int initial_page_checks() { return env_on("PLMLA_CHECK_PAGES") || env_on("PLMLA_DEBUG"); }
-int g_page_checks = initial_page_checks();
+std::atomic<int> g_page_checks{initial_page_checks()};   // set and read from any host thread
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -240,9 +241,15 @@ extern "C" plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_req
     return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
 }
 
-extern "C" void mla_set_page_checks(int32_t on) { g_page_checks = on != 0 ? 1 : 0; }
+extern "C" void mla_set_page_checks(int32_t on)
+{
+    g_page_checks.store(on != 0 ? 1 : 0, std::memory_order_relaxed);
+}
 
-extern "C" int32_t mla_get_page_checks(void) { return g_page_checks; }
+extern "C" int32_t mla_get_page_checks(void)
+{
+    return g_page_checks.load(std::memory_order_relaxed);
+}
 
 extern "C" plmla_status mla_merge_partials(const void *out_parts, const float *lse_parts,
                                            int32_t world, int64_t rows, void *out, float *lse,
@@ -409,7 +416,8 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
                          plan.status, s);
     if (err != cudaSuccess || record(ev.combine_end, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
-    if (g_page_checks && launch_check_pages(seq_lens, num_reqs, page_table, page_table_ld,
+    if (g_page_checks.load(std::memory_order_relaxed) != 0 &&
+        launch_check_pages(seq_lens, num_reqs, page_table, page_table_ld,
                                             num_pages, plan.status, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
     return PLMLA_OK;
