@@ -1,4 +1,4 @@
-"""Host logic of decode context parallelism (CPU, gloo, world size 2).
+"""Host logic of decode context parallelism (CPU, gloo, world sizes 2 and 3).
 
 Each rank takes its token range of every request from the same page-table
 column split the GPU path uses, computes its gated partial state with the
@@ -61,10 +61,12 @@ def _worker(rank, world, port, results):
     dist.destroy_process_group()
 
 
-def test_two_ranks_gather_and_merge_to_the_whole_history():
+@pytest.mark.parametrize("world", [2, 3])
+def test_two_ranks_gather_and_merge_to_the_whole_history(world):
+    """world 3: four table columns split 2 + 2 + 0, so the last rank holds no
+    token of any request and contributes empty parts (lse = -inf, weight 0)."""
     sys.path.insert(0, ROOT)
     import oracle
-    world = 2
     port = _free_port()
     with mp.Manager() as mgr:
         results = mgr.dict()
