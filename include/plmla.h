@@ -77,12 +77,13 @@ const char *mla_strerror(plmla_status status);
  *   members    = max(1, floor(slots / row_groups))   (persistent CTAs per group)
  *   budget     = max(26 * members, num_reqs * min_splits_per_req), at most 4096
  *
- * mla_decode runs row_groups x members persistent CTAs; each takes a contiguous,
- * cost-balanced run of the chunks (equal shares until the library has measured
- * the speed of each SM over a few calls with real work, then shares in
- * proportion to it, fixed from then on).  Returns the budget, or -1 for invalid
- * arguments, members above 256, num_reqs * min_splits_per_req above 4096, or no
- * CUDA device when cta_budget == 0.
+ * mla_decode runs row_groups x members persistent CTAs; each takes a contiguous
+ * run of the chunks holding an equal share of their cost (128-token tiles plus a
+ * charge for starting a request).  The schedule depends only on seq_lens and
+ * this shape, so repeated calls on the same inputs give the same bits, in any
+ * process.  Returns the budget, or -1 for invalid arguments, members above 256,
+ * num_reqs * min_splits_per_req above 4096, or no CUDA device when
+ * cta_budget == 0.
  */
 int32_t mla_split_budget(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_budget,
                          int32_t min_splits_per_req);
@@ -212,11 +213,16 @@ plmla_status mla_decode(const void *q_nope_absorbed, const void *q_rope, const v
  *
  * The first call on each device, made with that device current, looks up the
  * array's device address once (cudaGetSymbolAddress) and caches it; make that
- * first call before any stream capture.  All calls on a device share the one
- * array, which keeps the previous call's contents (nothing in it needs to start
- * at zero).  Calls whose executions overlap on the GPU -- on different streams,
- * or from several host threads -- race on the array and corrupt each other's
- * results: serialise them, e.g. on one stream.
+ * first call before any stream capture.  The cached address is only valid for
+ * the CUDA context that was current then: do not keep using the library after
+ * cudaDeviceReset or after the primary context was destroyed and re-created.
+ * All calls on a device share the one array, which keeps the previous call's
+ * contents (nothing in it needs to start at zero: each call's plan kernel
+ * rewrites every entry the later kernels read).  Calls whose executions overlap
+ * on the GPU -- on different streams, or from several host threads -- race on
+ * the array and corrupt each other's results: serialise them, e.g. on one
+ * stream.  The step's device status word (see mla_decode's `workspace`) lives
+ * in the array; mla_static_scratch_status reads it.
  */
 plmla_status mla_decode_static_scratch(const void *q_nope_absorbed, const void *q_rope,
                                        const void *gate, const void *slab_base,
@@ -226,6 +232,20 @@ plmla_status mla_decode_static_scratch(const void *q_nope_absorbed, const void *
                                        int32_t n_q_per_req, int32_t num_heads, float scale,
                                        void *out, float *lse, int32_t cta_budget,
                                        int32_t min_splits_per_req, void *stream);
+
+/*
+ * mla_static_scratch_status -- enqueue, on `stream`, a copy of the device status
+ * word of the last mla_decode_static_scratch step on the current device into
+ * `status_out` (4 bytes; device memory or pinned host memory, or pageable host
+ * memory, for which the copy completes before the call returns).  Values as for
+ * mla_decode's workspace status word: 0 = ok, 40 / 41 = page check failures,
+ * another nonzero value = a bounded pipeline wait gave up and the outputs are
+ * invalid.  Allocates nothing.  Like the decode entry point, the first call on a
+ * device looks up the array's address; call it after the step on the same
+ * stream.  Returns PLMLA_INVALID_ARGUMENT for a null or misaligned
+ * status_out, PLMLA_CUDA_ERROR if the copy cannot be enqueued.
+ */
+plmla_status mla_static_scratch_status(int32_t *status_out, void *stream);
 
 /*
  * Optional stage events for mla_decode_ex: each non-NULL member is a cudaEvent_t

@@ -19,5 +19,4 @@ from .oracle import (  # noqa: F401
     plan_splits,
     quantize_query_rows,
     query_scale_exponent,
-    split_budget,
 )

@@ -271,23 +271,6 @@ def plan_splits(seq_lens, budget: int, tile: int):
     return chunk, [_ceil_div(L, chunk) if L > 0 else 0 for L in lens]
 
 
-def split_budget(num_reqs: int, row_groups: int, cta_slots: int, min_splits: int,
-                 chunks_per_member: int = 26, limit: int = 4096) -> int:
-    """Chunk budget derived from the machine: 26 chunks for every persistent CTA
-    of a row group (the finer the chunks, the closer each CTA's share of the
-    work comes to its target), or enough for ``min_splits`` chunks per request
-    if that is more, capped at ``limit``.  A hard-coded budget left most of a
-    large GPU idle at batch 1 (AgentX - InferenceXv3 report, context-parallel
-    section on in-GPU parallelism limits).  Raises ValueError when the
-    per-request minimum alone is above ``limit``."""
-    members = max(1, cta_slots // row_groups)
-    wanted = num_reqs * max(1, min_splits)
-    if wanted > limit:
-        raise ValueError("budget above the planner's limit")
-    budget = min(max(chunks_per_member * members, wanted), limit)
-    return budget
-
-
 # --------------------------------------------------------------------------
 # KV append (vLLM blog "Kimi K3 Inference Backend Evolution", section "State
 # Overwrite: How KDA Breaks Traditional KV Cache", the append-only contract of

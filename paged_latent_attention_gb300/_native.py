@@ -30,6 +30,7 @@ SIGNATURES = {
     "mla_split_combine": (ctypes.c_int, [_p, _p, _p, _p, _i32, _i32, _i32, _p, _p, _p]),
     "mla_decode_static_scratch": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _p, _i64, _p, _i32,
                                                  _i32, _i32, _f, _p, _p, _i32, _i32, _p]),
+    "mla_static_scratch_status": (ctypes.c_int, [_p, _p]),
     "mla_kv_append": (ctypes.c_int, [_p, _p, _p, _i64, _i64, _p, _i64, _p, _i32, _i32, _p, _p]),
     "mla_workspace_size_fp8": (_sz, [_i32, _i32, _i32, _i32, _i32]),
     "mla_decode_fp8": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _f, _p, _i64, _p, _i32, _i32,

@@ -8,7 +8,6 @@
 #include <stdlib.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "plmla.h"
 #include "plmla_internal.cuh"
@@ -67,38 +66,9 @@ bool shape_ok(int32_t num_reqs, int32_t n_q, int32_t num_heads)
            num_heads >= 16 && num_heads <= 128 && num_heads % 16 == 0;
 }
 
-// The per-device SM speed records (zero-initialised when the module loads), one
-// per cache format: a tile of E4M3 pages takes about half the time of a bf16 one.
-__device__ SmCalib g_sm_calib;
-__device__ SmCalib g_sm_calib_fp8;
-
-constexpr int kMaxDevices = 64;
-std::mutex g_calib_mutex;
-SmCalib *g_calib_ptr[2][kMaxDevices] = {{nullptr}};
-
-// Device address of the speed record on the current device, looked up once;
-// null if the lookup fails (the planner then gives every CTA an equal share).
-SmCalib *calib_for_current_device(bool fp8)
-{
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-        return nullptr;
-    std::lock_guard<std::mutex> lock(g_calib_mutex);
-    SmCalib *&slot = g_calib_ptr[fp8 ? 1 : 0][dev];
-    if (slot == nullptr) {
-        void *ptr = nullptr;
-        const cudaError_t err = fp8 ? cudaGetSymbolAddress(&ptr, g_sm_calib_fp8)
-                                    : cudaGetSymbolAddress(&ptr, g_sm_calib);
-        if (err != cudaSuccess)
-            return nullptr;
-        slot = static_cast<SmCalib *>(ptr);
-    }
-    return slot;
-}
-
 struct WorkspaceLayout {
-    size_t status, calib_stage, indptr, chunk, seg_count, segments, seg_req, seg_member, done, claim,
-        o_part, lse_part, q8, qexp, total;
+    size_t status, indptr, chunk, seg_count, segments, seg_req, seg_member, done, o_part,
+        lse_part, q8, qexp, total;
     int32_t max_segments;
 };
 
@@ -149,8 +119,6 @@ WorkspaceLayout layout_for(int32_t num_reqs, const Shape &sh, bool fp8)
     size_t off = 0;
     w.status = off;
     off = align_up(off + sizeof(int32_t));
-    w.calib_stage = off;
-    off = align_up(off + sizeof(int32_t));
     w.indptr = off;
     off = align_up(off + sizeof(int32_t) * (size_t)(num_reqs + 1));
     w.chunk = off;
@@ -165,8 +133,6 @@ WorkspaceLayout layout_for(int32_t num_reqs, const Shape &sh, bool fp8)
     off = align_up(off + sizeof(int32_t) * (size_t)(sh.members + 1));
     w.done = off;
     off = align_up(off + sizeof(int32_t) * (size_t)sh.groups * num_reqs);
-    w.claim = off;
-    off = align_up(off + sizeof(int32_t) * (size_t)sh.groups * sh.members);
     const size_t part_rows = (size_t)sh.groups * w.max_segments * sh.group_rows;
     w.o_part = off;
     off = align_up(off + sizeof(float) * part_rows * kLatent);
@@ -355,10 +321,6 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     plan.seg_member_indptr = reinterpret_cast<int32_t *>(ws + w.seg_member);
     plan.done = reinterpret_cast<int32_t *>(ws + w.done);
     plan.n_done = sh.groups * num_reqs;
-    plan.claim = reinterpret_cast<int32_t *>(ws + w.claim);
-    plan.n_claim = sh.groups * sh.members;
-    plan.calib = calib_for_current_device(fmt.fp8);
-    plan.calib_stage = reinterpret_cast<int32_t *>(ws + w.calib_stage);
     plan.q_nope = static_cast<const __nv_bfloat16 *>(q_nope_absorbed);
     plan.q_rope = static_cast<const __nv_bfloat16 *>(q_rope);
     plan.q8 = fmt.fp8 ? reinterpret_cast<uint8_t *>(ws + w.q8) : nullptr;
@@ -399,9 +361,6 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     a.lse_part = lse_part;
     a.status = plan.status;
     a.done = plan.done;
-    a.claim = plan.claim;
-    a.calib = plan.calib;
-    a.calib_stage = plan.calib_stage;
     a.fp8 = fmt.fp8 ? 1 : 0;
     a.kv_scale = fmt.kv_scale;
     a.q8 = plan.q8;

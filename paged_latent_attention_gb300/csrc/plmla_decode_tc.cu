@@ -127,7 +127,7 @@ struct Smem {
     static constexpr int m_off = fin_off + 64 * 4;           // float m[64]   (log2 units)
     static constexpr int al_off = m_off + 64 * 4;            // float alpha[64]
     static constexpr int cf_off = al_off + 64 * 4;           // float cf[64]  (E4M3 score factors)
-    static constexpr int misc_off = cf_off + 64 * 4;         // tmem addr, abort, need[2], cta
+    static constexpr int misc_off = cf_off + 64 * 4;         // tmem addr, abort, need[2]
     static constexpr int bytes = misc_off + 32;
     static constexpr int alloc = bytes + 1024;               // slack for 1024-B alignment
     static_assert(k_slots >= 2 && v_slots >= 2, "ring depth");
@@ -663,8 +663,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
     volatile int *need_sm = reinterpret_cast<volatile int *>(smem + L::misc_off + 16);   // [2]
 
-    volatile int *cta_index = reinterpret_cast<volatile int *>(smem + L::misc_off + 12);
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_kv)) : "memory");
@@ -722,24 +720,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     // everything above overlaps the plan kernel (programmatic dependent launch);
     // the schedule is read only once that grid has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // Take the CTA index equal to this SM's id when it is free, so that the
-    // planner's speed-scaled share for that SM is the one this CTA runs; else
-    // the first free index (each of the grid's CTAs ends up with a distinct one).
-    uint32_t sm_id;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_id));
-    const unsigned long long t_start = global_ns();
-    if (threadIdx.x == 0) {
-        const int total = a.members * a.num_groups;
-        int c = -1;
-        if ((int)sm_id < total && atomicCAS(a.claim + sm_id, 0, 1) == 0)
-            c = (int)sm_id;
-        for (int k = 0; c < 0 && k < total; ++k)
-            if (atomicCAS(a.claim + k, 0, 1) == 0)
-                c = k;
-        *cta_index = c;
-    }
-    __syncthreads();
-    const int cta = *cta_index;
+    const int cta = (int)blockIdx.x;
     const int team = cta / a.members;
     const int member = cta % a.members;
     const int row0 = team * NG;
@@ -1317,24 +1298,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols));
-    }
-    if (threadIdx.x == 0 && a.calib != nullptr && a.calib_stage != nullptr &&
-        (int)sm_id < kMaxSms && *abort_flag == 0) {
-        // this SM's speed in the planner's cost units, from calls with real work,
-        // into the record stage the planner named for this call
-        const int st = *a.calib_stage;
-        if (st >= 0 && st < kCalibStages && a.calib->cost[st][sm_id] < kCalibCost) {
-            float cost = 0.f;
-            for (int s = seg_begin; s < seg_end; ++s) {
-                const int4 seg = a.segments[s];
-                cost += (float)((seg.z - seg.y + kTile - 1) / kTile +
-                                (seg.y == 0 ? kSegmentCostTiles : 0));
-            }
-            if (cost >= kCalibMinCost) {
-                atomicAdd(&a.calib->time_ns[st][sm_id], (float)(global_ns() - t_start));
-                atomicAdd(&a.calib->cost[st][sm_id], cost);
-            }
-        }
     }
 }
 

@@ -24,30 +24,7 @@ constexpr int kChunksPerMember = 26;  // default chunk budget per persistent CTA
 // partial-state epilogue).
 constexpr int kSegmentCostTiles = 2;
 
-constexpr int kMaxSms = 256;            // SM ids the speed record covers
-constexpr float kCalibCost = 192.f;     // cost units an SM measures before its speed is used
-constexpr float kCalibMinCost = 16.f;   // a call adds to the record only with this much work
-
-// Per-device record of how fast each SM works through the decode: cost units
-// (tiles plus a charge per request start, the planner's unit) and active time,
-// summed over calls in which the SM's CTA had at least kCalibMinCost of work,
-// until kCalibCost units are measured.  SMs of one chip run the same code at
-// repeatably different speeds (some TPCs sit closer to their GPC's crossbar
-// port, some GPCs have fewer TPCs), so the planner gives each CTA a share of
-// the work proportional to its SM's measured speed.  The record has stages:
-// stage 0 is measured under equal shares, stage k under the shares computed from
-// stage k - 1.  Equal shares let the fast SMs idle at the end, and the slow ones
-// then run alone and faster, so one stage under-corrects; a later stage
-// measures every SM busy for the whole kernel.  Once every stage is complete the
-// shares stay fixed (results are then bit-stable from call to call).
-constexpr int kCalibStages = 3;
-struct SmCalib {
-    float cost[kCalibStages][kMaxSms];
-    float time_ns[kCalibStages][kMaxSms];
-    // the planner's member weight prefix for one grid shape and stage
-    int32_t cache_members, cache_teams, cache_stage;
-    float cache_wprefix[kMaxSms + 1];
-};
+constexpr int kMaxSms = 256;            // persistent CTAs per row group the schedule covers
 
 struct PlanBuffers {
     int32_t *status;            // [1] device status word, reset to 0 by the plan kernel
@@ -60,10 +37,6 @@ struct PlanBuffers {
     int32_t *seg_member_indptr; // [members + 1] segments of member k: [k], [k + 1]
     int32_t *done;              // [n_done] finished-segment counters, zeroed by the plan kernel
     int32_t n_done;
-    int32_t *claim;             // [n_claim] CTA-index claims of the decode grid, zeroed here
-    int32_t n_claim;
-    SmCalib *calib;             // per-device speed record (null: equal shares)
-    int32_t *calib_stage;       // [1] written: the record stage this call's decode fills (-1: none)
     // FP8 decode: extra CTAs of the plan grid quantise the queries (null: none)
     const __nv_bfloat16 *q_nope; // [q_rows, 512]
     const __nv_bfloat16 *q_rope; // [q_rows, 64]
@@ -94,9 +67,6 @@ struct DecodeArgs {
     float *lse_part;               // [groups * S, group_rows], natural log
     int32_t *status;               // device status word (0 = ok, else the failed wait)
     int32_t *done;                 // [groups * R] segments of (team, request) written
-    int32_t *claim;                // [groups * members] CTA indices taken (zeroed by the plan)
-    SmCalib *calib;                // per-device speed record, or null
-    const int32_t *calib_stage;    // stage of the record to add this call's timing to (-1: none)
     // FP8 pages: slab holds E4M3 bytes (value = kv_scale * byte), the queries are
     // read as E4M3 codes q8 with per-row exponents qexp (written by the plan grid)
     int32_t fp8;

@@ -12,9 +12,10 @@
 // The chunks, in request order, are dealt out as contiguous runs so that every
 // CTA ("member") gets its share of the cost up to half a chunk, cost counted in
 // 128-token tiles plus a fixed charge for each request's first chunk (starting
-// a segment): a chunk goes to the member whose share holds the chunk's cost
-// midpoint (cost before it + half its cost).  Shares are equal until the decode
-// has measured each SM's speed (SmCalib), then proportional to it.  The chunks
+// a segment): a chunk goes to the member whose equal share holds the chunk's
+// cost midpoint (cost before it + half its cost).  The schedule depends only on
+// the histories and the grid shape, never on timing, so a step's outputs are
+// the same bits on every call and in every process.  The chunks
 // of one request all have the same length (the last may be shorter), so the
 // cost before any chunk has a closed form from a per-request prefix, and each
 // member's chunk range comes from a binary search over requests, without a
@@ -45,13 +46,10 @@ struct PlanSmem {
     int nonempty[kMaxReqs + 1];  // exclusive prefix of requests with at least one chunk
     int first[kMaxSms + 1];      // first chunk of each member (members + 1 entries)
     int nseg[kMaxSms + 1];       // exclusive prefix of segments per member
-    float wprefix[kMaxSms + 1];  // inclusive prefix of member weights
-    float wrate[kMaxSms];        // measured rate of each CTA index
     long long red64[kPlanWarps];
     int red32[kPlanWarps];
     int cand_k[kPlanWarps];
     int cand_fits[kPlanWarps];
-    int weighted;
 };
 
 // Block-wide sum / max of one value per thread; every thread gets the result.
@@ -258,33 +256,10 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
         local_sum += L[k];
         local_max = max(local_max, L[k]);
     }
-    // cached member weights for this grid shape (loaded early, used later)
-    const SmCalib *cal = plan.segments != nullptr ? plan.calib : nullptr;
-    const int n_cta = plan.n_claim;
-    const int teams = n_cta / max(members, 1);
-    int cache_hit = 0;
-    float cached_w = 0.f;
-    bool rec_done[kCalibStages];                // this thread's SM finished each record stage
-#pragma unroll
-    for (int k = 0; k < kCalibStages; ++k)
-        rec_done[k] = true;
-    if (cal != nullptr) {
-        cache_hit = cal->cache_members == members && cal->cache_teams == teams;
-        if (tid <= kMaxSms)
-            cached_w = cal->cache_wprefix[tid];
-        if (tid < n_cta && n_cta <= kMaxSms) {
-#pragma unroll
-            for (int k = 0; k < kCalibStages; ++k)
-                rec_done[k] = cal->cost[k][tid] >= kCalibCost && cal->time_ns[k][tid] > 0.f;
-        }
-    }
-    // finished-segment counters and CTA claims of this call's decode start from zero
+    // finished-segment counters of this call's decode start from zero
     if (plan.done != nullptr)
         for (int i = tid; i < plan.n_done; i += kPlanThreads)
             plan.done[i] = 0;
-    if (plan.claim != nullptr)
-        for (int i = tid; i < plan.n_claim; i += kPlanThreads)
-            plan.claim[i] = 0;
     const long long total = block_sum64(local_sum, sm.red64);   // also publishes sm.lens
     const int longest_len = block_max32(local_max, sm.red32);
 
@@ -394,104 +369,17 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
         return;
     }
 
-    // ---- member shares: CTA c of the decode grid runs on the SM with id c when
-    // it can (it claims that index).  `stage` = the number of record stages that
-    // every such SM has completed; with stage >= 1, member m of every team gets a
-    // share of the cost proportional to the mean speed of SMs team*members + m
-    // in record stage - 1, otherwise the shares are equal.  This call's decode
-    // adds its timing to record `stage` (if any is left).
-    const bool usable = cal != nullptr && teams >= 1 && n_cta <= kMaxSms;
-    int stage = 0;
-#pragma unroll
-    for (int k = 0; k < kCalibStages; ++k)
-        if (__syncthreads_and(usable && rec_done[k]) && stage == k)
-            stage = k + 1;
-    if (tid == 0 && plan.calib_stage != nullptr)
-        *plan.calib_stage = usable && stage < kCalibStages ? stage : -1;
-    cache_hit = cache_hit && stage >= 1 && cal->cache_stage == stage;
-    if (cache_hit) {
-        if (tid <= members)
-            sm.wprefix[tid] = cached_w;
-        if (tid == 0)
-            sm.weighted = 1;
-        __syncthreads();
-    } else {
-        if (usable && stage >= 1 && tid < n_cta) {
-            const float c = cal->cost[stage - 1][tid], t = cal->time_ns[stage - 1][tid];
-            sm.wrate[tid] = c / t;
-        }
-        const int ready = __syncthreads_or(stage >= 1);
-        if (ready && tid < 32) {
-            // member rate (mean over teams), then an inclusive prefix in warp 0:
-            // lane l owns members [8l, 8l + 8)
-            constexpr int per = kMaxSms / 32;
-            float loc[per];
-            float run = 0.f;
-#pragma unroll
-            for (int i = 0; i < per; ++i) {
-                const int m = tid * per + i;
-                float r = 0.f;
-                if (m < members) {
-                    for (int g = 0; g < teams; ++g)
-                        r += sm.wrate[g * members + m];
-                    r /= teams;
-                }
-                run += r;
-                loc[i] = run;
-            }
-            float incl = run;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float up = __shfl_up_sync(0xffffffffu, incl, o);
-                if (tid >= o)
-                    incl += up;
-            }
-            const float off = incl - run;
-#pragma unroll
-            for (int i = 0; i < per; ++i) {
-                const int m = tid * per + i;
-                if (m < members)
-                    sm.wprefix[m + 1] = off + loc[i];
-            }
-            if (tid == 0)
-                sm.wprefix[0] = 0.f;
-        }
-        if (tid == 0)
-            sm.weighted = ready ? 1 : 0;
-        __syncthreads();
-        if (ready) {
-            // the record stage this prefix comes from is complete: keep it for
-            // later calls of this grid shape until the next stage completes
-            SmCalib *wcal = plan.calib;
-            if (tid <= members)
-                wcal->cache_wprefix[tid] = sm.wprefix[tid];
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) {
-                wcal->cache_teams = teams;
-                wcal->cache_members = members;
-                wcal->cache_stage = stage;
-            }
-        }
-    }
-
     // ---- first chunk of every member: the first chunk whose doubled cost
     // midpoint reaches the member's doubled share boundary
-    const bool weighted = sm.weighted != 0;
     for (int m = tid; m <= members; m += kPlanThreads) {
         int firstc = n_splits;
         if (m == 0) {
             firstc = 0;
         } else if (m < members) {
             // a doubled midpoint v reaches member m's boundary when
-            // v >= 2 * total_cost * share(m): an integer threshold.  Single
-            // precision is enough: every step rounds monotonically, so the
-            // thresholds still rise with m and each chunk has one member (and
-            // this GPU's double-precision rate is a small fraction of fp32's).
-            const long long thr =
-                weighted ? (long long)ceilf(2.f * (float)total_cost *
-                                            (sm.wprefix[m] / sm.wprefix[members]))
-                         : (2LL * total_cost * m + members - 1) / members;
+            // v >= 2 * total_cost * m / members: an integer threshold that rises
+            // with m, so each chunk has exactly one member
+            const long long thr = (2LL * total_cost * m + members - 1) / members;
             auto reaches = [&](int v) -> bool { return (long long)v >= thr; };
             // the first request whose last chunk reaches it (lastm is a running
             // maximum, so this request has chunks)

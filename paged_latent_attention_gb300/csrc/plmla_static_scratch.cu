@@ -14,7 +14,12 @@
 // array's name as a device address (on the host it names a stand-in object),
 // so the first call on each device looks the real address up with
 // cudaGetSymbolAddress while that device is current, checks the result, and
-// caches it; later calls reuse the cached pointer.
+// caches it; later calls reuse the cached pointer.  The cache is keyed by device
+// ordinal only, so it does not survive a device reset (documented in the header).
+// The step's status word is the array's first 4 bytes (mla_decode's workspace
+// layout); mla_static_scratch_status copies it out without allocating.
+#include <stdint.h>
+
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -75,4 +80,19 @@ extern "C" plmla_status mla_decode_static_scratch(
                       page_table, page_table_ld, seq_lens, num_reqs, n_q_per_req, num_heads,
                       scale, out, lse, scratch, kScratchBytes, cta_budget, min_splits_per_req,
                       stream);
+}
+
+extern "C" plmla_status mla_static_scratch_status(int32_t *status_out, void *stream)
+{
+    if (status_out == nullptr || (reinterpret_cast<uintptr_t>(status_out) % 4) != 0)
+        return PLMLA_INVALID_ARGUMENT;
+    void *scratch = nullptr;
+    const plmla_status st = scratch_for_current_device(&scratch);
+    if (st != PLMLA_OK)
+        return st;
+    // the status word sits at offset 0 of mla_decode's workspace
+    const cudaError_t err = cudaMemcpyAsync(status_out, scratch, sizeof(int32_t),
+                                            cudaMemcpyDefault,
+                                            static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
 }

@@ -212,6 +212,43 @@ def make_slab(w: Workload, device="cpu", layer: int = 0, poison_nan: bool = Fals
     return slab
 
 
+HOST_PAGE_BANK = 16
+
+
+def make_host_pages(w: Workload, req_ids, layer: int = 0, fp8: bool = False,
+                    kv_scale: float = None):
+    """Host pages for the listed requests, for timing the oracle on a sample of
+    a workload whose pool is too large to draw on the host in reasonable time.
+    HOST_PAGE_BANK pages of N(0, 1) values are drawn from numpy's PCG64 keyed by
+    (seed, layer) and rounded to bf16 (or, with ``fp8``, cast to E4M3 as
+    make_slab_e4m3 does); each sampled page is a copy of a bank page chosen at
+    random.  The values follow the workload's recipe but are not the device
+    pool's values: use this only where the result is not compared.
+
+    Returns (slab [n_pages, page_stride] bf16 or uint8, table [len(req_ids), ld]
+    int32 indexing it, seq_lens int32 [len(req_ids)])."""
+    import torch
+    rng = np.random.Generator(np.random.PCG64([int(w.seed), int(layer), 17]))
+    per = [-(-int(w.seq_lens[r]) // w.page_tokens) for r in req_ids]
+    n = max(1, sum(per))
+    bank = torch.from_numpy(rng.standard_normal((HOST_PAGE_BANK, w.page_stride),
+                                                dtype=np.float32))
+    if fp8:
+        scale = KV_SCALE_E4M3 if kv_scale is None else kv_scale
+        bank = bank.div_(scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    else:
+        bank = bank.to(torch.bfloat16)
+    pick = torch.from_numpy(rng.integers(0, HOST_PAGE_BANK, size=n))
+    slab = bank.index_select(0, pick)
+    table = np.zeros((len(req_ids), max(1, max(per) if per else 1)), dtype=np.int32)
+    pos = 0
+    for i, k in enumerate(per):
+        table[i, :k] = np.arange(pos, pos + k)
+        pos += k
+    lens = np.asarray([int(w.seq_lens[r]) for r in req_ids], dtype=np.int32)
+    return slab, table, lens
+
+
 # Scale of the synthetic FP8 cache: N(0, 1) values reach E4M3's largest finite
 # value (448) at 6 standard deviations.
 KV_SCALE_E4M3 = 6.0 / 448.0

@@ -29,17 +29,45 @@ def test_status_names(lib):
     assert _native.strerror(99) == "PLMLA_UNKNOWN_STATUS"
 
 
-@pytest.mark.parametrize("R,n_q,H,slots,min_splits", [
-    (64, 1, 64, 152, 1), (32, 1, 64, 152, 1), (128, 4, 64, 152, 1), (4, 1, 64, 152, 128),
-    (2, 1, 16, 152, 1), (1, 1, 128, 152, 1), (1000, 2, 48, 148, 3), (7, 3, 16, 16, 2)])
-def test_split_budget_matches_oracle_rule(lib, R, n_q, H, slots, min_splits):
+def _stated_budget(R, n_q, H, slots, min_splits):
+    """The library's budget rule as include/plmla.h states it (library tuning
+    policy, not part of the method: the pages fix how a budget turns into
+    chunks, not the budget itself)."""
     rows = n_q * H
     group = 64 if rows % 64 == 0 else 32 if rows % 32 == 0 else 16
-    try:
-        expect = oracle.split_budget(R, rows // group, slots, min_splits)
-    except ValueError:
-        expect = -1
-    assert lib.mla_split_budget(R, n_q, H, slots, min_splits) == expect
+    members = max(1, slots // (rows // group))
+    wanted = R * min_splits
+    if members > 256 or wanted > 4096:
+        return -1
+    return min(max(26 * members, wanted), 4096)
+
+
+@pytest.mark.parametrize("R,n_q,H,slots,min_splits", [
+    (64, 1, 64, 152, 1), (32, 1, 64, 152, 1), (128, 4, 64, 152, 1), (4, 1, 64, 152, 128),
+    (2, 1, 16, 152, 1), (1, 1, 128, 152, 1), (1000, 2, 48, 148, 3), (7, 3, 16, 16, 2),
+    (30, 1, 16, 16, 20), (1, 1, 64, 256, 1), (1024, 1, 64, 152, 8)])
+def test_split_budget_follows_the_stated_rule(lib, R, n_q, H, slots, min_splits):
+    assert lib.mla_split_budget(R, n_q, H, slots, min_splits) == _stated_budget(
+        R, n_q, H, slots, min_splits)
+
+
+def test_split_budget_examples(lib):
+    # one row group: 26 chunks per persistent CTA on 152 SMs
+    assert lib.mla_split_budget(64, 1, 64, 152, 1) == 26 * 152
+    # four row groups share the SMs in teams of 38
+    assert lib.mla_split_budget(128, 4, 64, 152, 1) == 26 * 38
+    # >= 128 chunks for each of 4 million-token requests fits the default budget,
+    # and the oracle's planner (pinned by Figure 4) then gives each >= 128 chunks
+    b = lib.mla_split_budget(4, 1, 64, 152, 128)
+    assert b == 26 * 152
+    chunk, splits = oracle.plan_splits([1_000_000] * 4, b, 128)
+    assert min(splits) >= 128 and sum(splits) <= b
+    # a per-request minimum above the default raises the budget; a larger
+    # machine gets a larger one, up to the planner's limit
+    assert lib.mla_split_budget(30, 1, 16, 16, 20) == 600
+    assert lib.mla_split_budget(1, 1, 64, 152, 1) > lib.mla_split_budget(1, 1, 64, 16, 1)
+    assert lib.mla_split_budget(1, 1, 64, 256, 1) == 4096
+    assert lib.mla_split_budget(1024, 1, 64, 152, 8) == -1
 
 
 def test_workspace_grows_with_the_machine(lib):

@@ -87,22 +87,3 @@ def test_empty_requests_get_no_split():
     assert oracle.plan_splits([0, 0], 8, 128) == (128, [0, 0])
     chunk, splits = oracle.plan_splits([0, 1000, 0], 8, 128)
     assert splits[0] == 0 and splits[2] == 0 and splits[1] >= 1
-
-
-def test_split_budget_follows_the_machine():
-    # 26 chunks per persistent CTA: 152 CTAs for one row group
-    assert oracle.split_budget(64, 1, 152, 1) == 26 * 152
-    # four row groups split the CTAs into teams of 38
-    assert oracle.split_budget(128, 4, 152, 1) == 26 * 38
-    # >= 128 chunks for each of 4 requests fits in the default budget
-    b = oracle.split_budget(4, 1, 152, 128)
-    assert b == 26 * 152 and b >= 4 * 128
-    chunk, splits = oracle.plan_splits([1_000_000] * 4, b, 128)
-    assert min(splits) >= 128 and sum(splits) <= b
-    # a per-request minimum above the default raises the budget
-    assert oracle.split_budget(30, 1, 16, 20) == 600
-    # a larger machine gets a larger budget, up to the planner's limit
-    assert oracle.split_budget(1, 1, 152, 1) > oracle.split_budget(1, 1, 16, 1)
-    assert oracle.split_budget(1, 1, 256, 1) == 4096
-    with pytest.raises(ValueError):
-        oracle.split_budget(1024, 1, 152, 8)
