@@ -48,7 +48,8 @@ def _load():
     dbl, c_int = ctypes.c_double, ctypes.c_int
     lib.oracle_attend_rows.restype = c_int
     lib.oracle_attend_rows.argtypes = [p, p, p, c_int, dbl, i64, i64, i64, i64, p, i64, p, i64,
-                                       i64, i64, i64, i64, dbl, p, i64, i64, i64, p, p, p, c_int]
+                                       i64, i64, i64, i64, dbl, p, i64, i64, i64, p, p, p, p, p,
+                                       p, p, c_int]
     _lib = lib
     return lib
 
@@ -128,12 +129,17 @@ def _bf16_to_f64(a) -> np.ndarray:
 def attend_rows(q_nope, q_rope, slab, page_table, seq_lens, n_q, num_heads, scale, *,
                 num_pages, page_stride=None, page_tokens=PAGE_TOKENS, dc=DC, dr=DR,
                 rows=None, t_lo=0, t_hi=None, threads=None, kv_format="bf16", kv_scale=1.0,
-                with_abs=False):
+                with_abs=False, query_err=None):
     """Ungated softmax attention over the paged latent history.
 
-    Returns (o, lse), or (o, lse, o_abs) with ``with_abs``: o is [n_rows, dc]
+    Returns (o, lse), or (o, lse, extra) with ``with_abs``: o is [n_rows, dc]
     float64, lse is [n_rows] float64 (natural log; -inf where the row sees no
-    token), o_abs the probability-weighted absolute latent sum_t w_t |c_t|.
+    token); extra is a dict of sensitivity terms: "o_abs" = sum_t w_t |c_t|
+    (the probability-weighted absolute latent, [n_rows, dc]), "abs_sum" =
+    sum_t |c_t| ([n_rows, dc]), "w_max" = the largest weight ([n_rows]) and,
+    given ``query_err`` ([R*n_q*H, dc + dr] bounds on the error of each query
+    element), "d_max" = max_t |scale| sum_d query_err[d] |x_t[d]|, the largest
+    bound on a score's error ([n_rows]).
     ``rows`` lists flat row ids (r*n_q + j)*H + h; None means every row in that
     order.  ``[t_lo, t_hi)`` restricts the tokens (a KV chunk); the causal limit
     of draft token j is seq_lens[r] - (n_q - 1 - j).  The queries are bf16 (or
@@ -168,22 +174,32 @@ def attend_rows(q_nope, q_rope, slab, page_table, seq_lens, n_q, num_heads, scal
         rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
         n_rows = rows_arr.shape[0]
     o = np.zeros((n_rows, dc), dtype=np.float64)
-    o_abs = np.zeros((n_rows, dc), dtype=np.float64) if with_abs else None
     lse = np.zeros((n_rows,), dtype=np.float64)
+    extra = None
+    eps = None
+    if with_abs:
+        extra = {"o_abs": np.zeros((n_rows, dc)), "abs_sum": np.zeros((n_rows, dc)),
+                 "w_max": np.zeros((n_rows,)), "d_max": np.zeros((n_rows,))}
+        if query_err is not None:
+            eps = np.ascontiguousarray(np.asarray(query_err, dtype=np.float64)
+                                       .reshape(R * n_q * num_heads, row_elems))
     if t_hi is None:
         t_hi = np.iinfo(np.int64).max
+
+    def ptr(a):
+        return a.ctypes.data if a is not None else None
     rc = lib.oracle_attend_rows(
         qn.ctypes.data, qr.ctypes.data, sl.ctypes.data, fp8, float(kv_scale), num_pages,
         page_stride, page_tokens, row_elems, pt.ctypes.data, table_ld, lens.ctypes.data, R, n_q,
-        num_heads, dc, dr, float(scale), rows_arr.ctypes.data if rows_arr is not None else None,
-        n_rows, int(t_lo), int(t_hi), o.ctypes.data,
-        o_abs.ctypes.data if o_abs is not None else None, lse.ctypes.data,
-        int(threads or default_threads()))
+        num_heads, dc, dr, float(scale), ptr(rows_arr), n_rows, int(t_lo), int(t_hi),
+        o.ctypes.data, ptr(extra["o_abs"]) if extra else None, lse.ctypes.data, ptr(eps),
+        ptr(extra["abs_sum"]) if extra else None, ptr(extra["w_max"]) if extra else None,
+        ptr(extra["d_max"]) if extra else None, int(threads or default_threads()))
     if rc == -1:
         raise IndexError("page table entry outside the pool")
     if rc != 0:
         raise MemoryError("oracle allocation failed")
-    return (o, lse, o_abs) if with_abs else (o, lse)
+    return (o, lse, extra) if with_abs else (o, lse)
 
 
 def gate_sigmoid(o, gate_logits):
@@ -323,9 +339,11 @@ def kv_append(slab, page_table, seq_lens, latent_new, rope_new, n_new, *,
 # the AgentX - InferenceXv3 report name the encoding (float8_e4m3fn, as opposed
 # to gfx942's e4m3fnuz).  The pages give no scale granularity; the reading here
 # is one float scale per cache tensor: element value = kv_scale * decoded byte.
-# The FP8 tensor-core path multiplies FP8 by FP8, so the decode also quantises
-# each query row to E4M3 with a power-of-two scale; that step is part of what
-# the FP8 decode computes and the oracle takes it exactly.
+# The pages say nothing about the query: the definition keeps it bf16, so the
+# reference below is attention of the bf16 query over the dequantised cache.
+# quantize_query_rows restates the library's own query split (a documented
+# library function with no counterpart on the pages) only to check that
+# function bit for bit.
 # --------------------------------------------------------------------------
 
 E4M3_MAX = 448.0
@@ -383,47 +401,55 @@ def query_scale_exponent(amax) -> np.ndarray:
 
 
 def quantize_query_rows(q_nope, q_rope):
-    """FP8 queries: rows of [q_nope | q_rope] (dc + dr values) as E4M3 codes of
-    q * 2^-e, with e = query_scale_exponent(max |q| over the row).  Returns
-    (codes [rows, dc + dr] uint8, exps [rows] int32)."""
+    """The library's two-part FP8 query (checker of mla_quantize_queries_fp8):
+    each row of [q_nope | q_rope] (dc + dr values) is scaled by 2^-e, e =
+    query_scale_exponent(max |q| over the row); hi = E4M3 code of v = q * 2^-e,
+    lo = E4M3 code of v - decode(hi) (both round to nearest even).  Returns
+    (hi [rows, dc + dr] uint8, lo [rows, dc + dr] uint8, exps [rows] int32)."""
     qn, qr = _as_f64(q_nope), _as_f64(q_rope)
     qn = qn.reshape(-1, qn.shape[-1])
     qr = qr.reshape(-1, qr.shape[-1])
     q = np.concatenate([qn, qr], axis=1)
     e = query_scale_exponent(np.max(np.abs(q), axis=1))
-    codes = e4m3_encode(np.ldexp(q, -e[:, None].astype(np.int64)))
-    return codes, e
+    v = np.ldexp(q, -e[:, None].astype(np.int64))
+    hi = e4m3_encode(v)
+    lo = e4m3_encode(v - e4m3_decode(hi))
+    return hi, lo, e
 
 
-def dequantize_query_rows(codes, exps) -> np.ndarray:
-    """float64 values of FP8 query rows: decoded byte * 2^e (exact)."""
-    return np.ldexp(e4m3_decode(codes), np.asarray(exps, dtype=np.int64)[:, None])
+def dequantize_query_rows(hi, lo, exps) -> np.ndarray:
+    """float64 values of two-part FP8 query rows: (decode(hi) + decode(lo)) * 2^e."""
+    return np.ldexp(e4m3_decode(hi) + e4m3_decode(lo),
+                    np.asarray(exps, dtype=np.int64)[:, None])
 
 
 def mla_decode_e4m3_reference(q_nope, q_rope, gate, slab8, kv_scale, page_table, seq_lens, n_q,
                               num_heads, scale, *, num_pages, page_stride=None,
                               page_tokens=PAGE_TOKENS, dc=DC, dr=DR, rows=None, threads=None,
-                              with_abs=False):
-    """Gated MLA decode over E4M3 pages with FP8 queries.
+                              with_abs=False, query_err=None):
+    """Gated MLA decode over E4M3 pages: the bf16 query, exactly, attending over
+    the dequantised cache (kv_scale * decoded byte), then the sigmoid gate.
 
-    Every query row is quantised as quantize_query_rows does; the scores, the
-    softmax and the latent sum then follow the bf16 definition on the
-    dequantised values (kv_scale * decoded byte for the cache).  Returns (out,
-    lse), or (out, lse, bound) with ``with_abs``, bound = sigmoid(g) * sum_t w_t
-    |c_t|, the gated probability-weighted absolute latent."""
-    codes, exps = quantize_query_rows(q_nope, q_rope)
-    qd = dequantize_query_rows(codes, exps)
-    res = attend_rows(qd[:, :dc], qd[:, dc:], slab8, page_table, seq_lens, n_q, num_heads, scale,
+    Returns (out, lse), or with ``with_abs`` (out, lse, terms) where terms holds
+    the gated sensitivity terms "A" = sigmoid(g) * sum_t w_t |c_t|, "B" =
+    sigmoid(g) * w_max * sum_t |c_t| and "D" (per row, the bound on a score's
+    error for the per-element query errors ``query_err``, 0 without it); see
+    attend_rows."""
+    res = attend_rows(q_nope, q_rope, slab8, page_table, seq_lens, n_q, num_heads, scale,
                       num_pages=num_pages, page_stride=page_stride, page_tokens=page_tokens,
                       dc=dc, dr=dr, rows=rows, threads=threads, kv_format="e4m3",
-                      kv_scale=kv_scale, with_abs=with_abs)
+                      kv_scale=kv_scale, with_abs=with_abs, query_err=query_err)
     g = _bf16_to_f64(gate).reshape(-1, dc)
     if rows is not None:
         g = g[np.asarray(rows, dtype=np.int64)]
     out = gate_sigmoid(res[0], g)
-    if with_abs:
-        return out, res[1], gate_sigmoid(res[2], g)
-    return out, res[1]
+    if not with_abs:
+        return out, res[1]
+    x = res[2]
+    terms = {"A": gate_sigmoid(x["o_abs"], g),
+             "B": gate_sigmoid(x["w_max"][:, None] * x["abs_sum"], g),
+             "D": x["d_max"]}
+    return out, res[1], terms
 
 
 def kv_append_e4m3(slab8, page_table, seq_lens, latent_new, rope_new, n_new, kv_scale, *,

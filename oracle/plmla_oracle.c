@@ -43,8 +43,14 @@
  * every slab element is one OCP E4M3 byte (1 sign bit, 4 exponent bits with
  * bias 7, 3 mantissa bits; exponent 0 is subnormal, S.1111.111 is NaN, there is
  * no infinity) and the stored value is kv_scale times the decoded number.
- * The query is passed in double, so the caller decides what it is (for the FP8
- * decode: the dequantised FP8 query).
+ * The query is passed in double and used as given: the definition takes the
+ * bf16 query exactly, whatever the cache format.
+ *
+ * Sensitivity outputs (optional, for error bounds derived by the caller): the
+ * largest softmax weight w_max = 1 / Z, the unweighted absolute latent sum
+ * sum_t |c_t[d]|, and, given a per-element bound eps[d] on the error of a query
+ * element, the largest bound on a score's error over the row's tokens,
+ * D = max_t |scale| * sum_d eps[d] * |x_t[d]| (latent and rope elements).
  */
 #include <math.h>
 #include <stdint.h>
@@ -85,13 +91,16 @@ static double kv_elem(const void *slab, int64_t idx, int kv_fp8, double kv_scale
 
 /* Attention for one output row.  Returns 0 on success, -1 if a page index read
  * from the page table lies outside [0, num_pages).  o_abs (may be NULL)
- * receives sum_t w_t |c_t[d]|, the probability-weighted absolute latent. */
+ * receives sum_t w_t |c_t[d]|, the probability-weighted absolute latent; the
+ * sensitivity outputs abs_sum, w_max and d_max (each may be NULL; d_max needs
+ * eps) are described in the file header. */
 static int attend_one_row(const double *qn, const double *qr, const void *slab, int kv_fp8,
                           double kv_scale, int64_t num_pages, int64_t page_stride,
                           int64_t page_tokens, int64_t row_elems, const int32_t *table_row,
                           int64_t L_eff, int64_t t_lo, int64_t t_hi, int64_t dc, int64_t dr,
                           double scale, double *o_out, double *o_abs, double *lse_out,
-                          double *scores)
+                          double *scores, const double *eps, double *abs_sum, double *w_max,
+                          double *d_max)
 {
     int64_t lo = t_lo < 0 ? 0 : t_lo;
     int64_t hi = t_hi < L_eff ? t_hi : L_eff;
@@ -99,13 +108,20 @@ static int attend_one_row(const double *qn, const double *qr, const void *slab, 
         o_out[d] = 0.0;
         if (o_abs)
             o_abs[d] = 0.0;
+        if (abs_sum)
+            abs_sum[d] = 0.0;
     }
+    if (w_max)
+        *w_max = 0.0;
+    if (d_max)
+        *d_max = 0.0;
     if (hi <= lo) {
         *lse_out = -INFINITY;
         return 0;
     }
     /* pass 1: scores and their maximum */
     double m = -INFINITY;
+    double dm = 0.0;
     for (int64_t t = lo; t < hi; ++t) {
         int64_t page = table_row[t / page_tokens];
         if (page < 0 || page >= num_pages)
@@ -120,6 +136,15 @@ static int attend_one_row(const double *qn, const double *qr, const void *slab, 
         scores[t - lo] = s;
         if (s > m)
             m = s;
+        if (eps && d_max) {
+            double delta = 0.0;
+            for (int64_t d = 0; d < dc + dr; ++d)
+                if (eps[d] != 0.0)
+                    delta += eps[d] * fabs(kv_elem(slab, x + d, kv_fp8, kv_scale));
+            delta *= fabs(scale);
+            if (delta > dm)
+                dm = delta;
+        }
     }
     /* pass 2: normaliser and the probability-weighted latent sum */
     double Z = 0.0;
@@ -134,9 +159,15 @@ static int attend_one_row(const double *qn, const double *qr, const void *slab, 
             o_out[d] += p * c;
             if (o_abs)
                 o_abs[d] += p * fabs(c);
+            if (abs_sum)
+                abs_sum[d] += fabs(c);
         }
     }
     *lse_out = m + log(Z);
+    if (w_max)
+        *w_max = 1.0 / Z;   /* the weight of a token at the maximum score */
+    if (d_max)
+        *d_max = dm;
     return 0;
 }
 
@@ -155,6 +186,9 @@ static int attend_one_row(const double *qn, const double *qr, const void *slab, 
  * t_lo, t_hi  token window applied to every row (partial-state evaluation)
  * o        [n_rows, dc] double, lse [n_rows] double (outputs); o_abs [n_rows, dc]
  *          (NULL allowed) the probability-weighted absolute latent
+ * eps      [R*n_q*H, dc + dr] per-element query error bounds, or NULL
+ * abs_sum  [n_rows, dc], w_max [n_rows], d_max [n_rows]: sensitivity outputs
+ *          (each NULL allowed; d_max is written only with eps)
  *
  * Returns 0, or -1 if a page ID is out of range, or -2 on allocation failure.
  */
@@ -164,7 +198,8 @@ int oracle_attend_rows(const double *q_nope, const double *q_rope, const void *s
                        int64_t table_ld, const int32_t *seq_lens, int64_t R, int64_t n_q,
                        int64_t H, int64_t dc, int64_t dr, double scale, const int64_t *rows,
                        int64_t n_rows, int64_t t_lo, int64_t t_hi, double *o, double *o_abs,
-                       double *lse, int num_threads)
+                       double *lse, const double *eps, double *abs_sum, double *w_max,
+                       double *d_max, int num_threads)
 {
     int64_t total_rows = R * n_q * H;
     if (rows == NULL)
@@ -192,7 +227,10 @@ int oracle_attend_rows(const double *q_nope, const double *q_rope, const void *s
             int rc = attend_one_row(q_nope + row * dc, q_rope + row * dr, slab, kv_fp8, kv_scale,
                                     num_pages, page_stride, page_tokens, row_elems,
                                     page_table + r * table_ld, L_eff, t_lo, t_hi, dc, dr, scale,
-                                    o + i * dc, o_abs ? o_abs + i * dc : NULL, lse + i, scores);
+                                    o + i * dc, o_abs ? o_abs + i * dc : NULL, lse + i, scores,
+                                    eps ? eps + row * (dc + dr) : NULL,
+                                    abs_sum ? abs_sum + i * dc : NULL, w_max ? w_max + i : NULL,
+                                    (eps && d_max) ? d_max + i : NULL);
             if (rc != 0) {
 #pragma omp atomic write
                 status = rc;

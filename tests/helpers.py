@@ -76,14 +76,48 @@ def sample_rows(w, heads_per_token=4, seed=0):
 # --------------------------------------------------------------------------
 # FP8 (E4M3) pages
 # --------------------------------------------------------------------------
-
-# The FP8 decode rounds each probability to E4M3 before the value MMA (3
-# mantissa bits: relative error <= 2^-4), while the normaliser and the LSE use
-# the fp32 probabilities.  So |out - ref| may exceed the bf16 bound by at most
-# 2^-4 * sigmoid(g) * sum_t w_t |c_t| (w = the exact softmax weights, c = the
-# dequantised latent), which the oracle returns as `bound`.  The LSE bound is
-# unchanged.
+#
+# The reference is the pages' definition: the bf16 query, exactly, attending
+# over the dequantised cache (oracle.mla_decode_e4m3_reference).  The FP8
+# decode departs from it in two documented steps, and the tolerance adds a
+# bound for each, derived from E4M3's arithmetic (no observed error enters):
+#
+# (1) Query.  The FP8 tensor-core MMA multiplies E4M3 by E4M3, so each query row
+#     enters as two E4M3 parts, hi + lo, of v = q * 2^-e (e = the row's
+#     power-of-two scale, max |v| in (224, 448]).  v has bf16's 8 significant
+#     bits; hi keeps 4 and the remainder v - hi (at most 4 more bits, a multiple
+#     of v's last bit) is exact in lo while |v| >= 1/4 (the remainder's last bit
+#     is then >= 2^-9, E4M3's smallest step).  Below that lo is subnormal and off
+#     by at most half its step, 2^-10.  So query element d is off by at most
+#     eps_d = 2^(e - 10) where 0 < |q_d| < 2^(e - 2), else 0, and score t by at most
+#     delta_t = |scale| sum_d eps_d |x_t,d|; D = max_t delta_t.  Then the weights
+#     of the kernel's scores satisfy |w'_t / w_t - 1| <= e^{2D} - 1 and
+#     |lse' - lse| <= D.
+# (2) Probabilities.  P' = 2^(s' log2 e - m + 4) enters the value MMA as E4M3;
+#     P' <= 2^8 (rescale threshold 4), so it is off by at most max(2^-4 P',
+#     2^-10) (3 mantissa bits in the normal range, half the subnormal step
+#     below 2^-6).  The normaliser l' = sum P' is summed in fp32, and the
+#     largest P' is >= 2^4 (the reference maximum m never exceeds the largest
+#     score), so 2^-10 / l' <= 2^-14 w'_max.
+#
+# Together, per output element (A = sum_t w_t |c_t|, B = w_max sum_t |c_t|, both
+# gated, from the oracle):
+#   |out - ref| <= 1e-2 + 1e-2 |ref| + ((1 + 2^-4) e^{2D} - 1) A + 2^-14 e^{2D} B
+#   |lse - ref| <= 1e-3 + D
+# where 1e-2 + 1e-2 |ref| and 1e-3 are the bf16 path's tolerance (fp32
+# accumulation, bf16 output rounding).  For N(0, 1) queries D is ~1e-6, so (1)
+# adds almost nothing; (2) is the E4M3 probability rounding.
 P_E4M3_REL = 2.0 ** -4
+P_E4M3_SUB = 2.0 ** -14
+
+
+def fp8_query_error(qn, qr):
+    """eps [rows, 576]: the bound (1) above on each query element's error."""
+    qn, qr = oracle.oracle._as_f64(qn), oracle.oracle._as_f64(qr)
+    q = np.concatenate([qn.reshape(-1, qn.shape[-1]), qr.reshape(-1, qr.shape[-1])], axis=1)
+    e = oracle.query_scale_exponent(np.abs(q).max(axis=1)).astype(np.int64)[:, None]
+    small = (np.abs(q) < np.ldexp(1.0, e - 2)) & (q != 0.0)     # zero splits exactly
+    return np.where(small, np.ldexp(1.0, e - 10), 0.0)
 
 
 def gpu_decode_fp8(w, d, kv_scale, *, cta_budget=0, min_splits=None, scale=SCALE):
@@ -99,27 +133,37 @@ def gpu_decode_fp8(w, d, kv_scale, *, cta_budget=0, min_splits=None, scale=SCALE
 
 
 def oracle_decode_fp8(w, qn, qr, gate, slab8_host, kv_scale, rows=None, scale=SCALE):
+    """(out, lse, terms): the bf16-query reference and its bound terms."""
     return oracle.mla_decode_e4m3_reference(qn, qr, gate, slab8_host, kv_scale, w.page_table,
                                             w.seq_lens, w.n_q, w.num_heads, scale,
                                             num_pages=w.num_pages, page_stride=w.page_stride,
                                             page_tokens=w.page_tokens, dc=w.dc, dr=w.dr,
-                                            rows=rows, with_abs=True)
+                                            rows=rows, with_abs=True,
+                                            query_err=fp8_query_error(qn, qr))
 
 
-def assert_parity_fp8(out, lse, ref_out, ref_lse, bound, rows=None, what=""):
+def fp8_tolerance(ref_out, terms):
+    """(output bound [rows, 512], lse bound [rows]) of the derivation above."""
+    g = np.exp(2.0 * terms["D"])[:, None]
+    out_tol = (OUT_ATOL + OUT_RTOL * np.abs(ref_out) + ((1.0 + P_E4M3_REL) * g - 1.0) * terms["A"]
+               + P_E4M3_SUB * g * terms["B"])
+    return out_tol, LSE_ATOL + terms["D"]
+
+
+def assert_parity_fp8(out, lse, ref_out, ref_lse, terms, rows=None, what=""):
     o = out.float().cpu().numpy().reshape(-1, out.shape[-1]).astype(np.float64)
     l = lse.cpu().numpy().reshape(-1).astype(np.float64)
     if rows is not None:
         rows = np.asarray(rows, dtype=np.int64)
         o, l = o[rows], l[rows]
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    tol, ltol = fp8_tolerance(ref_out, terms)
     err = np.abs(o - ref_out)
-    tol = OUT_ATOL + OUT_RTOL * np.abs(ref_out) + P_E4M3_REL * bound
     bad = err > tol
     assert not bad.any(), (f"{what}: {int(bad.sum())} outputs out of tolerance, "
                            f"max err {err.max():.3e}")
     both_inf = np.isneginf(l) & np.isneginf(ref_lse)
     with np.errstate(invalid="ignore"):
         lerr = np.where(both_inf, 0.0, np.abs(l - ref_lse))
-    assert np.all(lerr <= LSE_ATOL), f"{what}: lse max err {np.nanmax(lerr):.3e}"
+    assert np.all(lerr <= ltol), f"{what}: lse max err {np.nanmax(lerr):.3e}"
     return float(err.max()), float(lerr.max())

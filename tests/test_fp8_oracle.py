@@ -79,22 +79,41 @@ def test_query_scale_is_the_smallest_power_of_two_that_fits():
     assert oracle.query_scale_exponent([448.0]).tolist() == [0]
 
 
-def test_query_rows_quantise_within_half_an_fp8_step():
+def test_two_part_query_is_exact_above_a_quarter_of_the_scale():
+    """The split the FP8 decode's tolerance relies on, by brute force over every
+    finite bf16 magnitude up to the row maximum: (hi + lo) * 2^e equals q
+    exactly where |q| >= 2^(e - 2), and is within 2^(e - 10) below that; hi
+    alone is within 2^-4 relative in E4M3's normal range."""
+    mags = np.arange(0, 0x43E1, dtype=np.uint16)          # +0 .. 448 as bf16 bit patterns
+    vals = oracle.oracle._bf16_to_f64(mags)
+    assert vals.max() == 448.0
+    for scale_exp in (0, -7, 5):
+        q = np.concatenate([vals, -vals]) * 2.0 ** scale_exp
+        pad = (-q.size) % ROW
+        q = np.concatenate([q, np.zeros(pad)]).reshape(-1, ROW)
+        q[:, 0] = 400.0 * 2.0 ** scale_exp                # every row's maximum: e = scale_exp
+        qn = _bf16_bits(q[:, :DC])
+        qr = _bf16_bits(q[:, DC:])
+        hi, lo, e = oracle.quantize_query_rows(qn, qr)
+        assert np.all(e == scale_exp)
+        back = oracle.dequantize_query_rows(hi, lo, e)
+        big = np.abs(q) >= 2.0 ** (scale_exp - 2)
+        assert np.array_equal(back[big], q[big])
+        assert np.abs(back - q)[~big].max() <= 2.0 ** (scale_exp - 10)
+        hi_only = np.ldexp(oracle.e4m3_decode(hi), e[:, None].astype(np.int64))
+        normal = np.abs(q) >= 2.0 ** (scale_exp - 6)
+        assert (np.abs(hi_only - q)[normal] / np.abs(q)[normal]).max() <= 2.0 ** -4
+
+
+def test_query_scale_puts_the_row_maximum_in_the_top_binade():
     rng = np.random.Generator(np.random.PCG64(2))
     qn = _bf16_bits(rng.standard_normal((6, DC)) * np.array([1, 1e-3, 100, 5, 1, 0.01])[:, None])
     qr = _bf16_bits(rng.standard_normal((6, DR)))
-    codes, e = oracle.quantize_query_rows(qn, qr)
-    assert codes.shape == (6, ROW) and codes.dtype == np.uint8
+    hi, lo, e = oracle.quantize_query_rows(qn, qr)
+    assert hi.shape == (6, ROW) and lo.shape == (6, ROW) and hi.dtype == np.uint8
     q = np.concatenate([oracle.oracle._bf16_to_f64(qn), oracle.oracle._bf16_to_f64(qr)], axis=1)
-    back = oracle.dequantize_query_rows(codes, e)
-    # the row maximum lands in (224, 448] and normal-range values are within 2^-4
     amax = np.abs(q).max(axis=1)
     assert np.all(amax * 2.0 ** -e > 224.0) and np.all(amax * 2.0 ** -e <= 448.0)
-    normal = np.abs(q) * 2.0 ** -e[:, None] >= 2.0 ** -6
-    rel = np.abs(back - q)[normal] / np.abs(q)[normal]
-    assert rel.max() <= 2.0 ** -4
-    # bf16 holds the dequantised values exactly (they are what the FP8 MMA multiplies)
-    _f64_to_bf16_exact(back)
 
 
 def _random_fp8_pool(rng, num_pages, page_tokens):
@@ -141,6 +160,9 @@ def test_fp8_kv_scale_factors_out_of_scores_and_outputs():
 
 
 def test_fp8_decode_is_the_softmax_over_explicit_dequantised_rows():
+    """The E4M3 reference is the bf16 query over the dequantised rows, and its
+    bound terms are what they claim: A = sigmoid(g) sum_t w_t |c_t|,
+    B = sigmoid(g) w_max sum_t |c_t|, D = max_t |scale| sum_d eps_d |x_t,d|."""
     rng = np.random.Generator(np.random.PCG64(5))
     pt, pages, H, n_q = 4, 8, 2, 1
     pool8 = _random_fp8_pool(rng, pages, pt)
@@ -149,25 +171,120 @@ def test_fp8_decode_is_the_softmax_over_explicit_dequantised_rows():
     qn = _bf16_bits(rng.standard_normal((2, H, DC)) * 3)
     qr = _bf16_bits(rng.standard_normal((2, H, DR)))
     gate = _bf16_bits(rng.standard_normal((2, H, DC)))
-    kv_scale, scale = 0.5, 0.25
-    out, lse, bound = oracle.mla_decode_e4m3_reference(
+    eps = rng.random((2 * H, ROW)) * (rng.random((2 * H, ROW)) < 0.1)
+    kv_scale, scale = 0.5, -0.25
+    out, lse, terms = oracle.mla_decode_e4m3_reference(
         qn, qr, gate, pool8, kv_scale, table, lens, n_q, H, scale, num_pages=pages,
-        page_tokens=pt, dc=DC, dr=DR, with_abs=True)
-    codes, e = oracle.quantize_query_rows(qn.reshape(-1, DC), qr.reshape(-1, DR))
-    qd = oracle.dequantize_query_rows(codes, e)
+        page_tokens=pt, dc=DC, dr=DR, with_abs=True, query_err=eps)
+    q = np.concatenate([oracle.oracle._bf16_to_f64(qn).reshape(-1, DC),
+                        oracle.oracle._bf16_to_f64(qr).reshape(-1, DR)], axis=1)
     g = oracle.oracle._bf16_to_f64(gate).reshape(-1, DC)
     for r in range(2):
         rows = [pool8[table[r, t // pt], (t % pt) * ROW:(t % pt + 1) * ROW] for t in range(lens[r])]
         x = kv_scale * oracle.e4m3_decode(np.stack(rows))
         for h in range(H):
             i = r * H + h
-            s = scale * (x @ qd[i])
+            s = scale * (x @ q[i])
             w = np.exp(s - s.max())
             w /= w.sum()
             sig = 1.0 / (1.0 + np.exp(-g[i]))
             assert np.allclose(out[i], sig * (w @ x[:, :DC]), rtol=1e-12, atol=1e-14)
-            assert np.allclose(bound[i], sig * (w @ np.abs(x[:, :DC])), rtol=1e-12, atol=1e-14)
+            assert np.allclose(terms["A"][i], sig * (w @ np.abs(x[:, :DC])), rtol=1e-12,
+                               atol=1e-14)
+            assert np.allclose(terms["B"][i], sig * w.max() * np.abs(x[:, :DC]).sum(axis=0),
+                               rtol=1e-12, atol=1e-14)
+            assert terms["D"][i] == pytest.approx(abs(scale) * (np.abs(x) @ eps[i]).max(),
+                                                  rel=1e-12)
             assert lse[i] == pytest.approx(s.max() + np.log(np.exp(s - s.max()).sum()), abs=1e-12)
+
+
+def test_derived_fp8_bound_covers_the_two_part_query_and_e4m3_probabilities():
+    """The tolerance the GPU tests use (tests/helpers.py), checked against a
+    double-precision model of the two documented approximations on a random
+    problem: the two-part query (exact dequantised values) and E4M3-rounded
+    probabilities 2^(x - m + 4) with fp32 normaliser.  A plausible mistake in the
+    bound (dropping a term, the wrong sign of D) fails here first."""
+    import helpers
+    rng = np.random.Generator(np.random.PCG64(9))
+    pt, pages, H = 8, 40, 4
+    pool8 = _random_fp8_pool(rng, pages, pt)
+    pool8[rng.random(pool8.shape) < 0.5] = 0x30         # a skewed pool: sharper softmax
+    lens = np.array([300, 17, 1], dtype=np.int32)
+    table = np.stack([rng.permutation(pages)[:38] for _ in range(3)]).astype(np.int32)
+    qn = _bf16_bits(rng.standard_normal((3, H, DC)) * 4)
+    qr = _bf16_bits(rng.standard_normal((3, H, DR)))
+    qn[0, 0, :4] = _bf16_bits(rng.standard_normal(4) * 1e-4)   # elements below 2^(e-2)
+    gate = _bf16_bits(rng.standard_normal((3, H, DC)))
+    kvs, scale = 0.05, 0.072
+    eps = helpers.fp8_query_error(qn, qr)
+    ref, ref_lse, terms = oracle.mla_decode_e4m3_reference(
+        qn, qr, gate, pool8, kvs, table, lens, 1, H, scale, num_pages=pages, page_tokens=pt,
+        dc=DC, dr=DR, with_abs=True, query_err=eps)
+    hi, lo, e = oracle.quantize_query_rows(qn, qr)
+    qd = oracle.dequantize_query_rows(hi, lo, e)
+    tol, ltol = helpers.fp8_tolerance(ref, terms)
+    g = oracle.oracle._bf16_to_f64(gate).reshape(-1, DC)
+    for r in range(3):
+        x = kvs * oracle.e4m3_decode(np.stack(
+            [pool8[table[r, t // pt], (t % pt) * ROW:(t % pt + 1) * ROW] for t in range(lens[r])]))
+        for h in range(H):
+            i = r * H + h
+            s = scale * (x @ qd[i]) * np.log2(np.e)          # the kernel's scores, log2 units
+            p = np.exp2(s - s.max() + 4.0)
+            p8 = oracle.e4m3_decode(oracle.e4m3_encode(p))
+            o = (p8 @ x[:, :DC]) / p.sum()
+            out = o / (1.0 + np.exp(-g[i]))
+            lse = (s.max() - 4.0 + np.log2(p.sum())) * np.log(2.0)
+            assert np.all(np.abs(out - ref[i]) <= tol[i] - 1e-2)   # inside the derived part alone
+            assert abs(lse - ref_lse[i]) <= ltol[i]
+    assert terms["D"][0] > 0.0
+
+
+def test_derived_fp8_bound_needs_each_of_its_terms():
+    """Two constructed rows where the model's error comes close to one term of
+    the bound, so that dropping that term (or flipping the sign of D) fails.
+    Head 0: one token at the maximum and 10,000 equal tokens 13.51 log2 units
+    below it, whose probabilities 0.7 * 2^-9 all round up to the subnormal step
+    2^-9 (the B term).  Head 1: eleven query elements of 0.6 * 2^-17 whose lo
+    parts all round the same way, shifting every score by 0.8 D (the D term)."""
+    import helpers
+    pt, n = 8, 10_001
+    pages = -(-n // pt)
+    row = np.full(ROW, 0x7E, dtype=np.uint8)          # 448 everywhere but element 0
+    row[0] = 0x00
+    pool8 = np.tile(row, (pages, pt))
+    pool8[0, 0] = 0x38                                # token 0: element 0 = 1.0
+    table = np.arange(pages, dtype=np.int32)[None, :]
+    lens = np.array([n], dtype=np.int32)
+    q = np.zeros((1, 2, ROW))
+    q[0, :, 0] = 1.0
+    q[0, 1, 1:] = 0.6 * 2.0 ** -17
+    qn, qr = _bf16_bits(q[..., :DC]), _bf16_bits(q[..., DC:])
+    gate = _bf16_bits(np.zeros((1, 2, DC)))
+    scale = (13.0 - np.log2(0.7) + 4.0 - 4.0) / np.log2(np.e)   # 13.51 log2 units per unit
+    eps = helpers.fp8_query_error(qn, qr)
+    ref, ref_lse, terms = oracle.mla_decode_e4m3_reference(
+        qn, qr, gate, pool8, 1.0, table, lens, 1, 2, scale, num_pages=pages, page_tokens=pt,
+        dc=DC, dr=DR, with_abs=True, query_err=eps)
+    hi, lo, e = oracle.quantize_query_rows(qn, qr)
+    qd = oracle.dequantize_query_rows(hi, lo, e)
+    x = oracle.e4m3_decode(pool8.reshape(-1, ROW)[:n])
+    assert terms["D"][0] == 0.0 and terms["D"][1] > 0.1
+    tol, ltol = helpers.fp8_tolerance(ref, terms)
+    for h in range(2):
+        s = scale * (x @ qd[h]) * np.log2(np.e)
+        p = np.exp2(s - s.max() + 4.0)
+        p8 = oracle.e4m3_decode(oracle.e4m3_encode(p))
+        out = 0.5 * (p8 @ x[:, :DC]) / p.sum()
+        lse = (s.max() - 4.0 + np.log2(p.sum())) * np.log(2.0)
+        err = np.abs(out - ref[h])
+        assert np.all(err <= tol[h] - 1e-2 - 1e-2 * np.abs(ref[h]))
+        assert abs(lse - ref_lse[h]) <= ltol[h]
+        if h == 0:       # the B term carries it: the rest of the bound is too small
+            rest = ((1 + helpers.P_E4M3_REL) * np.exp(2 * terms["D"][0]) - 1) * terms["A"][0]
+            assert err[1:].max() > 2 * rest[1:].max()
+        else:            # the LSE moves by most of D
+            assert abs(lse - ref_lse[h]) > 0.5 * terms["D"][1] > 1e-2
 
 
 def test_fp8_append_lands_rows_as_codes_of_the_scaled_values():
