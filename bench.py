@@ -61,6 +61,11 @@ def parse_args(argv=None):
                          "(the deployment's FP8 cache, 576 bytes per token row)")
     ap.add_argument("--workload", default="long",
                     choices=["tiny", "steady", "agentic", "spec", "long", "extend"])
+    ap.add_argument("--layers", type=int, default=None,
+                    help="decode only the first N layer slabs of a multi-layer workload: a "
+                         "smaller case of the same per-layer launch for ncu captures (each "
+                         "layer's launch is the same work on its own slab); the line then "
+                         "names N layers and is not the workload's measurement")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -304,8 +309,10 @@ def cpu_baseline(w, qn, qr, gate, slab_dev, target_s, kv_scale=None):
     gbs = frac * kv * reps / elapsed / 1e9
     what = ("all {} heads".format(w.num_heads) if rows is None else
             f"{frac:.4f} of the rows (first, middle and last new token, 4 heads)")
+    layer = (f" of layer 0 (of {w.num_slabs}; every layer is the same work, so the rate "
+             f"is the step's)" if w.num_slabs > 1 else "")
     return {"value": gbs, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n} of {w.num_reqs} requests x {what}, {reps} pass(es), "
+            "sample": f"{n} of {w.num_reqs} requests x {what}{layer}, {reps} pass(es), "
                       f"{elapsed:.1f} s of double-precision oracle time, KV bytes credited "
                       f"in proportion to the rows",
             "request_steps_per_s": frac * n * reps / elapsed}
@@ -335,6 +342,10 @@ def run_gpu(args):
     dist = dist_init(world, "nccl")
 
     w = inputs.make_workload(args.workload)
+    if args.layers is not None:
+        if not 1 <= args.layers <= w.num_slabs:
+            raise SystemExit(f"--layers must lie in [1, {w.num_slabs}]")
+        w.num_slabs = args.layers
     fp8 = args.kv == "fp8"
     layers = w.num_slabs
     qs = [inputs.make_queries(w, device, layer=l) for l in range(layers)]

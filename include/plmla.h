@@ -276,8 +276,8 @@ plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q_rope, cons
 
 /*
  * mla_workspace_size_fp8 -- workspace bytes of mla_decode_fp8 for a shape: that
- * of mla_decode plus the quantised queries (num_reqs*n_q*num_heads rows of 576
- * bytes and one int32 exponent each).  0 for an unsupported shape.
+ * of mla_decode plus the two-part FP8 queries (num_reqs*n_q*num_heads rows of
+ * 2 x 576 bytes and one int32 exponent each).  0 for an unsupported shape.
  */
 size_t mla_workspace_size_fp8(int32_t num_reqs, int32_t n_q, int32_t num_heads,
                               int32_t cta_budget, int32_t min_splits_per_req);
@@ -290,19 +290,23 @@ size_t mla_workspace_size_fp8(int32_t num_reqs, int32_t n_q, int32_t num_heads,
  *
  * Every slab element is one OCP E4M3 byte (bias 7, 3 mantissa bits, no
  * infinity, S.1111.111 = NaN) and stands for kv_scale * its value; a token row
- * is 576 bytes (512 latent, then 64 rope).  The queries stay bf16 at the
- * boundary; the call quantises each query row q = [q_nope | q_rope] (576
- * values) to E4M3 codes of q * 2^-e, with e the smallest integer >= -126 for
- * which max|q| * 2^-e <= 448 (0 for an all-zero row), because the FP8
- * tensor-core MMA multiplies E4M3 by E4M3.  Then, with q' = 2^e * code:
+ * is 576 bytes (512 latent, then 64 rope).  The operation is mla_decode's with
+ * x_t = kv_scale * decoded bytes and the bf16 query as given:
  *
- *   s_t = scale * kv_scale * (q'[0:512] . x_t[0:512] + q'[512:576] . x_t[512:576])
- *   o   = kv_scale * sum_{t < L'} softmax(s)_t * x_t[0:512]
+ *   s_t = scale * (q_nope_absorbed . x_t[0:512] + q_rope . x_t[512:576])
+ *   o   = sum_{t < L'} softmax(s)_t * x_t[0:512]
  *   lse = ln sum_{t < L'} exp(s_t);   out = bf16_rn(sigmoid(gate) * o)
  *
- * computed with fp32 accumulation; the probabilities enter the value MMA as
- * E4M3 (relative rounding <= 2^-4 per weight), their sum for the normaliser
- * and lse stays fp32.
+ * How it is computed: the FP8 tensor-core MMA multiplies E4M3 by E4M3, so each
+ * query row q = [q_nope | q_rope] is scaled to v = q * 2^-e (e the smallest
+ * integer >= -126 with max|q| * 2^-e <= 448; 0 for an all-zero row) and enters
+ * as two E4M3 parts, hi = E4M3(v) and lo = E4M3(v - hi), each multiplied with
+ * the cache in its own MMA into one fp32 accumulator.  hi + lo equals v
+ * exactly where |v| >= 2^-2 and is within 2^-10 below it, so the scores are
+ * those of the bf16 query up to that.  The probabilities enter the value MMA
+ * as E4M3 (relative rounding <= 2^-4 in E4M3's normal range, <= 2^-10 absolute
+ * below it, with the row's largest probability scaled to >= 16); their sum for
+ * the normaliser and lse stays fp32.
  *
  * Arguments as mla_decode, except:
  * slab_base          E4M3 bytes, 16-byte aligned
@@ -324,10 +328,12 @@ plmla_status mla_decode_fp8(const void *q_nope_absorbed, const void *q_rope, con
 /*
  * mla_quantize_queries_fp8 -- the query step of mla_decode_fp8 on its own: rows
  * of [q_nope | q_rope] (512 + 64 bf16 values, row i at q_nope + 512 i and
- * q_rope + 64 i) become q8[576 i .. 576 i + 575] = E4M3 codes of q * 2^-e
- * (round to nearest even) and qexp[i] = e, the smallest integer >= -126 with
- * max|q| * 2^-e <= 448 (0 for an all-zero row).  q_nope, q_rope and q8 16-byte
- * aligned; rows 0 .. 2^31-1.  Asynchronous on `stream`.
+ * q_rope + 64 i) become two E4M3 parts of v = q * 2^-e (round to nearest even):
+ * q8[576 i .. 576 i + 575] = hi = E4M3(v) and q8[576 (rows + i) ..] = lo =
+ * E4M3(v - hi), and qexp[i] = e, the smallest integer >= -126 with
+ * max|q| * 2^-e <= 448 (0 for an all-zero row).  q8 holds 2 * rows * 576 bytes
+ * (the hi plane, then the lo plane).  q_nope, q_rope and q8 16-byte aligned;
+ * rows 0 .. 2^30.  Asynchronous on `stream`.
  */
 plmla_status mla_quantize_queries_fp8(const void *q_nope_absorbed, const void *q_rope,
                                       int64_t rows, void *q8, int32_t *qexp, void *stream);

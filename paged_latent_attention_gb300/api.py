@@ -108,7 +108,8 @@ def mla_decode_fp8(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, *,
     """mla_decode over E4M3 pages: slab is [num_pages, page_stride] uint8 (or
     float8_e4m3fn) holding E4M3 codes of value / kv_scale, 576 bytes per token
     row (page_stride >= 1536*576, a multiple of 16).  The queries stay bf16;
-    the library quantises each query row to E4M3 with a power-of-two scale.
+    the library splits each query row into two E4M3 parts with a power-of-two
+    scale (exact for elements above 2^-2 of the scale).
     The workspace must come from allocate_workspace(..., fp8=True)."""
     _require(math.isfinite(kv_scale) and kv_scale > 0, "kv_scale must be finite and > 0")
     return _decode(q_nope_absorbed, q_rope, gate, _byte_view(slab), page_table, seq_lens,
@@ -175,21 +176,23 @@ def _decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, kv_scale,
 
 
 def mla_quantize_queries_fp8(q_nope_absorbed, q_rope, stream=None):
-    """The FP8 decode's query step: (codes [rows, 576] uint8, exps [rows] int32)
-    for the rows of [q_nope | q_rope] (any leading shape, flattened)."""
+    """The FP8 decode's query step: (hi [rows, 576] uint8, lo [rows, 576] uint8,
+    exps [rows] int32) for the rows of [q_nope | q_rope] (any leading shape,
+    flattened): q = (decode(hi) + decode(lo)) * 2^exp, exactly where
+    |q| >= 2^(exp - 2)."""
     _require(q_nope_absorbed.is_cuda and q_nope_absorbed.dtype == torch.bfloat16
              and q_nope_absorbed.is_contiguous() and q_nope_absorbed.shape[-1] == LATENT,
              "q_nope_absorbed must be contiguous CUDA bf16 [..., 512]")
     rows = q_nope_absorbed.numel() // LATENT
     _require(q_rope.is_cuda and q_rope.dtype == torch.bfloat16 and q_rope.is_contiguous()
              and q_rope.numel() == rows * ROPE, "q_rope must be contiguous CUDA bf16 [..., 64]")
-    codes = torch.empty(rows, ROW, dtype=torch.uint8, device=q_nope_absorbed.device)
+    codes = torch.empty(2, rows, ROW, dtype=torch.uint8, device=q_nope_absorbed.device)
     exps = torch.empty(rows, dtype=torch.int32, device=q_nope_absorbed.device)
     status = _native.lib().mla_quantize_queries_fp8(
         q_nope_absorbed.data_ptr(), q_rope.data_ptr(), rows, codes.data_ptr(), exps.data_ptr(),
         _stream_ptr(stream, q_nope_absorbed.device))
     _native.check(status, "mla_quantize_queries_fp8")
-    return codes, exps
+    return codes[0], codes[1], exps
 
 
 def set_page_checks(on: bool) -> None:

@@ -140,7 +140,7 @@ WorkspaceLayout layout_for(int32_t num_reqs, const Shape &sh, bool fp8)
     off = align_up(off + sizeof(float) * part_rows);
     const size_t q_rows = (size_t)num_reqs * sh.rows_per_req;
     w.q8 = off;
-    off = fp8 ? align_up(off + (size_t)kRow * q_rows) : off;
+    off = fp8 ? align_up(off + 2 * (size_t)kRow * q_rows) : off;   // hi and lo planes
     w.qexp = off;
     off = fp8 ? align_up(off + sizeof(int32_t) * q_rows) : off;
     w.total = off;
@@ -509,7 +509,7 @@ extern "C" plmla_status mla_quantize_queries_fp8(const void *q_nope_absorbed, co
                                                  int64_t rows, void *q8, int32_t *qexp,
                                                  void *stream)
 {
-    if (rows < 0 || rows > INT32_MAX)
+    if (rows < 0 || rows > (int64_t)1 << 30)
         return PLMLA_INVALID_ARGUMENT;
     if (rows == 0)
         return PLMLA_OK;

@@ -72,7 +72,7 @@ constexpr int kWarpVProducer = 10, kWarpPvIssuer = 11;
 constexpr int kSubBytes = kTile * 64 * 2;       // one ring slot: 16 KB
 constexpr int kVHalf = 64 * 64 * 2;             // one 64 x 64 half of a bf16 V item
 constexpr int kTmemCols = 512;
-constexpr int kTmemS = 256;                     // S^T buffers at columns 256 and 320
+constexpr int kTmemS = 256;                     // S^T buffers from column 256 on
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;
@@ -85,8 +85,11 @@ constexpr int kMaxK = 8, kMaxV = 8;             // ring slots (K, V) at most
 //     two 64-column TMA boxes; P^T in bf16 (tcgen05 kind::f16).
 //   E4M3 pages (FP8 cache): five K items of 128 byte-columns (4 latent blocks +
 //     the rope block, whose upper 64 columns the TMA unit fills with zeros and no
-//     MMA reads), 4 MMAs of K = 32 each (2 on the rope); four V items of 128
-//     tokens x 128 latent rows; P^T in E4M3 (kind::f8f6f4, E4M3 x E4M3).
+//     MMA reads), 4 MMAs of K = 32 each (2 on the rope) with N = 2 NG: the B
+//     operand stacks the hi rows of the two-part query over its lo rows, so the
+//     K tile is read once and S^T holds hi and lo scores side by side (the
+//     softmax adds them); four V items of 128 tokens x 128 latent rows; P^T in
+//     E4M3 (kind::f8f6f4, E4M3 x E4M3).
 // P = 2^(x - m + p_off) with x - m <= tau keeps P finite in its format; the
 // E4M3 offset moves the bulk of a diffuse softmax above E4M3's subnormals.
 template <bool F8>
@@ -94,8 +97,12 @@ struct Fmt {
     static constexpr int sub = F8 ? 5 : 9;              // K items per tile
     static constexpr int col_step = F8 ? 128 : 64;      // K item width (elements)
     static constexpr int rope_mmas = F8 ? 2 : 4;        // MMAs on the rope item
-    static constexpr int v_items = F8 ? 4 : 8;          // V items per tile
     static constexpr int v_tokens = F8 ? 128 : 64;      // tokens per V item
+    static constexpr int s_rows = F8 ? 2 : 1;           // S^T columns per query row (hi, lo)
+    static constexpr int s_stride = F8 ? 128 : 64;      // TMEM columns between S^T buffers
+    static constexpr int v_per_block = kTile / v_tokens; // V items per 128-latent block
+    static constexpr int v_items = 4 * v_per_block;     // V items per tile
+    static constexpr int v_slot = v_tokens * 128 * (F8 ? 1 : 2);   // bytes per V item (ring slot)
     static constexpr float tau = F8 ? 4.f : 8.f;        // lagged-maximum threshold (log2)
     static constexpr float p_off = F8 ? 4.f : 0.f;
 };
@@ -105,21 +112,28 @@ struct Smem {
     using F = Fmt<F8>;
     static constexpr int pn = F8 && NG < 32 ? 32 : NG;      // P^T columns (MMA N of P^T V)
     static constexpr int p_row = F8 ? pn : 2 * NG;          // bytes per token row of P^T
-    static constexpr int q_chunk = NG * 128;                // one 128-byte column block of Q^T
-    // Q^T: bf16 nine 128-byte blocks; E4M3 four 128-byte latent blocks and the rope
-    // block of 64 bytes per row (64-byte swizzle)
-    static constexpr int q_rope_bytes = F8 ? NG * 64 : q_chunk;
+    // Q^T: bf16 nine 128-byte column blocks of NG rows; E4M3 four 128-byte latent
+    // blocks and the rope block of 64 bytes per row (64-byte swizzle), each with
+    // the NG hi rows of the two-part query followed by its NG lo rows
+    static constexpr int q_chunk = F::s_rows * NG * 128;    // one 128-byte column block
+    static constexpr int q_lo = NG * 128;                   // lo rows within a block (E4M3)
+    static constexpr int q_rope_bytes = F8 ? 2 * NG * 64 : q_chunk;
+    static constexpr int q_rope_lo = NG * 64;               // lo rows within the rope block
     static constexpr int q_bytes = (F::sub - 1) * q_chunk + q_rope_bytes;
     static constexpr int p_bytes = kTile * p_row;           // P^T
     static constexpr int bar_bytes = 512;
     static constexpr int misc_bytes = bar_bytes + 4 * 64 * 4 + 4 * 64 * 4 + 32;
-    static constexpr int fixed = p_bytes + q_bytes + misc_bytes + 1024;
-    static constexpr int slots_fit = (kMaxDynSmem - fixed) / kSubBytes;
-    // bf16: half of the slots for each ring; E4M3: one tile of V items, the rest K
-    static constexpr int v_slots = F8 ? 4 : (slots_fit / 2 < kMaxV ? slots_fit / 2 : kMaxV);
-    static constexpr int k_slots = slots_fit - v_slots < kMaxK ? slots_fit - v_slots : kMaxK;
+    // no alignment slack: the dynamic shared memory base is 1024-aligned (the
+    // kernel checks it on entry)
+    static constexpr int fixed = p_bytes + q_bytes + misc_bytes;
+    static constexpr int avail = kMaxDynSmem - fixed;
+    // bf16: half of the 16 KB slots for each ring; E4M3: four 8 KB V slots (half
+    // a tile), the rest K
+    static constexpr int v_slots = F8 ? 4 : ((avail / kSubBytes) / 2 < kMaxV ? (avail / kSubBytes) / 2 : kMaxV);
+    static constexpr int k_fit = (avail - v_slots * F::v_slot) / kSubBytes;
+    static constexpr int k_slots = k_fit < kMaxK ? k_fit : kMaxK;
     static constexpr int v_off = k_slots * kSubBytes;
-    static constexpr int p_off = v_off + v_slots * kSubBytes;
+    static constexpr int p_off = v_off + v_slots * F::v_slot;
     static constexpr int q_off = p_off + p_bytes;            // 1024-aligned
     static constexpr int bar_off = q_off + q_bytes;          // 1024-aligned
     static constexpr int red_off = bar_off + bar_bytes;      // float red[4][64]
@@ -129,9 +143,10 @@ struct Smem {
     static constexpr int cf_off = al_off + 64 * 4;           // float cf[64]  (E4M3 score factors)
     static constexpr int misc_off = cf_off + 64 * 4;         // tmem addr, abort, need[2]
     static constexpr int bytes = misc_off + 32;
-    static constexpr int alloc = bytes + 1024;               // slack for 1024-B alignment
+    static constexpr int alloc = bytes;
     static_assert(k_slots >= 2 && v_slots >= 2, "ring depth");
-    static_assert(p_bytes % 1024 == 0 && q_chunk % 1024 == 0 && q_bytes % 1024 == 0,
+    static_assert(p_bytes % 1024 == 0 && q_chunk % 1024 == 0 && q_lo % 1024 == 0 &&
+                      q_rope_lo % 512 == 0 && F::v_slot % 1024 == 0 && F::s_rows * NG <= F::s_stride,
                   "swizzle atom alignment");
     static_assert(alloc <= kMaxDynSmem, "shared memory budget");
 };
@@ -550,15 +565,22 @@ __device__ __forceinline__ void scatter_to_red(const float (&v)[NG], float *red_
 // tokens a row may not see set to -inf: past the chunk end, or past the row's
 // causal limit L - (n_q - 1 - j) among the draft tokens.  The mask runs behind
 // one branch that is taken only on a request's last tiles.  bf16 scores take the
-// one factor scale * log2 e; E4M3 scores the per-row factor at cf_addr
-// (scale * log2 e * kv_scale * 2^e_row, the query row's power-of-two scale).
+// one factor scale * log2 e; E4M3 scores (hi plus lo part) the per-row factor at
+// cf_addr (scale * log2 e * kv_scale * 2^e_row, the query row's power-of-two scale).
 template <int NG, bool F8>
-__device__ __forceinline__ void load_scores(uint32_t taddr, float scale_log2, uint32_t cf_addr,
-                                            bool tile_visible, int t, int t_end, int vis_all,
-                                            int row0, int heads, float (&x)[NG])
+__device__ __forceinline__ void load_scores(uint32_t taddr, uint32_t lo_cols, float scale_log2,
+                                            uint32_t cf_addr, bool tile_visible, int t, int t_end,
+                                            int vis_all, int row0, int heads, float (&x)[NG])
 {
     tmem_load_cols<NG>(taddr, x);
     if constexpr (F8) {
+        // the lo part's scores sit lo_cols columns further on: the row's score is
+        // the sum of the two (both in units of the query's 2^e)
+        float y[NG];
+        tmem_load_cols<NG>(taddr + lo_cols, y);
+#pragma unroll
+        for (int c = 0; c < NG; ++c)
+            x[c] += y[c];
 #pragma unroll
         for (int c4 = 0; c4 < NG; c4 += 4) {
             float f[4];
@@ -635,9 +657,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     using L = Smem<NG, F8>;
     using F = Fmt<F8>;
     constexpr int NK = L::k_slots, NV = L::v_slots;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *smem = reinterpret_cast<unsigned char *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // The swizzled TMA boxes and MMA operands need 1024-byte alignment, and the
+    // layout has no slack for it: with no static shared memory the dynamic base
+    // is aligned.  Should it ever not be, report status 12 and touch nothing.
+    if ((smem_u32(smem_raw) & 1023u) != 0u) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");   // the plan resets the status word
+        if (threadIdx.x == 0)
+            atomicExch(a.status, 12);
+        return;
+    }
+    unsigned char *smem = smem_raw;
     const uint32_t s_k = smem_u32(smem);             // K ring
     const uint32_t s_v = s_k + L::v_off;             // V ring
     const uint32_t s_p = s_k + L::p_off;             // P^T
@@ -708,7 +738,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     if (warp == kWarpVProducer) {
         // V slots start at zero: a partial item leaves the rows past the history
         // untouched, and they must be finite (they meet zero probabilities)
-        for (int off = 16 * lane; off < NV * kSubBytes; off += 16 * 32)
+        for (int off = 16 * lane; off < NV * F::v_slot; off += 16 * 32)
             st_shared_v4(s_v + off, 0u, 0u, 0u, 0u);
         fence_proxy_async();
     }
@@ -755,10 +785,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 mbar_arrive_expect_tx(bar_q, L::q_bytes);
                 if constexpr (F8) {
                     // E4M3 rows of 576 bytes: four latent blocks, then the 64-byte rope
-                    // block through its own map
-                    for (int k = 0; k < F::sub - 1; ++k)
+                    // block through its own map; the hi part (rows of plane 0), then the
+                    // lo part (plane 1, all query rows further on)
+                    const int qrow_lo = qrow + a.num_reqs * a.rows_per_req;
+                    for (int k = 0; k < F::sub - 1; ++k) {
                         tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 128 * k, qrow, bar_q);
+                        tma_load_2d(s_q + k * L::q_chunk + L::q_lo, &tm_qn, 128 * k, qrow_lo,
+                                    bar_q);
+                    }
                     tma_load_2d(s_q + (F::sub - 1) * L::q_chunk, &tm_qr, kLatent, qrow, bar_q);
+                    tma_load_2d(s_q + (F::sub - 1) * L::q_chunk + L::q_rope_lo, &tm_qr, kLatent,
+                                qrow_lo, bar_q);
                 } else {
                     for (int k = 0; k < F::sub - 1; ++k)
                         tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 64 * k, qrow, bar_q);
@@ -826,8 +863,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         }
     } else if (warp == kWarpVProducer) {
         // ---------------------------------------------------------- V producer
-        // bf16: V item v of a tile = latent block v / 2 (128 columns), token half
-        // v % 2.  E4M3: item v = latent block v, all 128 tokens of the tile.
+        // V item v of a tile = latent block v / v_per_block (128 latent columns: two
+        // 64-column boxes for bf16, one 128-byte box for E4M3), the tile's tokens
+        // [(v % v_per_block) * v_tokens, + v_tokens).
         // In a request's last tile an item loads only its rows inside the history,
         // as boxes of power-of-two heights (the tail maps) issued together; the
         // rows past the history keep what the slot held before -- zeros written
@@ -849,19 +887,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 const int tok = t % kPageTokens;
                 for (int v = 0; v < F::v_items; ++v) {
                     // first token of the item within the tile
-                    const int toff = F8 ? 0 : 64 * (v & 1);
+                    const int toff = (v % F::v_per_block) * F::v_tokens;
                     bool got = true;
                     if (lane == 0)
                         got = wait_bounded(bar_empty_v + 8 * slot, phase ^ 1, abort_flag, a.status,
                                            11);
                     if (lane == 0 && got) {
-                        const uint32_t dst = s_v + slot * kSubBytes;
+                        const uint32_t dst = s_v + slot * F::v_slot;
                         const uint32_t fb = bar_full_v + 8 * slot;
-                        const int col = F8 ? 128 * v : 128 * (v >> 1), tk = tok + toff;
+                        const int col = 128 * (v / F::v_per_block), tk = tok + toff;
                         // rows of the item inside the history
                         const int live = seg.z - (t + toff);
                         if (live >= F::v_tokens) {
-                            mbar_arrive_expect_tx(fb, kSubBytes);
+                            mbar_arrive_expect_tx(fb, F::v_slot);
                             tma_load_3d_hint(dst, &tm_v, col, tk, page, fb, pol_once);
                             if constexpr (!F8)
                                 tma_load_3d_hint(dst + kVHalf, &tm_v, col + 64, tk, page, fb,
@@ -908,7 +946,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         // -------------------------------------------------------- S^T issuer
         if (lane == 0) {
             bool issued = false, ok = true;
-            constexpr uint32_t idesc_s = idesc_for<F8>(128, NG, false, false);
+            constexpr uint32_t idesc_s = idesc_for<F8>(128, F::s_rows * NG, false, false);
             const uint64_t dk0 = sdesc(s_k, 16, 1024, kSw128);
             const uint64_t dq0 = sdesc(s_q, 16, 1024, kSw128);
             const uint64_t dq_rope =
@@ -943,7 +981,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t d_s = tmem + kTmemS + 64 * b;
+                    const uint32_t d_s = tmem + kTmemS + F::s_stride * b;
 #pragma unroll
                     for (int k = 0; k < F::sub; ++k) {
                         if (!wait_bounded(bar_full_k + 8 * slot, phase, abort_flag, a.status, 4)) {
@@ -1018,15 +1056,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t da = dv0 + (uint64_t)(slot * (kSubBytes >> 4));
-                        // O^T block j; the item's token half h (bf16 items are 64 tokens)
-                        const int j = F8 ? v : v >> 1, h = F8 ? 0 : v & 1;
+                        const uint64_t da = dv0 + (uint64_t)(slot * (F::v_slot >> 4));
+                        // O^T block j; the item's first token h within the tile
+                        const int j = v / F::v_per_block, h = (v % F::v_per_block) * F::v_tokens;
                         // each MMA takes 16 (bf16) or 32 (E4M3) tokens: 2 or 4 row groups
                         constexpr int k_tok = F8 ? 32 : 16;
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
+                        for (int kk = 0; kk < F::v_tokens / k_tok; ++kk)
                             mma<F8>(tmem + 64 * j, da + (uint64_t)((k_tok * 128 >> 4) * kk),
-                                    dp0 + (uint64_t)(((64 * h + k_tok * kk) * L::p_row) >> 4),
+                                    dp0 + (uint64_t)(((h + k_tok * kk) * L::p_row) >> 4),
                                     idesc_pv, (i | h | kk) != 0);
                         mma_commit(bar_empty_v + 8 * slot);
                         issued = true;
@@ -1097,7 +1135,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 const int t = t_base + tok;
                 const bool tile_visible = t_base + kTile <= vis_all;
                 const uint32_t b = gt & 1;
-                const uint32_t s_col = kTmemS + 64 * b + col0;
+                const uint32_t s_col = kTmemS + F::s_stride * b + col0;
                 // warp-uniform, because tcgen05.ld below is a .sync.aligned instruction
                 const bool got = __all_sync(
                     0xffffffffu, wait_bounded(bar_s + 8 * b, (gt >> 1) & 1, abort_flag, a.status, 7));
@@ -1105,8 +1143,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 bool exceed = false;
                 if (got) {
                     tc_fence_after();
-                    load_scores<CH, F8>(tmem + t_lane + s_col, a.scale_log2, cf_addr, tile_visible,
-                                        t, seg.z, vis_all, row0 + col0, a.num_heads, x);
+                    load_scores<CH, F8>(tmem + t_lane + s_col, NG, a.scale_log2, cf_addr,
+                                        tile_visible, t, seg.z, vis_all, row0 + col0, a.num_heads, x);
                     exceed = shift_and_test<CH, F8>(x, m_addr);
                 }
                 if (softmax_bar_or(exceed || !got || *abort_flag)) {
@@ -1168,8 +1206,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                             tmem_wait_st();
                         }
                     }
-                    load_scores<CH, F8>(tmem + t_lane + s_col, a.scale_log2, cf_addr, tile_visible,
-                                        t, seg.z, vis_all, row0 + col0, a.num_heads, x);
+                    load_scores<CH, F8>(tmem + t_lane + s_col, NG, a.scale_log2, cf_addr,
+                                        tile_visible, t, seg.z, vis_all, row0 + col0, a.num_heads, x);
                     shift_and_test<CH, F8>(x, m_addr);
                 }
                 // this S^T buffer may now be overwritten by the tile after next
@@ -1369,7 +1407,8 @@ bool kv_maps(const DecodeArgs &a, bool f8, KvMaps *out)
     // one box row is 128 bytes: 64 bf16 or 128 E4M3 columns
     const cuuint32_t cols = f8 ? 128 : 64;
     const cuuint32_t kv_box[3] = {cols, (cuuint32_t)kTile, 1};
-    const cuuint32_t v_box[3] = {cols, f8 ? (cuuint32_t)kTile : 64u, 1};
+    const cuuint32_t v_box[3] = {cols, (cuuint32_t)(f8 ? Fmt<true>::v_tokens : Fmt<false>::v_tokens),
+                                 1};
     KvMaps m;
     if (!make_map(&m.kv, dt, a.slab, 3, dims, strides, kv_box) ||
         !make_map(&m.v, dt, a.slab, 3, dims, strides, v_box))
@@ -1390,15 +1429,15 @@ bool kv_maps(const DecodeArgs &a, bool f8, KvMaps *out)
     return true;
 }
 
-// Query maps: bf16 q_nope (64-column boxes) and q_rope, or the quantised E4M3
-// rows [R*n_q*H, 576]: 128-byte boxes for the latent, a 64-byte box (64-byte
-// swizzle) for the rope.
+// Query maps: bf16 q_nope (64-column boxes) and q_rope, or the two-part E4M3
+// rows [2 * R*n_q*H, 576] (hi plane, then lo plane): 128-byte boxes for the
+// latent, a 64-byte box (64-byte swizzle) for the rope.
 template <int NG>
 bool q_maps(const DecodeArgs &a, bool f8, CUtensorMap *qn, CUtensorMap *qr)
 {
     const cuuint64_t rows = (cuuint64_t)a.num_reqs * a.rows_per_req;
     if (f8) {
-        const cuuint64_t q_dims[2] = {(cuuint64_t)kRow, rows};
+        const cuuint64_t q_dims[2] = {(cuuint64_t)kRow, 2 * rows};
         const cuuint64_t q_strides[1] = {(cuuint64_t)kRow};
         const cuuint32_t q_box[2] = {128, (cuuint32_t)NG};
         const cuuint32_t r_box[2] = {64, (cuuint32_t)NG};

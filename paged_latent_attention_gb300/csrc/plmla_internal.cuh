@@ -40,7 +40,7 @@ struct PlanBuffers {
     // FP8 decode: extra CTAs of the plan grid quantise the queries (null: none)
     const __nv_bfloat16 *q_nope; // [q_rows, 512]
     const __nv_bfloat16 *q_rope; // [q_rows, 64]
-    uint8_t *q8;                 // [q_rows, 576] E4M3 codes of q * 2^-e
+    uint8_t *q8;                 // [2, q_rows, 576] E4M3 hi and lo parts of q * 2^-e
     int32_t *qexp;               // [q_rows] e
     int32_t q_rows;
 };
@@ -71,7 +71,7 @@ struct DecodeArgs {
     // read as E4M3 codes q8 with per-row exponents qexp (written by the plan grid)
     int32_t fp8;
     float kv_scale;
-    const uint8_t *q8;             // [R*n_q*H, 576]
+    const uint8_t *q8;             // [2, R*n_q*H, 576]: hi plane, then lo plane
     const int32_t *qexp;           // [R*n_q*H]
 };
 
@@ -92,7 +92,8 @@ size_t plan_smem_bytes();
 cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int members,
                         PlanBuffers plan, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream);
-// The FP8 decode's query quantiser as a kernel of its own (rows of 576 values).
+// The FP8 decode's query quantiser as a kernel of its own (rows of 576 values;
+// q8 holds the hi plane, then the lo plane).
 cudaError_t launch_quantize(const __nv_bfloat16 *q_nope, const __nv_bfloat16 *q_rope, int rows,
                             uint8_t *q8, int32_t *qexp, cudaStream_t stream);
 // KV append (plmla_append.cu): status codes it writes for a bad row.

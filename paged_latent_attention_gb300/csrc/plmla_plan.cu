@@ -161,13 +161,51 @@ __device__ __forceinline__ int chunk_mid2(int cost0, int tiles, int chunk_tiles,
                   : 2 * cost0 + 2 * kSegmentCostTiles + 2 * s * chunk_tiles + t;
 }
 
+// Two E4M3 values (low byte first) widened exactly to floats.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    float lo, hi;
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\t"
+        "cvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+    return make_float2(lo, hi);
+}
+
+// The remainder v - decode(hi) of one scaled value: exact in fp32 (v and
+// decode(hi) are within a factor of two, or decode(hi) is zero).  A nonzero q
+// whose scaled value underflowed fp32 has the exact remainder v itself, a tiny
+// number of q's sign, whose E4M3 code is q's signed zero.
+__device__ __forceinline__ float remainder_of(float q, float v, float hi)
+{
+    return (v == 0.f && q != 0.f) ? copysignf(0.f, q) : v - hi;
+}
+
+// E4M3 codes of four values times p2 as one word (hi part), and the E4M3 codes
+// of their remainders (lo part); both round to nearest even.
+__device__ __forceinline__ void split4(const float *q, float p2, uint32_t &hi, uint32_t &lo)
+{
+    const float a = q[0] * p2, b = q[1] * p2, c = q[2] * p2, d = q[3] * p2;
+    const uint16_t h0 = e4m3x2(a, b), h1 = e4m3x2(c, d);
+    const float2 f0 = e4m3x2_to_float2(h0), f1 = e4m3x2_to_float2(h1);
+    hi = (uint32_t)h0 | ((uint32_t)h1 << 16);
+    lo = (uint32_t)e4m3x2(remainder_of(q[0], a, f0.x), remainder_of(q[1], b, f0.y)) |
+         ((uint32_t)e4m3x2(remainder_of(q[2], c, f1.x), remainder_of(q[3], d, f1.y)) << 16);
+}
+
 // FP8 queries for the FP8 decode (its tensor-core kind multiplies E4M3 by E4M3):
-// row i of [q_nope | q_rope] (576 values) becomes the E4M3 codes of q * 2^-e,
-// with e the smallest exponent for which max |q| * 2^-e <= 448 (E4M3's largest
-// finite value), at least -126, and 0 for an all-zero row.  The scaling by a
-// power of two is exact; the conversion rounds to nearest even.  One warp per
-// row: lane l takes latent values [16 l, 16 l + 16) and, for l < 8, rope values
-// [8 l, 8 l + 8).
+// row i of [q_nope | q_rope] (576 values) is scaled to v = q * 2^-e, with e the
+// smallest exponent for which max |q| * 2^-e <= 448 (E4M3's largest finite
+// value), at least -126, and 0 for an all-zero row; the scaling by a power of
+// two is exact.  v enters as two E4M3 parts: hi = E4M3(v) (plane 0 of q8) and
+// lo = E4M3(v - hi) (plane 1, rows q_rows further on).  v has bf16's 8
+// significant bits, hi keeps 4 and the remainder's at most 4 others fit lo
+// exactly while |v| >= 2^-2 (below it lo is subnormal, off by at most 2^-10),
+// so the decode's scores use the bf16 query itself, up to that last bit.  One
+// warp per row: lane l takes latent values [16 l, 16 l + 16) and, for l < 8,
+// rope values [8 l, 8 l + 8).
 __device__ void quantize_queries(const PlanBuffers &plan, int cta)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -205,19 +243,22 @@ __device__ void quantize_queries(const PlanBuffers &plan, int cta)
             }
         }
         const float p2 = __uint_as_float((uint32_t)(127 - e) << 23);   // 2^-e, exact
-        uint32_t out[4], rope_out[2];
+        uint32_t hi[4], lo[4], rope_hi[2], rope_lo[2];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-            out[i] = (uint32_t)e4m3x2(v[4 * i] * p2, v[4 * i + 1] * p2) |
-                     ((uint32_t)e4m3x2(v[4 * i + 2] * p2, v[4 * i + 3] * p2) << 16);
+            split4(v + 4 * i, p2, hi[i], lo[i]);
 #pragma unroll
         for (int i = 0; i < 2; ++i)
-            rope_out[i] = (uint32_t)e4m3x2(v[16 + 4 * i] * p2, v[16 + 4 * i + 1] * p2) |
-                          ((uint32_t)e4m3x2(v[16 + 4 * i + 2] * p2, v[16 + 4 * i + 3] * p2) << 16);
+            split4(v + 16 + 4 * i, p2, rope_hi[i], rope_lo[i]);
         uint8_t *dst = plan.q8 + (int64_t)row * kRow;
-        *reinterpret_cast<uint4 *>(dst + 16 * lane) = make_uint4(out[0], out[1], out[2], out[3]);
-        if (lane < 8)
-            *reinterpret_cast<uint2 *>(dst + kLatent + 8 * lane) = make_uint2(rope_out[0], rope_out[1]);
+        uint8_t *dst_lo = plan.q8 + ((int64_t)plan.q_rows + row) * kRow;
+        *reinterpret_cast<uint4 *>(dst + 16 * lane) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(dst_lo + 16 * lane) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        if (lane < 8) {
+            *reinterpret_cast<uint2 *>(dst + kLatent + 8 * lane) = make_uint2(rope_hi[0], rope_hi[1]);
+            *reinterpret_cast<uint2 *>(dst_lo + kLatent + 8 * lane) =
+                make_uint2(rope_lo[0], rope_lo[1]);
+        }
         if (lane == 0)
             plan.qexp[row] = e;
     }

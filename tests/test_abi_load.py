@@ -129,9 +129,9 @@ def test_query_token_limit_and_fp8_arguments(lib):
     assert lib.mla_split_budget(4, 256, 64, 152, 1) > 0
     assert lib.mla_split_budget(4, 257, 64, 152, 1) == -1
     assert lib.mla_workspace_size_fp8(4, 257, 64, 152, 1) == 0
-    # the FP8 workspace adds the quantised queries: 576 bytes and an exponent per row
+    # the FP8 workspace adds the two-part queries: 2 x 576 bytes and an exponent per row
     extra = lib.mla_workspace_size_fp8(64, 1, 64, 152, 1) - lib.mla_workspace_size(64, 1, 64, 152, 1)
-    assert extra >= 64 * 64 * (576 + 4)
+    assert 64 * 64 * (2 * 576 + 4) <= extra < 64 * 64 * (2 * 576 + 4) + 1024
     fake = 1 << 20
 
     def fp8(stride=1536 * 576, kv_scale=0.5):
