@@ -61,6 +61,12 @@ def parse_args(argv=None):
                          "(the deployment's FP8 cache, 576 bytes per token row)")
     ap.add_argument("--workload", default="long",
                     choices=["tiny", "steady", "agentic", "spec", "long", "extend"])
+    ap.add_argument("--split", choices=["per-request", "uniform"], default="per-request",
+                    help="split rule of the planner: per-request split counts (the library's "
+                         "default) or the uniform baseline the pages compare it with")
+    ap.add_argument("--control", action="store_true",
+                    help="the workload's equal-length control: same requests and total KV "
+                         "tokens, every history at the average length")
     ap.add_argument("--layers", type=int, default=None,
                     help="decode only the first N layer slabs of a multi-layer workload: a "
                          "smaller case of the same per-layer launch for ncu captures (each "
@@ -342,6 +348,9 @@ def run_gpu(args):
     dist = dist_init(world, "nccl")
 
     w = inputs.make_workload(args.workload)
+    if args.control:
+        w = inputs.equal_length_control(w)
+    plmla.set_split_mode(args.split)
     if args.layers is not None:
         if not 1 <= args.layers <= w.num_slabs:
             raise SystemExit(f"--layers must lie in [1, {w.num_slabs}]")
@@ -466,7 +475,7 @@ def run_gpu(args):
                    "n_q": w.n_q, "heads": w.num_heads, "layers": layers,
                    "kv_tokens": w.kv_tokens, "kv_bytes_per_step": kv_bytes_step,
                    "l2": "inputs larger than L2 (KV per step >> 129 MB L2), no flush",
-                   "parallelism": f"replicas x{world}"},
+                   "split": args.split, "parallelism": f"replicas x{world}"},
         "pct_of_hbm_peak": 100.0 * value / world / peak,
         "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
         "request_steps_per_s": w.num_reqs * world / (max_ms / K / 1e3),
@@ -809,6 +818,8 @@ def run_reference(args):
     import oracle
     from paged_latent_attention_gb300 import inputs
     w = inputs.make_workload(args.workload)
+    if args.control:
+        w = inputs.equal_length_control(w)
     fp8 = args.kv == "fp8"
     kv_scale = KV_SCALE_FP8 if fp8 else None
     qn, qr, gate = inputs.make_queries(w, "cpu")

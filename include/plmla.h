@@ -110,6 +110,24 @@ void mla_set_page_checks(int32_t on);
 int32_t mla_get_page_checks(void);
 
 /*
+ * mla_set_split_mode -- process-wide choice of the split rule that mla_decode,
+ * mla_decode_fp8 and mla_plan_splits plan with (not part of the method's
+ * default; it exists to reproduce the comparison of [AX, Figure 5]):
+ *   0  per-request split counts [AX, Figure 4] (the default, see mla_plan_splits)
+ *   1  uniform split counts, the baseline that figure compares against: every
+ *      request with history gets su = split_budget / (requests with history)
+ *      chunks (at least 1), so request r's chunk is ceil(L_r / su) rounded up to
+ *      a multiple of 128 and splits_r = ceil(L_r / that chunk)
+ * The environment variable PLMLA_SPLIT_MODE=uniform selects 1 when the library
+ * loads.  The decode's outputs agree under both rules within rounding (the
+ * partial states merge to the same softmax); under 1, mla_plan_splits writes
+ * split_chunk = 0 (the chunk differs per request).  Returns
+ * PLMLA_INVALID_ARGUMENT for another mode.  mla_get_split_mode returns it.
+ */
+plmla_status mla_set_split_mode(int32_t mode);
+int32_t mla_get_split_mode(void);
+
+/*
  * mla_plan_splits -- per-request KV split plan [AX, Figure 4], on the device.
  *
  *   chunk     = ceil(sum_r L_r / split_budget) rounded up to a multiple of 128,
@@ -391,6 +409,38 @@ plmla_status mla_split_combine(const float *o_part, const float *lse_part,
  */
 plmla_status mla_merge_partials(const void *out_parts, const float *lse_parts, int32_t world,
                                 int64_t rows, void *out, float *lse, void *stream);
+
+/*
+ * mla_dcp_shard -- one rank's part of every request's history for decode
+ * context parallelism over `world` ranks [AX, "AgentX benchmark results": the
+ * ranks decode parts of the context and combine partial attention results].
+ * Page column c of request r (its tokens [1536 c, 1536 (c + 1)) of the
+ * history) belongs to rank (c + r) mod world: every rank holds the same number
+ * of a request's pages up to one, and the rotation by r spreads the leftover
+ * pages over the ranks.  For rank `rank` this writes, per request, the page IDs
+ * of its columns in column order into table_out row r, and into lens_out[r]
+ * the tokens they hold (1536 per page; the request's last page, if this rank
+ * holds it, only its L - 1536 (n - 1) tokens).  mla_decode on (table_out,
+ * lens_out) with single-token queries then gives the rank's gated part (the
+ * order of the tokens does not change the softmax), and mla_merge_partials of
+ * the ranks' parts gives mla_decode over the whole history.
+ *
+ * page_table    int32, row r at page_table + r * page_table_ld (as mla_decode);
+ *               columns 0 .. ceil(L_r / 1536) - 1 are read, at most
+ *               page_table_ld of them (a longer history keeps the row's pages)
+ * seq_lens      int32 [num_reqs], num_reqs 1 .. 1024
+ * world         1 .. 4096; rank in [0, world)
+ * table_out     int32 [num_reqs, table_out_ld], table_out_ld >=
+ *               ceil(page_table_ld / world); entries past a row's page count are
+ *               not written
+ * lens_out      int32 [num_reqs], written
+ * Device pointers; asynchronous on `stream`; reads nothing back.  Returns
+ * PLMLA_INVALID_ARGUMENT for null or misaligned pointers and bad sizes.
+ */
+plmla_status mla_dcp_shard(const int32_t *page_table, int64_t page_table_ld,
+                           const int32_t *seq_lens, int32_t num_reqs, int32_t world, int32_t rank,
+                           int32_t *table_out, int64_t table_out_ld, int32_t *lens_out,
+                           void *stream);
 
 /*
  * mla_kv_append -- write each request's new latent and rope rows into the flat

@@ -17,6 +17,7 @@ from .oracle import (  # noqa: F401
     mla_decode_e4m3_reference,
     mla_decode_reference,
     plan_splits,
+    plan_splits_uniform,
     quantize_query_rows,
     query_scale_exponent,
 )

@@ -287,6 +287,29 @@ def plan_splits(seq_lens, budget: int, tile: int):
     return chunk, [_ceil_div(L, chunk) if L > 0 else 0 for L in lens]
 
 
+def plan_splits_uniform(seq_lens, budget: int, tile: int):
+    """The uniform baseline of the same section (Figure 4, left panel; the
+    comparison of Figure 5): every request with history gets the same number of
+    chunks, su = budget // (requests with history), at least 1.  Returns
+    (chunks, splits): request r's chunk ceil(L_r / su) rounded up to the tile,
+    and its split count ceil(L_r / chunk_r) (0 and 0 for L_r = 0)."""
+    lens = [int(x) for x in seq_lens]
+    if budget < 1 or tile < 1:
+        raise ValueError("budget and tile must be positive")
+    live = sum(1 for L in lens if L > 0)
+    su = max(1, budget // max(1, live))
+    chunks, splits = [], []
+    for L in lens:
+        if L == 0:
+            chunks.append(0)
+            splits.append(0)
+            continue
+        c = _ceil_div(_ceil_div(L, su), tile) * tile
+        chunks.append(c)
+        splits.append(_ceil_div(L, c))
+    return chunks, splits
+
+
 # --------------------------------------------------------------------------
 # KV append (vLLM blog "Kimi K3 Inference Backend Evolution", section "State
 # Overwrite: How KDA Breaks Traditional KV Cache", the append-only contract of

@@ -8,6 +8,8 @@ from .api import (  # noqa: F401
     allocate_workspace,
     device_status,
     get_page_checks,
+    get_split_mode,
+    mla_dcp_shard,
     mla_decode,
     mla_decode_fp8,
     mla_kv_append,
@@ -20,4 +22,5 @@ from .api import (  # noqa: F401
     mla_workspace_size,
     mla_workspace_size_fp8,
     set_page_checks,
+    set_split_mode,
 )

@@ -41,7 +41,10 @@ SIGNATURES = {
                                          _p, _p]),
     "mla_quantize_queries_fp8": (ctypes.c_int, [_p, _p, _i64, _p, _p, _p]),
     "mla_merge_partials": (ctypes.c_int, [_p, _p, _i32, _i64, _p, _p, _p]),
+    "mla_dcp_shard": (ctypes.c_int, [_p, _i64, _p, _i32, _i32, _i32, _p, _i64, _p, _p]),
     "mla_set_page_checks": (None, [_i32]),
+    "mla_set_split_mode": (ctypes.c_int, [_i32]),
+    "mla_get_split_mode": (_i32, []),
     "mla_get_page_checks": (_i32, []),
 }
 

@@ -205,6 +205,22 @@ def get_page_checks() -> bool:
     return bool(_native.lib().mla_get_page_checks())
 
 
+SPLIT_MODES = {"per-request": 0, "uniform": 1}
+
+
+def set_split_mode(mode: str) -> None:
+    """Process-wide split rule of the planner: "per-request" (the default) or
+    "uniform" (the same split count for every request, the baseline of the
+    pages' Figure 5 comparison)."""
+    _require(mode in SPLIT_MODES, f"split mode must be one of {sorted(SPLIT_MODES)}")
+    _native.check(_native.lib().mla_set_split_mode(SPLIT_MODES[mode]), "mla_set_split_mode")
+
+
+def get_split_mode() -> str:
+    m = int(_native.lib().mla_get_split_mode())
+    return {v: k for k, v in SPLIT_MODES.items()}[m]
+
+
 def device_status(workspace) -> int:
     """The decode kernel's status word from the workspace of the last step
     (0 = ok).  Reads device memory: synchronises with the workspace's stream."""
@@ -223,6 +239,28 @@ def mla_plan_splits(seq_lens, split_budget, stream=None):
                                            _stream_ptr(stream, seq_lens.device))
     _native.check(status, "mla_plan_splits")
     return indptr, chunk
+
+
+def mla_dcp_shard(page_table, seq_lens, world, rank, stream=None):
+    """Rank `rank`'s page table and history lengths for decode context
+    parallelism over `world` ranks (page column c of request r belongs to rank
+    (c + r) mod world): (table_k [R, ceil(ld / world)] int32, lens_k [R] int32),
+    computed on the device."""
+    _require(page_table.is_cuda and page_table.dtype == torch.int32 and page_table.dim() == 2
+             and page_table.stride(1) == 1, "page_table must be a CUDA int32 [R, ld] view")
+    _require(seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous(),
+             "seq_lens must be a contiguous CUDA int32 vector")
+    R = seq_lens.shape[0]
+    ld = page_table.stride(0)
+    out_ld = max(1, -(-ld // world))
+    table_k = torch.empty(R, out_ld, dtype=torch.int32, device=page_table.device)
+    lens_k = torch.empty(R, dtype=torch.int32, device=page_table.device)
+    _native.check(_native.lib().mla_dcp_shard(page_table.data_ptr(), ld, seq_lens.data_ptr(), R,
+                                              int(world), int(rank), table_k.data_ptr(), out_ld,
+                                              lens_k.data_ptr(),
+                                              _stream_ptr(stream, page_table.device)),
+                  "mla_dcp_shard")
+    return table_k, lens_k
 
 
 def mla_split_combine(o_part, lse_part, split_indptr, gate, *, n_q=1, out=None, lse=None,

@@ -29,6 +29,7 @@ SOURCES = [
     "plmla_static_scratch.cu",
     "plmla_append.cu",
     "plmla_check.cu",
+    "plmla_dcp.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",

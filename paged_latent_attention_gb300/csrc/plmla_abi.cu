@@ -23,6 +23,10 @@ cudaError_t launch_check_pages(const int32_t *seq_lens, int num_reqs, const int3
 cudaError_t launch_merge_partials(const __nv_bfloat16 *parts, const float *lse_parts, int world,
                                   int64_t rows, __nv_bfloat16 *out, float *lse,
                                   cudaStream_t stream);
+// plmla_dcp.cu: one rank's page-table rows and history lengths.
+cudaError_t launch_dcp_shard(const int32_t *table, int64_t ld, const int32_t *lens, int num_reqs,
+                             int world, int rank, int32_t *table_out, int64_t out_ld,
+                             int32_t *lens_out, cudaStream_t stream);
 }  // namespace plmla
 
 namespace {
@@ -39,6 +43,15 @@ bool env_on(const char *name)
 }
 int initial_page_checks() { return env_on("PLMLA_CHECK_PAGES") || env_on("PLMLA_DEBUG"); }
 std::atomic<int> g_page_checks{initial_page_checks()};   // set and read from any host thread
+
+// Split rule of the planner: 0 = per-request (default), 1 = uniform split counts;
+// PLMLA_SPLIT_MODE=uniform in the environment selects 1 when the library loads.
+int initial_split_mode()
+{
+    const char *v = getenv("PLMLA_SPLIT_MODE");
+    return (v != nullptr && v[0] == 'u') ? 1 : 0;
+}
+std::atomic<int> g_split_mode{initial_split_mode()};
 
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
@@ -202,7 +215,8 @@ extern "C" plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_req
     PlanBuffers plan = {};
     plan.indptr = split_indptr;
     plan.chunk = split_chunk;
-    cudaError_t err = launch_plan(seq_lens, num_reqs, split_budget, 1, plan,
+    cudaError_t err = launch_plan(seq_lens, num_reqs, split_budget, 1,
+                                  g_split_mode.load(std::memory_order_relaxed), plan,
                                   static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
 }
@@ -215,6 +229,19 @@ extern "C" void mla_set_page_checks(int32_t on)
 extern "C" int32_t mla_get_page_checks(void)
 {
     return g_page_checks.load(std::memory_order_relaxed);
+}
+
+extern "C" plmla_status mla_set_split_mode(int32_t mode)
+{
+    if (mode != 0 && mode != 1)
+        return PLMLA_INVALID_ARGUMENT;
+    g_split_mode.store(mode, std::memory_order_relaxed);
+    return PLMLA_OK;
+}
+
+extern "C" int32_t mla_get_split_mode(void)
+{
+    return g_split_mode.load(std::memory_order_relaxed);
 }
 
 extern "C" plmla_status mla_merge_partials(const void *out_parts, const float *lse_parts,
@@ -231,6 +258,23 @@ extern "C" plmla_status mla_merge_partials(const void *out_parts, const float *l
                                             lse_parts, world, rows,
                                             static_cast<__nv_bfloat16 *>(out), lse,
                                             static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
+}
+
+extern "C" plmla_status mla_dcp_shard(const int32_t *page_table, int64_t page_table_ld,
+                                      const int32_t *seq_lens, int32_t num_reqs, int32_t world,
+                                      int32_t rank, int32_t *table_out, int64_t table_out_ld,
+                                      int32_t *lens_out, void *stream)
+{
+    if (page_table == nullptr || seq_lens == nullptr || table_out == nullptr ||
+        lens_out == nullptr || num_reqs < 1 || num_reqs > kMaxReqs || world < 1 ||
+        world > 4096 || rank < 0 || rank >= world || page_table_ld < 1 ||
+        table_out_ld < (page_table_ld + world - 1) / world || !aligned(page_table, 4) ||
+        !aligned(seq_lens, 4) || !aligned(table_out, 4) || !aligned(lens_out, 4))
+        return PLMLA_INVALID_ARGUMENT;
+    const cudaError_t err = launch_dcp_shard(page_table, page_table_ld, seq_lens, num_reqs, world,
+                                             rank, table_out, table_out_ld, lens_out,
+                                             static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
 }
 
@@ -333,7 +377,8 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     const plmla_stage_events &ev = events != nullptr ? *events : none;
     if (record(ev.plan_begin, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
-    cudaError_t err = launch_plan(seq_lens, num_reqs, sh.budget, sh.members, plan, s);
+    cudaError_t err = launch_plan(seq_lens, num_reqs, sh.budget, sh.members,
+                                  g_split_mode.load(std::memory_order_relaxed), plan, s);
     if (err != cudaSuccess || record(ev.decode_begin, s) != cudaSuccess)
         return PLMLA_CUDA_ERROR;
 

@@ -21,12 +21,13 @@
 // tensor map [page][token][576] over the slab: page IDs come from the page
 // table with the table's row stride, and the page offset is 64-bit inside the
 // TMA unit (pools above 2 GB; AgentX - InferenceXv3 report, ROCm AITER section).
-// Shared memory holds Q^T (9 x NG x 128 B), the probability tile P^T, and two
-// rings of 16 KB slots through which every tile streams twice:
+// Shared memory holds Q^T (bf16: 9 x NG x 128 B), the probability tile P^T,
+// and two rings of 16 KB slots through which every tile streams twice:
 //   K ring: the nine 128 x 64 column blocks of the tile, for S^T (from HBM);
 //   V ring: eight 64-token x 128-latent blocks of the same tile, for O^T
 //           (a re-read that hits L2), each covering both 64-column halves of
 //           one 128-row O^T block.
+// (E4M3 pages: see Fmt below.)
 // S^T and P^T V are issued by two threads in different warps: at M = 128,
 // N <= 64 a single issuing thread cannot keep the tensor pipe busy.  S^T is
 // double-buffered in TMEM, so S^T of tile i+1 runs while the softmax of tile i
@@ -36,8 +37,7 @@
 // TMEM owner, warps 2..9 = softmax (two warps per TMEM lane quadrant, each with
 // half of a token's query-row columns; the same threads write the partial
 // output, one thread per latent row of O^T and column half), warp 10 = V
-// producer (it also zeroes, in the request's last partial tile, the latent
-// rows past the history before releasing the item), warp 11 = P^T V issuer.
+// producer, warp 11 = P^T V issuer.
 // Two softmax warps per SM sub-partition keep the dependent softmax arithmetic
 // from exposing its full latency.
 //
@@ -50,8 +50,10 @@
 // <= 2^kTau stays finite in bf16.
 //
 // Tokens at or past the chunk end (the request's last, partial tile) are
-// masked in the scores and their latent rows are zeroed in the V items before
-// P^T V, so stale or NaN page contents never reach the output.
+// masked in the scores (probability 0), and the V producer loads only the
+// item rows inside the history: the slot rows past it keep what the slot held
+// before, zeros written at kernel start or earlier history rows, finite either
+// way, so stale or NaN page contents never reach the output (0 * NaN would).
 //
 // Every mbarrier wait is bounded: after kWaitLimitNs the waiting thread sets
 // the workspace status word and a CTA-wide abort flag, the producer waits (with

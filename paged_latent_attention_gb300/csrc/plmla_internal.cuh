@@ -89,8 +89,10 @@ inline int group_rows_for(int rows)
 }
 
 size_t plan_smem_bytes();
+// uniform != 0: every request with history gets budget / (such requests) splits
+// (the uniform baseline of the split rule), else the per-request rule.
 cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int members,
-                        PlanBuffers plan, cudaStream_t stream);
+                        int uniform, PlanBuffers plan, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream);
 // The FP8 decode's query quantiser as a kernel of its own (rows of 576 values;
 // q8 holds the hi plane, then the lo plane).

@@ -7,6 +7,9 @@
 // chunks do not fit the budget, chunk grows (the smallest multiple of kTile
 // that fits, found by a parallel search because the chunk count only falls as
 // the chunk grows), never beyond the longest history rounded up to kTile.
+// Uniform mode (the baseline of that section's Figure 5 comparison): every
+// request with history gets the same split count su = budget / (requests with
+// history), so request r's chunk is ceil(L_r / su) rounded up to kTile.
 //
 // Schedule (the GB300 side): the decode kernel runs one persistent CTA per SM.
 // The chunks, in request order, are dealt out as contiguous runs so that every
@@ -44,6 +47,7 @@ struct PlanSmem {
     int cost0[kMaxReqs + 1];     // exclusive prefix of request cost (tiles + start charge)
     int lastm[kMaxReqs];         // running max of each request's last-chunk doubled midpoint
     int nonempty[kMaxReqs + 1];  // exclusive prefix of requests with at least one chunk
+    int ctile[kMaxReqs];         // chunk length of each request, in tiles
     int first[kMaxSms + 1];      // first chunk of each member (members + 1 entries)
     int nseg[kMaxSms + 1];       // exclusive prefix of segments per member
     long long red64[kPlanWarps];
@@ -266,7 +270,7 @@ __device__ void quantize_queries(const PlanBuffers &plan, int cta)
 
 __global__ void __launch_bounds__(kPlanThreads, 1)
 plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int members,
-            PlanBuffers plan)
+            int uniform, PlanBuffers plan)
 {
     extern __shared__ __align__(16) unsigned char plan_smem_raw[];
     PlanSmem &sm = *reinterpret_cast<PlanSmem *>(plan_smem_raw);
@@ -287,7 +291,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     const int r0 = tid * kReqPerThread;
     int L[kReqPerThread];
     long long local_sum = 0;
-    int local_max = 0;
+    int local_max = 0, local_live = 0;
 #pragma unroll
     for (int k = 0; k < kReqPerThread; ++k) {
         const int r = r0 + k;
@@ -296,6 +300,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
             sm.lens[r] = L[k];
         local_sum += L[k];
         local_max = max(local_max, L[k]);
+        local_live += L[k] > 0 ? 1 : 0;
     }
     // finished-segment counters of this call's decode start from zero
     if (plan.done != nullptr)
@@ -303,10 +308,13 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
             plan.done[i] = 0;
     const long long total = block_sum64(local_sum, sm.red64);   // also publishes sm.lens
     const int longest_len = block_max32(local_max, sm.red32);
+    const int live = (int)block_sum64(local_live, sm.red64);
+    // uniform mode: split count of every request with history
+    const long long su = max(1, budget / max(1, live));
 
-    // ---- chunk length
+    // ---- chunk length (per-request mode)
     long long chunk = kTile;
-    if (total > 0) {
+    if (total > 0 && !uniform) {
         const long long c0 = (((total + budget - 1) / budget + kTile - 1) / kTile) * kTile;
         const long long longest = ((longest_len + kTile - 1) / (long long)kTile) * kTile;
         chunk = c0;
@@ -344,14 +352,22 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
             chunk = c0 + (long long)lo * kTile;
         }
     }
-    const int chunk_tiles = (int)(chunk / kTile);
 
-    // ---- per request: chunks, tiles, cost (tiles plus the start charge); prefixes
-    int ns[kReqPerThread], nt[kReqPerThread];
+    // ---- per request: chunk length, chunks, tiles, cost (tiles plus the start
+    // charge); prefixes
+    int ns[kReqPerThread], nt[kReqPerThread], ct[kReqPerThread];
     int my_chunks = 0, my_cost = 0, my_nonempty = 0;
 #pragma unroll
     for (int k = 0; k < kReqPerThread; ++k) {
-        ns[k] = (int)((L[k] + chunk - 1) / chunk);
+        long long c = chunk;
+        if (uniform) {
+            const long long per = (L[k] + su - 1) / su;
+            c = max(1LL, (per + kTile - 1) / kTile) * kTile;
+        }
+        ct[k] = (int)(c / kTile);
+        if (r0 + k < num_reqs)
+            sm.ctile[r0 + k] = ct[k];
+        ns[k] = (int)((L[k] + c - 1) / c);
         nt[k] = (L[k] + kTile - 1) / kTile;
         my_chunks += ns[k];
         my_cost += nt[k] + (ns[k] > 0 ? kSegmentCostTiles : 0);
@@ -367,7 +383,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
         int c = cost_run;
 #pragma unroll
         for (int k = 0; k < kReqPerThread; ++k) {
-            lm[k] = ns[k] > 0 ? chunk_mid2(c, nt[k], chunk_tiles, ns[k] - 1) : -1;
+            lm[k] = ns[k] > 0 ? chunk_mid2(c, nt[k], ct[k], ns[k] - 1) : -1;
             my_lm = max(my_lm, lm[k]);
             c += nt[k] + (ns[k] > 0 ? kSegmentCostTiles : 0);
         }
@@ -400,7 +416,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
     if (tid == 0) {
         if (plan.status != nullptr)
             *plan.status = 0;
-        *plan.chunk = chunk;
+        *plan.chunk = uniform ? 0 : chunk;
     }
     if (plan.segments == nullptr)
         return;
@@ -438,6 +454,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
                 const int nsr = sm.sb[r + 1] - sm.sb[r];
                 const int c = sm.cost0[r];
                 int s = 0;
+                const int chunk_tiles = sm.ctile[r];
                 if (!reaches(chunk_mid2(c, tiles, chunk_tiles, 0))) {
                     int a = 1, b = nsr - 1;   // the last chunk reaches
                     while (a < b) {
@@ -501,8 +518,9 @@ plan_kernel(const int32_t *__restrict__ seq_lens, int num_reqs, int budget, int 
             const int b = min(c1i, sm.sb[r + 1]) - sm.sb[r];
             int4 seg;
             seg.x = r;
-            seg.y = (int)(a * chunk);
-            seg.z = (int)min((long long)sm.lens[r], b * chunk);
+            const long long cr = (long long)sm.ctile[r] * kTile;
+            seg.y = (int)(a * cr);
+            seg.z = (int)min((long long)sm.lens[r], b * cr);
             seg.w = tid;
             plan.segments[id] = seg;
             ++id;
@@ -575,7 +593,7 @@ cudaError_t launch_quantize(const __nv_bfloat16 *q_nope, const __nv_bfloat16 *q_
 size_t plan_smem_bytes() { return sizeof(PlanSmem); }
 
 cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int members,
-                        PlanBuffers plan, cudaStream_t stream)
+                        int uniform, PlanBuffers plan, cudaStream_t stream)
 {
     const int smem = (int)sizeof(PlanSmem);
     cudaError_t err =
@@ -596,7 +614,8 @@ cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int m
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, num_reqs, budget, members, plan);
+    return cudaLaunchKernelEx(&cfg, plan_kernel, seq_lens, num_reqs, budget, members, uniform,
+                              plan);
 }
 
 }  // namespace plmla

@@ -1,23 +1,25 @@
 """Decode context parallelism: one request's history split across GPUs.
 
-Each of ``world`` ranks holds, for every request, a contiguous run of page-table
-columns -- pages [rank * S, (rank + 1) * S) -- and decodes only those tokens with
-mla_decode (its own plan, split decode and gated combine); one all-gather brings
-every rank's gated output and log-sum-exp together and mla_merge_partials merges
-them (TokenSpeed AgentX post, "AgentX benchmark results": decode context
-parallelism, ranks combine partial attention results).  This shards the KV
-pool's capacity and bandwidth for histories that one GPU cannot hold or stream
-fast enough, at the price of one exchange of T x H x (512 bf16 + 1 fp32) per rank.
+Each of ``world`` ranks holds, for every request, every world-th page of its
+history -- page column c of request r belongs to rank (c + r) mod world -- and
+decodes only those tokens with mla_decode (its own plan, split decode and gated
+combine); one all-gather brings every rank's gated output and log-sum-exp
+together and mla_merge_partials merges them (TokenSpeed AgentX post, "AgentX
+benchmark results": decode context parallelism, ranks combine partial attention
+results).  This shards the KV pool's capacity and bandwidth for histories that
+one GPU cannot hold or stream fast enough, at the price of one exchange of
+T x H x (512 bf16 + 1 fp32) per rank.
 
-The split is by page-table columns, identical for every request, so a rank's
-share is a plain strided view of the table and a clamp of the lengths, computed
-on the device (no host round trip per step).  Only single-token decode is
-sharded: with draft tokens the causal limit falls in the last rank's part only,
-which the per-rank decode cannot tell from a history that ends there.
+Dealing pages round-robin gives every rank the same number of a request's pages
+up to one, and rotating the first rank with the request spreads the leftover
+pages over the ranks, so the ranks stream nearly the same number of tokens
+(the softmax does not depend on the order of the tokens, so a rank's pages
+form one local history).  A rank's table rows and lengths are built on the
+device by mla_dcp_shard (no host round trip per step).  Only single-token
+decode is sharded: with draft tokens the causal limit falls on the request's
+last tokens, which one rank alone holds.
 """
 from __future__ import annotations
-
-import math
 
 import torch
 
@@ -26,39 +28,24 @@ from . import api
 PAGE_TOKENS = api.PAGE_TOKENS
 
 
-def pages_per_rank(table_cols: int, world: int) -> int:
-    """Page-table columns each rank owns (the last rank may own fewer)."""
-    if world < 1 or table_cols < 1:
-        raise ValueError("world and table columns must be positive")
-    return math.ceil(table_cols / world)
+def owner(column: int, request: int, world: int) -> int:
+    """The rank that holds page column `column` of request `request`."""
+    return (column + request) % world
 
 
-def shard_bounds(rank: int, world: int, table_cols: int, page_tokens: int = PAGE_TOKENS):
-    """Token range [t_lo, t_hi) of every request that rank `rank` decodes."""
+def shard_view(page_table, seq_lens, rank: int, world: int, stream=None):
+    """Rank `rank`'s page table ([R, ceil(ld / world)], its pages in column
+    order) and history lengths (device tensors, no synchronisation)."""
     if not 0 <= rank < world:
         raise ValueError("rank outside the group")
-    s = pages_per_rank(table_cols, world)
-    return rank * s * page_tokens, (rank + 1) * s * page_tokens
-
-
-def shard_view(page_table, seq_lens, rank: int, world: int, page_tokens: int = PAGE_TOKENS):
-    """Rank `rank`'s page table (a column view of the full one, same row stride)
-    and history lengths (device tensors, no synchronisation)."""
-    cols = page_table.shape[1]
-    s = pages_per_rank(cols, world)
-    first = rank * s
-    # a rank past the last column sees no tokens; any valid column start serves
-    table_k = page_table[:, min(first, cols - 1):]
-    t_lo, t_hi = shard_bounds(rank, world, cols, page_tokens)
-    lens_k = (seq_lens.to(torch.int64) - t_lo).clamp_(0, t_hi - t_lo).to(torch.int32)
-    return table_k, lens_k
+    return api.mla_dcp_shard(page_table, seq_lens, world, rank, stream=stream)
 
 
 def decode_shard(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, rank, world, *,
                  kv_scale=None, scale=api.DEFAULT_SCALE, workspace=None, stream=None):
     """Rank `rank`'s gated part (out_k, lse_k): mla_decode (mla_decode_fp8 when
-    `kv_scale` is given and the slab holds E4M3 codes) on its column view."""
-    table_k, lens_k = shard_view(page_table, seq_lens, rank, world)
+    `kv_scale` is given and the slab holds E4M3 codes) on its pages."""
+    table_k, lens_k = shard_view(page_table, seq_lens, rank, world, stream=stream)
     if kv_scale is None:
         return api.mla_decode(q_nope_absorbed, q_rope, gate, slab, table_k, lens_k, n_q=1,
                               scale=scale, workspace=workspace, stream=stream)

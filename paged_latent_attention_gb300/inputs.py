@@ -157,6 +157,26 @@ def make_workload(name: str) -> Workload:
     raise KeyError(name)
 
 
+def equal_length_control(w: Workload) -> Workload:
+    """The equal-length control of a workload (TokenSpeed AgentX post, section
+    "Balance MLA work with per-request KV splitting", the paragraph under
+    Figure 5): the same requests and the same total KV tokens, every history at
+    the batch's average length (the remainder of the division spread one token
+    each over the first requests); pool = pages needed + 10% free, scattered."""
+    total = w.kv_tokens
+    R = w.num_reqs
+    lens = np.full(R, total // R, dtype=np.int64)
+    lens[: total % R] += 1
+    lens = lens.astype(np.int32)
+    rng = np.random.Generator(np.random.PCG64([int(w.seed), 99]))
+    need = sum(_pages_for(lens, w.page_tokens))
+    pages = need + -(-need // 10)
+    table = _assign_pages(rng, lens, pages, w.page_tokens)
+    return Workload(w.name + "-control", R, w.n_q, w.num_heads, lens, table, pages,
+                    num_slabs=w.num_slabs, seed=w.seed, min_splits=w.min_splits,
+                    page_tokens=w.page_tokens, dc=w.dc, dr=w.dr)
+
+
 WORKLOAD_NAMES = ("tiny", "steady", "agentic", "spec", "long", "extend")
 
 

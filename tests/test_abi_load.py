@@ -165,3 +165,21 @@ def test_page_check_switch_reads_the_environment_at_load(lib, env, expect):
                          text=True, timeout=120, cwd=os.path.dirname(os.path.dirname(__file__)))
     assert out.returncode == 0, out.stderr
     assert out.stdout.split() == [str(expect), str(1 - expect)]
+
+
+@pytest.mark.parametrize("env,expect", [({}, 0), ({"PLMLA_SPLIT_MODE": "uniform"}, 1),
+                                        ({"PLMLA_SPLIT_MODE": "per-request"}, 0)])
+def test_split_mode_switch(lib, env, expect):
+    """Host logic only: the split rule's initial value comes from the
+    environment, the setter overrides it, and other modes are rejected."""
+    import os
+    import subprocess
+    import sys
+    clean = {k: v for k, v in os.environ.items() if k != "PLMLA_SPLIT_MODE"}
+    code = ("from paged_latent_attention_gb300 import _native; l = _native.lib(); "
+            "a = l.mla_get_split_mode(); r = l.mla_set_split_mode(1 - a); "
+            "bad = l.mla_set_split_mode(2); print(a, l.mla_get_split_mode(), r, bad)")
+    out = subprocess.run([sys.executable, "-c", code], env={**clean, **env}, capture_output=True,
+                         text=True, timeout=120, cwd=os.path.dirname(os.path.dirname(__file__)))
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.split() == [str(expect), str(1 - expect), "0", "1"]

@@ -1,10 +1,11 @@
 """Host logic of decode context parallelism (CPU, gloo, world sizes 2 and 3).
 
-Each rank takes its token range of every request from the same page-table
-column split the GPU path uses, computes its gated partial state with the
-oracle, and the ranks all-gather and merge; the merge of the gated parts must
-equal the oracle on the whole history (the gate is elementwise and the same for
-every part, so gated parts merge directly)."""
+Each rank takes the pages of every request that the GPU path gives it (page
+column c of request r belongs to rank (c + r) mod world), computes its gated
+partial state with the oracle (the merge of its pages' one-page windows), and
+the ranks all-gather and merge; the merge of the gated parts must equal the
+oracle on the whole history (the gate is elementwise and the same for every
+part, so gated parts merge directly)."""
 import os
 import socket
 import sys
@@ -38,16 +39,28 @@ def _attend(w, qn, qr, slab, t_lo=0, t_hi=None):
                               num_pages=w.num_pages, t_lo=t_lo, t_hi=t_hi, threads=2)
 
 
+def _rank_part(w, qn, qr, slab, rank, world):
+    """The oracle's partial state of `rank`'s pages: its one-page windows merged."""
+    import oracle
+    from paged_latent_attention_gb300 import dcp
+    rows_req = np.arange(w.num_reqs * w.num_heads) // w.num_heads
+    os_, ls_ = [], []
+    for c in range(w.page_table.shape[1]):
+        o, lse = _attend(w, qn, qr, slab, c * 1536, (c + 1) * 1536)
+        mine = np.array([dcp.owner(c, int(r), world) == rank for r in rows_req])
+        os_.append(o)
+        ls_.append(np.where(mine, lse, -np.inf))
+    return oracle.lse_merge(np.stack(os_), np.stack(ls_))
+
+
 def _worker(rank, world, port, results):
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     import torch.distributed as dist
     import oracle
-    from paged_latent_attention_gb300 import dcp
     dist.init_process_group("gloo", rank=rank, world_size=world)
     w, qn, qr, gate, slab = _problem()
-    t_lo, t_hi = dcp.shard_bounds(rank, world, w.page_table.shape[1])
-    o, lse = _attend(w, qn, qr, slab, t_lo, t_hi)
+    o, lse = _rank_part(w, qn, qr, slab, rank, world)
     g = np.asarray(gate.float().numpy(), dtype=np.float64).reshape(o.shape)
     part = torch.from_numpy(oracle.gate_sigmoid(o, g))
     parts = [torch.empty_like(part) for _ in range(world)]
@@ -61,10 +74,10 @@ def _worker(rank, world, port, results):
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("world", [2, 3, 5])
 def test_two_ranks_gather_and_merge_to_the_whole_history(world):
-    """world 3: four table columns split 2 + 2 + 0, so the last rank holds no
-    token of any request and contributes empty parts (lse = -inf, weight 0)."""
+    """world 5: the short histories have fewer pages than ranks, so some ranks
+    hold no token of a request and contribute empty parts (lse = -inf, weight 0)."""
     sys.path.insert(0, ROOT)
     import oracle
     port = _free_port()
@@ -84,22 +97,22 @@ def test_two_ranks_gather_and_merge_to_the_whole_history(world):
                                    rtol=0, atol=1e-12)
 
 
-@pytest.mark.parametrize("world", [1, 2, 3, 4, 7])
-def test_shard_view_lengths_cover_each_history_once(world):
+@pytest.mark.parametrize("world", [1, 2, 3, 4, 8])
+def test_pages_cover_each_history_once_and_balance_the_ranks(world):
+    """Host logic of the page-to-rank rule on the steady mix (64 histories in
+    [8192, 32768]): every token belongs to exactly one rank, each request's
+    ranks differ by at most one page, and the ranks' totals by a few pages."""
     sys.path.insert(0, ROOT)
-    from paged_latent_attention_gb300 import dcp
-    lens = torch.tensor([0, 1, 1535, 1536, 1537, 9000, 20000], dtype=torch.int32)
-    cols = 14
-    table = torch.arange(7 * cols, dtype=torch.int32).reshape(7, cols)
-    total = torch.zeros_like(lens)
-    for rank in range(world):
-        table_k, lens_k = dcp.shard_view(table, lens, rank, world)
-        t_lo, t_hi = dcp.shard_bounds(rank, world, cols)
-        assert table_k.stride() == table.stride()
-        assert bool((lens_k >= 0).all()) and bool((lens_k <= t_hi - t_lo).all())
-        live = lens_k > 0
-        # a rank's first column is the page holding its first token
-        if bool(live.any()):
-            assert int(table_k[0, 0]) == int(table[0, t_lo // 1536])
-        total += lens_k
-    assert torch.equal(total, lens)
+    from paged_latent_attention_gb300 import dcp, inputs
+    w = inputs.make_workload("steady")
+    per = np.zeros((w.num_reqs, world), dtype=np.int64)
+    for r, L in enumerate(w.seq_lens):
+        for c in range(-(-int(L) // 1536)):
+            per[r, dcp.owner(c, r, world)] += min(1536, int(L) - c * 1536)
+    assert np.array_equal(per.sum(axis=1), w.seq_lens.astype(np.int64))
+    assert (per.max(axis=1) - per.min(axis=1)).max() <= 1536
+    totals = per.sum(axis=0)
+    assert totals.max() - totals.min() <= 6 * 1536
+    # the contiguous split it replaces left the ranks far apart
+    if world > 1:
+        assert totals.max() - totals.min() < 0.1 * totals.mean()

@@ -1,8 +1,8 @@
 """Decode context parallelism on one GPU: the ranks' parts run one after the
-other here (each is an ordinary mla_decode on its column view of the page table;
-no kernel waits on another), then mla_merge_partials merges them as the
-exchange step would.  The merged result must match the oracle on the whole
-history, and mla_decode on the whole history."""
+other here (each is an ordinary mla_decode on the rank's pages, from
+mla_dcp_shard; no kernel waits on another), then mla_merge_partials merges them
+as the exchange step would.  The merged result must match the oracle on the
+whole history, and mla_decode on the whole history."""
 import numpy as np
 import pytest
 import torch
@@ -104,3 +104,30 @@ def test_dcp_decode_through_a_one_rank_process_group():
         assert_parity(out, lse, ref_out, ref_lse, what="dcp_decode one rank")
     finally:
         dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8])
+def test_shard_kernel_follows_the_page_rule(world):
+    """mla_dcp_shard against the rule restated on the host: rank k's row holds
+    the page IDs of the columns c with (c + r) mod world == k, in column order,
+    and its length their tokens (the last page partial)."""
+    from paged_latent_attention_gb300 import dcp
+    rng = np.random.Generator(np.random.PCG64(70 + world))
+    R, ld = 37, 23
+    lens = rng.integers(0, ld * 1536 + 1, size=R).astype(np.int32)
+    lens[:4] = [0, 1, 1536, 1537]
+    table = rng.integers(0, 10_000, size=(R, ld + 5)).astype(np.int32)
+    dt = torch.as_tensor(table, device="cuda")[:, :ld]          # row stride ld + 5
+    dl = torch.as_tensor(lens, device="cuda")
+    total = np.zeros(R, dtype=np.int64)
+    for rank in range(world):
+        tk, lk = api.mla_dcp_shard(dt, dl, world, rank)
+        tk, lk = tk.cpu().numpy(), lk.cpu().numpy()
+        for r in range(R):
+            n = -(-int(lens[r]) // 1536)
+            cols = [c for c in range(n) if dcp.owner(c, r, world) == rank]
+            assert tk[r, :len(cols)].tolist() == [int(table[r, c]) for c in cols]
+            expect = sum(min(1536, int(lens[r]) - c * 1536) for c in cols)
+            assert int(lk[r]) == expect
+            total[r] += expect
+    assert np.array_equal(total, lens.astype(np.int64))

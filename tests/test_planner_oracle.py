@@ -35,6 +35,11 @@ def test_figure4_worked_example(case):
         assert [L // per_req for L in case["seq_lens"]] == case["uniform_chunk_lens"]
         # per-request splitting shortens the longest chunk (the kernel's tail)
         assert chunk < max(case["uniform_chunk_lens"])
+        # the oracle's uniform baseline gives the figure's left panel exactly
+        # (tile 1: the figure's chunks are not rounded)
+        uchunks, usplits = oracle.plan_splits_uniform(case["seq_lens"], case["budget"], 1)
+        assert usplits == case["uniform_splits"]
+        assert uchunks == case["uniform_chunk_lens"]
 
 
 def test_equal_length_control_keeps_total_work():
@@ -87,3 +92,22 @@ def test_empty_requests_get_no_split():
     assert oracle.plan_splits([0, 0], 8, 128) == (128, [0, 0])
     chunk, splits = oracle.plan_splits([0, 1000, 0], 8, 128)
     assert splits[0] == 0 and splits[2] == 0 and splits[1] >= 1
+
+
+def test_uniform_baseline_rounds_to_the_tile_and_keeps_the_split_count():
+    rng = np.random.Generator(np.random.PCG64(2))
+    for _ in range(200):
+        R = int(rng.integers(1, 40))
+        lens = rng.integers(0, 300_000, size=R).tolist()
+        budget = int(rng.integers(1, 600))
+        chunks, splits = oracle.plan_splits_uniform(lens, budget, 128)
+        live = sum(1 for L in lens if L > 0)
+        su = max(1, budget // max(1, live))
+        for L, c, s in zip(lens, chunks, splits):
+            if L == 0:
+                assert (c, s) == (0, 0)
+                continue
+            assert c % 128 == 0 and (s - 1) * c < L <= s * c
+            assert s <= su                           # rounding up never adds a split
+            assert c - 128 < -(-L // su) <= c        # the smallest tile multiple that fits
+        assert sum(splits) <= max(budget, live)
