@@ -639,6 +639,35 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
     return v;
 }
 
+// Q^T of one segment's query rows (row qrow on): bf16 nine 64-column blocks;
+// E4M3 rows of 576 bytes: four latent blocks, then the 64-byte rope block
+// through its own map, the hi part (rows of plane 0) and the lo part (plane 1,
+// `planes` rows further on) of each.  Not inlined: it runs once per segment and
+// keeps the kernel's code small.
+template <int NG, bool F8>
+__device__ __noinline__ void load_query(uint32_t s_q, const CUtensorMap *tm_qn,
+                                        const CUtensorMap *tm_qr, int qrow, int planes,
+                                        uint32_t bar_q)
+{
+    using L = Smem<NG, F8>;
+    using F = Fmt<F8>;
+    mbar_arrive_expect_tx(bar_q, L::q_bytes);
+    if constexpr (F8) {
+        const int qrow_lo = qrow + planes;
+        for (int k = 0; k < F::sub - 1; ++k) {
+            tma_load_2d(s_q + k * L::q_chunk, tm_qn, 128 * k, qrow, bar_q);
+            tma_load_2d(s_q + k * L::q_chunk + L::q_lo, tm_qn, 128 * k, qrow_lo, bar_q);
+        }
+        tma_load_2d(s_q + (F::sub - 1) * L::q_chunk, tm_qr, kLatent, qrow, bar_q);
+        tma_load_2d(s_q + (F::sub - 1) * L::q_chunk + L::q_rope_lo, tm_qr, kLatent, qrow_lo,
+                    bar_q);
+    } else {
+        for (int k = 0; k < F::sub - 1; ++k)
+            tma_load_2d(s_q + k * L::q_chunk, tm_qn, 64 * k, qrow, bar_q);
+        tma_load_2d(s_q + (F::sub - 1) * L::q_chunk, tm_qr, 0, qrow, bar_q);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -775,47 +804,88 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
             int issued = 0;                          // K items issued (all segments)
             int q_loads = 0;
             bool ok = true;
-            for (int s = seg_begin; s < seg_end && ok; ++s) {
+            // Q^T of segment s: the buffer is free once the previous segment's last
+            // S^T has completed (bar_qe)
+            auto load_q = [&](int s) -> bool {
                 const int local = s - seg_begin;
-                const int4 seg = a.segments[s];
-                if (local > 0 &&
-                    !wait_bounded(bar_qe, (local - 1) & 1, abort_flag, a.status, 1)) {
-                    ok = false;
-                    break;
-                }
-                const int qrow = seg.x * a.rows_per_req + row0;
-                mbar_arrive_expect_tx(bar_q, L::q_bytes);
-                if constexpr (F8) {
-                    // E4M3 rows of 576 bytes: four latent blocks, then the 64-byte rope
-                    // block through its own map; the hi part (rows of plane 0), then the
-                    // lo part (plane 1, all query rows further on)
-                    const int qrow_lo = qrow + a.num_reqs * a.rows_per_req;
-                    for (int k = 0; k < F::sub - 1; ++k) {
-                        tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 128 * k, qrow, bar_q);
-                        tma_load_2d(s_q + k * L::q_chunk + L::q_lo, &tm_qn, 128 * k, qrow_lo,
-                                    bar_q);
-                    }
-                    tma_load_2d(s_q + (F::sub - 1) * L::q_chunk, &tm_qr, kLatent, qrow, bar_q);
-                    tma_load_2d(s_q + (F::sub - 1) * L::q_chunk + L::q_rope_lo, &tm_qr, kLatent,
-                                qrow_lo, bar_q);
-                } else {
-                    for (int k = 0; k < F::sub - 1; ++k)
-                        tma_load_2d(s_q + k * L::q_chunk, &tm_qn, 64 * k, qrow, bar_q);
-                    tma_load_2d(s_q + (F::sub - 1) * L::q_chunk, &tm_qr, 0, qrow, bar_q);
-                }
+                if (local > 0 && !wait_bounded(bar_qe, (local - 1) & 1, abort_flag, a.status, 1))
+                    return false;
+                const int qrow = a.segments[s].x * a.rows_per_req + row0;
+                load_query<NG, F8>(s_q, &tm_qn, &tm_qr, qrow, a.num_reqs * a.rows_per_req, bar_q);
                 ++q_loads;
-                const int32_t *trow = a.page_table + (int64_t)seg.x * a.table_ld;
-                const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
-                for (int i = 0; i < n_tiles && ok; ++i) {
-                    const int t = seg.y + i * kTile;
-                    const int page = trow[t / kPageTokens];
-                    const int tok = t % kPageTokens;
-                    if constexpr (!F8) {
+                return true;
+            };
+            if constexpr (F8) {
+                // E4M3 pages: each segment's Q^T before its K items (measured faster
+                // for this variant than the deferred order below)
+                for (int s = seg_begin; s < seg_end && ok; ++s) {
+                    const int4 seg = a.segments[s];
+                    if (!load_q(s)) {
+                        ok = false;
+                        break;
+                    }
+                    const int32_t *trow = a.page_table + (int64_t)seg.x * a.table_ld;
+                    const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
+                    for (int i = 0; i < n_tiles && ok; ++i) {
+                        const int t = seg.y + i * kTile;
+                        const int page = trow[t / kPageTokens];
+                        const int tok = t % kPageTokens;
+                        for (int k = 0; k < F::sub; ++k) {
+                            if (!wait_bounded(bar_empty_k + 8 * slot, phase ^ 1, abort_flag,
+                                              a.status, 2)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(bar_full_k + 8 * slot, kSubBytes);
+                            tma_load_3d_hint(s_k + slot * kSubBytes, &tm_kv, F::col_step * k, tok,
+                                             page, bar_full_k + 8 * slot,
+                                             k < F::sub - 1 ? pol_keep : pol_once);
+                            ++issued;
+                            if (++slot == NK) {
+                                slot = 0;
+                                phase ^= 1;
+                            }
+                        }
+                    }
+                }
+            } else {
+                // A segment's first K items go out before its Q^T: their ring slots are
+                // freed by S^T of the previous segment's items, which needs no new Q^T,
+                // so the HBM stream keeps going while that S^T finishes.  Q^T of the
+                // `pending` segment must be loaded before K item `q_deadline` (the first
+                // item whose slot only this segment's S^T can free).
+                int pending = -1, q_deadline = 0;
+                for (int s = seg_begin; s < seg_end && ok; ++s) {
+                    const int local = s - seg_begin;
+                    const int4 seg = a.segments[s];
+                    if (pending >= 0) {                  // a segment of fewer than NK items
+                        if (!load_q(pending)) {
+                            ok = false;
+                            break;
+                        }
+                        pending = -1;
+                    }
+                    if (local == 0) {
+                        if (!load_q(s)) {
+                            ok = false;
+                            break;
+                        }
+                    } else {
+                        pending = s;
+                        q_deadline = issued + NK;
+                    }
+                    const int32_t *trow = a.page_table + (int64_t)seg.x * a.table_ld;
+                    const int n_tiles = (seg.z - seg.y + kTile - 1) / kTile;
+                    for (int i = 0; i < n_tiles && ok; ++i) {
+                        const int t = seg.y + i * kTile;
+                        const int page = trow[t / kPageTokens];
+                        const int tok = t % kPageTokens;
                         // Entering a page: warm the address translations of the next page
                         // this CTA reads (the segment's next page, else the next segment's
-                        // first) with one-row L2 prefetches of its first row and of the first
-                        // row past a 2 MiB boundary inside it, a page's worth of tiles before
-                        // the ring reaches it.  Measured: ~2% off the steady step.
+                        // first) with one-row L2 prefetches of its first row and of the
+                        // first row past a 2 MiB boundary inside it, a page's worth of
+                        // tiles before the ring reaches it.  Measured: ~2% off the steady
+                        // step.
                         if (i == 0 || tok == 0) {
                             const int tn = (t / kPageTokens + 1) * kPageTokens;
                             int np = -1, nt0 = 0;
@@ -837,24 +907,34 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                                     tma_prefetch_3d(&tail.m[0], 0, tb, np);
                             }
                         }
-                    }
-                    for (int k = 0; k < F::sub; ++k) {
-                        if (!wait_bounded(bar_empty_k + 8 * slot, phase ^ 1, abort_flag, a.status,
-                                          2)) {
-                            ok = false;
-                            break;
-                        }
-                        mbar_arrive_expect_tx(bar_full_k + 8 * slot, kSubBytes);
-                        tma_load_3d_hint(s_k + slot * kSubBytes, &tm_kv, F::col_step * k, tok,
-                                         page, bar_full_k + 8 * slot,
-                                         k < F::sub - 1 ? pol_keep : pol_once);
-                        ++issued;
-                        if (++slot == NK) {
-                            slot = 0;
-                            phase ^= 1;
+                        for (int k = 0; k < F::sub; ++k) {
+                            if (pending >= 0 && issued >= q_deadline) {
+                                if (!load_q(pending)) {
+                                    ok = false;
+                                    break;
+                                }
+                                pending = -1;
+                            }
+                            if (!wait_bounded(bar_empty_k + 8 * slot, phase ^ 1, abort_flag,
+                                              a.status, 2)) {
+                                ok = false;
+                                break;
+                            }
+                            mbar_arrive_expect_tx(bar_full_k + 8 * slot, kSubBytes);
+                            tma_load_3d_hint(s_k + slot * kSubBytes, &tm_kv, F::col_step * k, tok,
+                                             page, bar_full_k + 8 * slot,
+                                             k < F::sub - 1 ? pol_keep : pol_once);
+                            ++issued;
+                            if (++slot == NK) {
+                                slot = 0;
+                                phase ^= 1;
+                            }
                         }
                     }
                 }
+                // the last segment's Q^T, if it still waits (fewer than NK items)
+                if (ok && pending >= 0)
+                    load_q(pending);
             }
             // every issued copy must land before the CTA can exit: the last NK
             // items may still be in flight, earlier ones were consumed
