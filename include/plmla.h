@@ -75,14 +75,14 @@ const char *mla_strerror(plmla_status status);
  *                one CTA owns); row_groups = n_q * num_heads / group_rows
  *   slots      = cta_budget, or the current device's SM count when 0
  *   members    = max(1, floor(slots / row_groups))   (persistent CTAs per group)
- *   budget     = max(26 * members, num_reqs * min_splits_per_req), at most 4096
+ *   budget     = max(104 * members, num_reqs * min_splits_per_req), at most 32768
  *
  * mla_decode runs row_groups x members persistent CTAs; each takes a contiguous
  * run of the chunks holding an equal share of their cost (128-token tiles plus a
  * charge for starting a request).  The schedule depends only on seq_lens and
  * this shape, so repeated calls on the same inputs give the same bits, in any
  * process.  Returns the budget, or -1 for invalid arguments, members above 256,
- * num_reqs * min_splits_per_req above 4096, or no CUDA device when
+ * num_reqs * min_splits_per_req above 32768, or no CUDA device when
  * cta_budget == 0.
  */
 int32_t mla_split_budget(int32_t num_reqs, int32_t n_q, int32_t num_heads, int32_t cta_budget,
@@ -137,7 +137,7 @@ int32_t mla_get_split_mode(void);
  *   split s of request r covers tokens [s*chunk, min((s+1)*chunk, L_r)).
  *
  * seq_lens      [num_reqs] int32, device, L_r >= 0;  num_reqs 1 .. 1024.
- * split_budget  1 .. 4096 (PLMLA_UNSUPPORTED above).
+ * split_budget  1 .. 32768 (PLMLA_UNSUPPORTED above).
  * split_indptr  [num_reqs + 1] int32, device, written: exclusive prefix sum of
  *               splits_r in request order (split ids of request r are
  *               split_indptr[r] .. split_indptr[r+1]-1).

@@ -17,8 +17,8 @@ constexpr int kMaxReqs = 1024;
 // query tokens per request: draft tokens of a verify step (4) up to a chunk of
 // new tokens of an extend (prefill) step, causal among themselves
 constexpr int kMaxNq = 256;
-constexpr int kMaxPlanSplits = 4096;  // chunks the device planner can schedule
-constexpr int kChunksPerMember = 26;  // default chunk budget per persistent CTA
+constexpr int kMaxPlanSplits = 32768; // chunks the device planner can schedule
+constexpr int kChunksPerMember = 104; // default chunk budget per persistent CTA
 // Planner cost of starting a segment, in 128-token tiles: a request's first
 // chunk carries it (query load, first-tile softmax, the previous segment's
 // partial-state epilogue).

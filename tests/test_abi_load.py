@@ -37,37 +37,39 @@ def _stated_budget(R, n_q, H, slots, min_splits):
     group = 64 if rows % 64 == 0 else 32 if rows % 32 == 0 else 16
     members = max(1, slots // (rows // group))
     wanted = R * min_splits
-    if members > 256 or wanted > 4096:
+    if members > 256 or wanted > 32768:
         return -1
-    return min(max(26 * members, wanted), 4096)
+    return min(max(104 * members, wanted), 32768)
 
 
 @pytest.mark.parametrize("R,n_q,H,slots,min_splits", [
     (64, 1, 64, 152, 1), (32, 1, 64, 152, 1), (128, 4, 64, 152, 1), (4, 1, 64, 152, 128),
     (2, 1, 16, 152, 1), (1, 1, 128, 152, 1), (1000, 2, 48, 148, 3), (7, 3, 16, 16, 2),
-    (30, 1, 16, 16, 20), (1, 1, 64, 256, 1), (1024, 1, 64, 152, 8)])
+    (30, 1, 16, 16, 20), (1, 1, 64, 256, 1), (1024, 1, 64, 152, 8), (1024, 1, 64, 152, 40),
+    (1024, 1, 64, 152, 32)])
 def test_split_budget_follows_the_stated_rule(lib, R, n_q, H, slots, min_splits):
     assert lib.mla_split_budget(R, n_q, H, slots, min_splits) == _stated_budget(
         R, n_q, H, slots, min_splits)
 
 
 def test_split_budget_examples(lib):
-    # one row group: 26 chunks per persistent CTA on 152 SMs
-    assert lib.mla_split_budget(64, 1, 64, 152, 1) == 26 * 152
+    # one row group: 104 chunks per persistent CTA on 152 SMs
+    assert lib.mla_split_budget(64, 1, 64, 152, 1) == 104 * 152
     # four row groups share the SMs in teams of 38
-    assert lib.mla_split_budget(128, 4, 64, 152, 1) == 26 * 38
+    assert lib.mla_split_budget(128, 4, 64, 152, 1) == 104 * 38
     # >= 128 chunks for each of 4 million-token requests fits the default budget,
     # and the oracle's planner (pinned by Figure 4) then gives each >= 128 chunks
     b = lib.mla_split_budget(4, 1, 64, 152, 128)
-    assert b == 26 * 152
+    assert b == 104 * 152
     chunk, splits = oracle.plan_splits([1_000_000] * 4, b, 128)
     assert min(splits) >= 128 and sum(splits) <= b
     # a per-request minimum above the default raises the budget; a larger
     # machine gets a larger one, up to the planner's limit
-    assert lib.mla_split_budget(30, 1, 16, 16, 20) == 600
+    assert lib.mla_split_budget(300, 1, 16, 16, 20) == 6000
     assert lib.mla_split_budget(1, 1, 64, 152, 1) > lib.mla_split_budget(1, 1, 64, 16, 1)
-    assert lib.mla_split_budget(1, 1, 64, 256, 1) == 4096
-    assert lib.mla_split_budget(1024, 1, 64, 152, 8) == -1
+    assert lib.mla_split_budget(1, 1, 64, 256, 1) == 104 * 256
+    assert lib.mla_split_budget(1024, 1, 64, 152, 32) == 32768
+    assert lib.mla_split_budget(1024, 1, 64, 152, 33) == -1
 
 
 def test_workspace_grows_with_the_machine(lib):
@@ -80,7 +82,7 @@ def test_workspace_grows_with_the_machine(lib):
 
 @pytest.mark.parametrize("args", [(0, 1, 64, 152, 1), (2, 0, 64, 152, 1), (2, 1, 24, 152, 1),
                                   (2, 1, 64, -1, 1), (2, 1, 64, 152, 0), (2000, 1, 64, 152, 1),
-                                  (1024, 1, 64, 152, 8)])
+                                  (1024, 1, 64, 152, 40)])
 def test_bad_shapes_are_rejected_on_the_host(lib, args):
     assert lib.mla_split_budget(*args) == -1
     assert lib.mla_workspace_size(*args) == 0
