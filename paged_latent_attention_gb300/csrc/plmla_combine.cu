@@ -6,10 +6,13 @@
 // gate is the sigmoid output gate of Gated MLA (AgentX post, "Kernel fusion and
 // overlap complete the decode path").
 //
-// One warp per output row (draft token, head).  Each lane owns 16 of the 512
-// latent columns as four float4 groups (lane + 32k), so every split's row is
-// read with fully coalesced 512-byte transactions.  Splits are visited in a
-// fixed order: the result does not depend on scheduling.
+// SPLIT warps per output row (draft token, head), each with 512 / SPLIT of its
+// latent columns; a lane owns 4 / SPLIT float4 groups (lane + 32k of the warp's
+// part), so every split's row is read with fully coalesced 512-byte
+// transactions.  Splits are visited in a fixed order, and every warp of a row
+// computes the same weights, so the result does not depend on scheduling or on
+// SPLIT.  Few rows (a handful of long requests) take SPLIT = 4 so that enough
+// warps merge in parallel once the decode's last segments are published.
 #include <math.h>
 
 #include "plmla_internal.cuh"
@@ -63,6 +66,7 @@ __device__ bool wait_segments(const int32_t *counter, int need, int32_t *status)
     return ok;
 }
 
+template <int SPLIT>
 __global__ void __launch_bounds__(kThreads)
 combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_part,
                const int32_t *__restrict__ indptr, const int32_t *__restrict__ seg_stride,
@@ -77,8 +81,12 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     // kernel (or on its own), wait for the previous grid's partial states.
     if (done == nullptr)
         asm volatile("griddepcontrol.wait;" ::: "memory");
+    constexpr int KG = 4 / SPLIT;                // float4 groups per lane
     const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t wid = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t row = wid / SPLIT;
+    const int part = (int)(wid % SPLIT);
+    const int f0 = part * 32 * KG + lane;        // this lane's first float4 of the row
     const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
     if (row >= rows)
         return;
@@ -91,10 +99,10 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     const int s0 = base + __ldcg(indptr + r), s1 = base + __ldcg(indptr + r + 1);
     // the gate logits are an input of the step: read them before waiting
     const uint2 *gp = reinterpret_cast<const uint2 *>(gate + row * kLatent);
-    uint2 graw[4];
+    uint2 graw[KG];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-        graw[k] = gp[lane + 32 * k];
+    for (int k = 0; k < KG; ++k)
+        graw[k] = gp[f0 + 32 * k];
     // With counters: this request's partial states are complete once all its
     // segments of this team are published (other requests may still run).
     if (done != nullptr && !wait_segments(done + g * num_reqs + r, s1 - s0, status))
@@ -114,9 +122,9 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     for (int o = 16; o > 0; o >>= 1)
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
 
-    float4 acc[4];
+    float4 acc[KG];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < KG; ++k)
         acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     float wsum = 0.f;
     if (m != -INFINITY) {
@@ -136,8 +144,8 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
                     continue;                    // warp-uniform: an empty segment
                 const float4 *src = src0 + k * seg_step;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float4 v = __ldcg(src + lane + 32 * j);
+                for (int j = 0; j < KG; ++j) {
+                    const float4 v = __ldcg(src + f0 + 32 * j);
                     acc[j].x = fmaf(w, v.x, acc[j].x);
                     acc[j].y = fmaf(w, v.y, acc[j].y);
                     acc[j].z = fmaf(w, v.z, acc[j].z);
@@ -152,7 +160,7 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     uint2 *dst = reinterpret_cast<uint2 *>(out + row * kLatent);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < KG; ++k) {
         const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw[k].x));
         const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&graw[k].y));
         const float o0 = acc[k].x * inv / (1.f + expf(-g01.x));
@@ -164,9 +172,9 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
         uint2 packed;
         packed.x = *reinterpret_cast<const uint32_t *>(&p01);
         packed.y = *reinterpret_cast<const uint32_t *>(&p23);
-        dst[lane + 32 * k] = packed;
+        dst[f0 + 32 * k] = packed;
     }
-    if (lse != nullptr && lane == 0)
+    if (lse != nullptr && lane == 0 && part == 0)
         lse[row] = wsum > 0.f ? m + logf(wsum) : -INFINITY;
 }
 
@@ -261,7 +269,14 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, const int
                            int32_t *status, cudaStream_t stream)
 {
     const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
-    const int64_t blocks = (rows + kThreads / 32 - 1) / (kThreads / 32);
+    // warps per row: enough warps for about one CTA of 8 per SM
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    const int64_t target = (int64_t)sms * (kThreads / 32);
+    const int split = rows >= target ? 1 : (2 * rows >= target ? 2 : 4);
+    const int64_t blocks = (rows * split + kThreads / 32 - 1) / (kThreads / 32);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kThreads);
@@ -274,8 +289,9 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, const int
     cfg.numAttrs = 1;
     if ((done == nullptr) != (status == nullptr))
         return cudaErrorInvalidValue;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, o_part, lse_part, indptr, seg_stride,
-                              group_rows, gate, num_reqs, n_q, num_heads, out, lse, done, status);
+    auto kernel = split == 1 ? combine_kernel<1> : (split == 2 ? combine_kernel<2> : combine_kernel<4>);
+    return cudaLaunchKernelEx(&cfg, kernel, o_part, lse_part, indptr, seg_stride, group_rows, gate,
+                              num_reqs, n_q, num_heads, out, lse, done, status);
 }
 
 }  // namespace plmla
