@@ -33,7 +33,7 @@ def test_captured_step_follows_new_lengths_and_queries(n_q, H):
         api.mla_decode(d["qn"], d["qr"], d["gate"], d["slab"], d["table"], d["lens"], n_q=n_q,
                        scale=SCALE, out=out, lse=lse, workspace=ws)
 
-    for _ in range(3):                 # eager calls first (tensor maps, the SM speed record)
+    for _ in range(3):                 # eager calls first (tensor maps, function attributes)
         step()
     torch.cuda.synchronize()
     graph = torch.cuda.CUDAGraph()
