@@ -226,6 +226,10 @@ def test_plan_matches_oracle_planner():
         cases.append((lens.tolist(), int(rng.integers(1, 2000))))
     cases.append(([1_000_000] * 4, 608))
     cases.append(([0] * 5, 7))
+    # budgets up to the library's cap (104 chunks per CTA on 152 SMs, and the limit)
+    for budget in (104 * 152, 32768):
+        cases.append((rng.integers(0, 1_000_001, size=64).tolist(), budget))
+        cases.append(([1_000_000] * 4, budget))
     for lens, budget in cases:
         chunk, splits = oracle.plan_splits(lens, budget, 128)
         indptr, dchunk = api.mla_plan_splits(torch.tensor(lens, dtype=torch.int32,
