@@ -836,11 +836,10 @@ def run_reference(args):
     per_step = max(1, min(w.num_reqs, int(budget_s / total / max(t1, 1e-3))))
     rows, frac = row_sample(w, per_step)
     times, kv = [], []
-    cache = {}
+    cache = {}                    # every distinct sample, drawn once (a few GB at most)
     for s in range(total):
         ids = tuple((s * per_step + i) % w.num_reqs for i in range(per_step))
         if ids not in cache:
-            cache.clear()
             cache[ids] = sample(list(ids))
         dt = run_oracle(w, cache[ids], kv_scale, rows)
         if s >= args.warmup:
