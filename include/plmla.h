@@ -128,6 +128,21 @@ plmla_status mla_set_split_mode(int32_t mode);
 int32_t mla_get_split_mode(void);
 
 /*
+ * mla_set_team_clusters -- process-wide widest thread-block cluster of query-row
+ * teams (1, 2 or 4; default 4) for the bf16 decode.  When a step has two or more
+ * teams of 64 rows (n_q * num_heads a multiple of 128), the CTAs that hold the
+ * same member's work for 2 or 4 teams run as one cluster and every KV tile is
+ * read from memory once and multicast by TMA into all of them, instead of once
+ * per team.  The width used is the largest of 4, 2 within max_teams that divides
+ * the team count and whose clusters the device holds at once (all of the grid's
+ * CTAs must be resident together), else 1.  Only the loads change: the outputs
+ * are bit-identical for every setting.  PLMLA_INVALID_ARGUMENT for another value.
+ * mla_get_team_clusters returns the setting.
+ */
+plmla_status mla_set_team_clusters(int32_t max_teams);
+int32_t mla_get_team_clusters(void);
+
+/*
  * mla_plan_splits -- per-request KV split plan [AX, Figure 4], on the device.
  *
  *   chunk     = ceil(sum_r L_r / split_budget) rounded up to a multiple of 128,

@@ -9,6 +9,7 @@ from .api import (  # noqa: F401
     device_status,
     get_page_checks,
     get_split_mode,
+    get_team_clusters,
     mla_dcp_shard,
     mla_decode,
     mla_decode_fp8,
@@ -23,4 +24,5 @@ from .api import (  # noqa: F401
     mla_workspace_size_fp8,
     set_page_checks,
     set_split_mode,
+    set_team_clusters,
 )

@@ -45,6 +45,8 @@ SIGNATURES = {
     "mla_set_page_checks": (None, [_i32]),
     "mla_set_split_mode": (ctypes.c_int, [_i32]),
     "mla_get_split_mode": (_i32, []),
+    "mla_set_team_clusters": (ctypes.c_int, [_i32]),
+    "mla_get_team_clusters": (_i32, []),
     "mla_get_page_checks": (_i32, []),
 }
 

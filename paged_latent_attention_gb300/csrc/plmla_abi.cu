@@ -53,6 +53,9 @@ int initial_split_mode()
 }
 std::atomic<int> g_split_mode{initial_split_mode()};
 
+// Widest cluster of 64-row teams that share KV loads (1 = none, 2 or 4).
+std::atomic<int> g_team_clusters{kClusterTeams};
+
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -244,6 +247,19 @@ extern "C" int32_t mla_get_split_mode(void)
     return g_split_mode.load(std::memory_order_relaxed);
 }
 
+extern "C" plmla_status mla_set_team_clusters(int32_t max_teams)
+{
+    if (max_teams != 1 && max_teams != 2 && max_teams != 4)
+        return PLMLA_INVALID_ARGUMENT;
+    g_team_clusters.store(max_teams, std::memory_order_relaxed);
+    return PLMLA_OK;
+}
+
+extern "C" int32_t mla_get_team_clusters(void)
+{
+    return g_team_clusters.load(std::memory_order_relaxed);
+}
+
 extern "C" plmla_status mla_merge_partials(const void *out_parts, const float *lse_parts,
                                            int32_t world, int64_t rows, void *out, float *lse,
                                            void *stream)
@@ -398,6 +414,14 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     a.group_rows = sh.group_rows;
     a.num_groups = sh.groups;
     a.members = sh.members;
+    // teams of a member in one cluster share its KV items (multicast), when the
+    // device holds every cluster of the grid at once; the arithmetic, and so
+    // every output bit, is the same either way
+    a.cluster = decode_cluster_teams(sh.group_rows, sh.groups, fmt.fp8,
+                                     g_team_clusters.load(std::memory_order_relaxed));
+    while (a.cluster > 1 &&
+           (int64_t)sh.members * (sh.groups / a.cluster) > decode_max_clusters(a.cluster))
+        a.cluster /= 2;
     a.scale_log2 = scale * 1.4426950408889634f;
     a.segments = plan.segments;
     a.seg_member_indptr = plan.seg_member_indptr;

@@ -271,6 +271,47 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
         : "memory");
 }
 
+// The hinted load delivered to the same shared-memory offset of every CTA in
+// `cta_mask` (thread-block cluster), completing on the barrier at the same
+// offset in each of them.
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                               int c2, uint32_t bar, uint16_t cta_mask,
+                                               uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint "
+        "[%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "h"(cta_mask),
+        "l"(policy)
+        : "memory");
+}
+
+// A KV load into the ring slot at `dst`: to this CTA alone (CL = 1) or to all
+// CL CTAs of the cluster.
+template <int CL>
+__device__ __forceinline__ void kv_load(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                        uint32_t bar, uint64_t policy)
+{
+    if constexpr (CL == 1)
+        tma_load_3d_hint(dst, map, c0, c1, c2, bar, policy);
+    else
+        tma_load_3d_mc(dst, map, c0, c1, c2, bar, (uint16_t)((1u << CL) - 1u), policy);
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster (release / acquire).
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Prefetch one box of a tiled tensor into L2 (no shared memory, no barrier).
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2)
 {
@@ -389,6 +430,22 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
+}
+
+// Arrive on the barrier at offset `bar` of every CTA of the cluster once this
+// thread's MMAs so far have completed (CL = 1: this CTA's barrier).
+template <int CL>
+__device__ __forceinline__ void mma_commit_all(uint32_t bar)
+{
+    if constexpr (CL == 1) {
+        mma_commit(bar);
+    } else {
+        const uint16_t mask = (uint16_t)((1u << CL) - 1u);
+        asm volatile(
+            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+            "h"(mask)
+            : "memory");
+    }
 }
 
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
@@ -679,7 +736,7 @@ struct TailMaps {
     CUtensorMap m[kTailMaps];
 };
 
-template <int NG, bool F8>
+template <int NG, bool F8, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_v,
                  const __grid_constant__ CUtensorMap tm_qn, const __grid_constant__ CUtensorMap tm_qr,
@@ -687,6 +744,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
 {
     using L = Smem<NG, F8>;
     using F = Fmt<F8>;
+    static_assert(CL == 1 || (!F8 && (CL == 2 || CL == 4)), "cluster of teams: bf16 pages, 2 or 4");
     constexpr int NK = L::k_slots, NV = L::v_slots;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // The swizzled TMA boxes and MMA operands need 1024-byte alignment, and the
@@ -735,11 +793,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     if (threadIdx.x == 0) {
         for (int k = 0; k < NK; ++k) {
             mbar_init(bar_full_k + 8 * k, 1);
-            mbar_init(bar_empty_k + 8 * k, 1);
+            mbar_init(bar_empty_k + 8 * k, CL);        // a release from each CTA of the cluster
         }
         for (int k = 0; k < NV; ++k) {
             mbar_init(bar_full_v + 8 * k, 1);
-            mbar_init(bar_empty_v + 8 * k, 1);
+            mbar_init(bar_empty_v + 8 * k, CL);
         }
         mbar_init(bar_q, 1);
         mbar_init(bar_qe, 1);
@@ -777,13 +835,28 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // clustered teams: every CTA's barriers are initialised and its V slots
+    // zeroed before any CTA multicasts into them
+    if constexpr (CL > 1)
+        cluster_sync();
 
     // everything above overlaps the plan kernel (programmatic dependent launch);
     // the schedule is read only once that grid has completed
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int cta = (int)blockIdx.x;
-    const int team = cta / a.members;
-    const int member = cta % a.members;
+    // CL = 1: CTA = team * members + member.  CL > 1: the CTAs of a cluster are CL
+    // teams of one member (they read the same KV items); cluster c holds teams
+    // [(c % per) * CL, + CL) of member c / per, per = teams / CL.
+    int team, member, rank = 0;
+    if constexpr (CL == 1) {
+        team = cta / a.members;
+        member = cta % a.members;
+    } else {
+        rank = (int)cluster_rank();
+        const int per = a.num_groups / CL;
+        team = ((cta / CL) % per) * CL + rank;
+        member = (cta / CL) / per;
+    }
     const int row0 = team * NG;
     const int seg_begin = a.seg_member_indptr[member];
     const int seg_end = a.seg_member_indptr[member + 1];   // empty range: no work
@@ -921,9 +994,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                                 break;
                             }
                             mbar_arrive_expect_tx(bar_full_k + 8 * slot, kSubBytes);
-                            tma_load_3d_hint(s_k + slot * kSubBytes, &tm_kv, F::col_step * k, tok,
-                                             page, bar_full_k + 8 * slot,
-                                             k < F::sub - 1 ? pol_keep : pol_once);
+                            // clustered teams take turns: item n comes from CTA n % CL
+                            if (CL == 1 || issued % CL == rank)
+                                kv_load<CL>(s_k + slot * kSubBytes, &tm_kv, F::col_step * k, tok,
+                                            page, bar_full_k + 8 * slot,
+                                            k < F::sub - 1 ? pol_keep : pol_once);
                             ++issued;
                             if (++slot == NK) {
                                 slot = 0;
@@ -975,6 +1050,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                         got = wait_bounded(bar_empty_v + 8 * slot, phase ^ 1, abort_flag, a.status,
                                            11);
                     if (lane == 0 && got) {
+                        // clustered teams take turns: item n comes from CTA n % CL (the
+                        // others only expect its bytes)
+                        const bool mine = CL == 1 || issued % CL == rank;
                         const uint32_t dst = s_v + slot * F::v_slot;
                         const uint32_t fb = bar_full_v + 8 * slot;
                         const int col = 128 * (v / F::v_per_block), tk = tok + toff;
@@ -982,10 +1060,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                         const int live = seg.z - (t + toff);
                         if (live >= F::v_tokens) {
                             mbar_arrive_expect_tx(fb, F::v_slot);
-                            tma_load_3d_hint(dst, &tm_v, col, tk, page, fb, pol_once);
-                            if constexpr (!F8)
-                                tma_load_3d_hint(dst + kVHalf, &tm_v, col + 64, tk, page, fb,
-                                                 pol_once);
+                            if (mine) {
+                                kv_load<CL>(dst, &tm_v, col, tk, page, fb, pol_once);
+                                if constexpr (!F8)
+                                    kv_load<CL>(dst + kVHalf, &tm_v, col + 64, tk, page, fb,
+                                                pol_once);
+                            }
                         } else if (live <= 0) {
                             mbar_arrive(fb);
                         } else {
@@ -993,13 +1073,13 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                             mbar_arrive_expect_tx(fb, (uint32_t)(live * 128 * halves));
                             int r0 = 0;
 #pragma unroll
-                            for (int b = kTailMaps - 1; b >= 0; --b) {
+                            for (int b = kTailMaps - 1; b >= 0 && mine; --b) {
                                 if ((live >> b) & 1) {
-                                    tma_load_3d_hint(dst + r0 * 128, &tail.m[b], col, tk + r0, page,
-                                                     fb, pol_once);
+                                    kv_load<CL>(dst + r0 * 128, &tail.m[b], col, tk + r0, page, fb,
+                                                pol_once);
                                     if constexpr (!F8)
-                                        tma_load_3d_hint(dst + kVHalf + r0 * 128, &tail.m[b],
-                                                         col + 64, tk + r0, page, fb, pol_once);
+                                        kv_load<CL>(dst + kVHalf + r0 * 128, &tail.m[b], col + 64,
+                                                    tk + r0, page, fb, pol_once);
                                     r0 += 1 << b;
                                 }
                             }
@@ -1084,7 +1164,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                                                             : dq0 + (uint64_t)(k * (L::q_chunk >> 4) + 2 * kk);
                                 mma<F8>(d_s, da + 2 * kk, db, idesc_s, (k | kk) != 0);
                             }
-                        mma_commit(bar_empty_k + 8 * slot);
+                        mma_commit_all<CL>(bar_empty_k + 8 * slot);
                         issued = true;
                         if (++slot == NK) {
                             slot = 0;
@@ -1148,7 +1228,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                             mma<F8>(tmem + 64 * j, da + (uint64_t)((k_tok * 128 >> 4) * kk),
                                     dp0 + (uint64_t)(((h + k_tok * kk) * L::p_row) >> 4),
                                     idesc_pv, (i | h | kk) != 0);
-                        mma_commit(bar_empty_v + 8 * slot);
+                        mma_commit_all<CL>(bar_empty_v + 8 * slot);
                         issued = true;
                         if (++slot == NV) {
                             slot = 0;
@@ -1419,6 +1499,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols));
     }
+    // clustered teams: no CTA leaves while another may still write into its
+    // shared memory or arrive on its barriers (every wait above is bounded, so
+    // every thread of the cluster gets here)
+    if constexpr (CL > 1)
+        cluster_sync();
 }
 
 // ---------------------------------------------------------------------------
@@ -1537,7 +1622,7 @@ bool q_maps(const DecodeArgs &a, bool f8, CUtensorMap *qn, CUtensorMap *qr)
            make_map(qr, bf16, a.q_rope, 2, qr_dims, qr_strides, q_box);
 }
 
-template <int NG, bool F8>
+template <int NG, bool F8, int CL>
 cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
 {
     KvMaps kv;
@@ -1545,7 +1630,7 @@ cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
     if (!kv_maps(a, F8, &kv) || !q_maps<NG>(a, F8, &qn, &qr))
         return cudaErrorInvalidValue;
     constexpr int smem = Smem<NG, F8>::alloc;
-    cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<NG, F8>,
+    cudaError_t err = cudaFuncSetAttribute(decode_tc_kernel<NG, F8, CL>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (err != cudaSuccess)
         return err;
@@ -1554,30 +1639,91 @@ cudaError_t launch_ng(const DecodeArgs &a, cudaStream_t stream)
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CL;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CL > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NG, F8, CL>, kv.kv, kv.v, qn, qr, kv.tail, a);
+}
+
+// Clusters of CL decode CTAs (64-row teams, bf16 pages) that the device holds at
+// once, or 0.
+template <int CL>
+int max_clusters_of()
+{
+    constexpr int smem = Smem<64, false>::alloc;
+    if (cudaFuncSetAttribute(decode_tc_kernel<64, false, CL>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(CL);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<NG, F8>, kv.kv, kv.v, qn, qr, kv.tail, a);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<64, false, CL>, &cfg) != cudaSuccess)
+        return 0;
+    return n;
 }
 
 }  // namespace
+
+int decode_cluster_teams(int group_rows, int groups, bool fp8, int max_teams)
+{
+    if (fp8 || group_rows != 64)
+        return 1;
+    if (max_teams >= 4 && groups % 4 == 0)
+        return 4;
+    return max_teams >= 2 && groups % 2 == 0 ? 2 : 1;
+}
+
+int decode_max_clusters(int cluster)
+{
+    static int cached[64][2] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0)
+        return 0;
+    const int k = cluster == 4 ? 1 : 0;
+    if (cluster != 2 && cluster != 4)
+        return 0;
+    if (dev < 64 && cached[dev][k] > 0)
+        return cached[dev][k];
+    const int n = cluster == 4 ? max_clusters_of<4>() : max_clusters_of<2>();
+    if (dev < 64 && n > 0)
+        cached[dev][k] = n;
+    return n;
+}
 
 cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream)
 {
     if (args.fp8) {
         switch (args.group_rows) {
-        case 64: return launch_ng<64, true>(args, stream);
-        case 32: return launch_ng<32, true>(args, stream);
-        case 16: return launch_ng<16, true>(args, stream);
+        case 64: return launch_ng<64, true, 1>(args, stream);
+        case 32: return launch_ng<32, true, 1>(args, stream);
+        case 16: return launch_ng<16, true, 1>(args, stream);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (args.group_rows) {
-    case 64: return launch_ng<64, false>(args, stream);
-    case 32: return launch_ng<32, false>(args, stream);
-    case 16: return launch_ng<16, false>(args, stream);
+    case 64:
+        if (args.cluster == 4)
+            return launch_ng<64, false, 4>(args, stream);
+        if (args.cluster == 2)
+            return launch_ng<64, false, 2>(args, stream);
+        return launch_ng<64, false, 1>(args, stream);
+    case 32: return launch_ng<32, false, 1>(args, stream);
+    case 16: return launch_ng<16, false, 1>(args, stream);
     default: return cudaErrorInvalidValue;
     }
 }

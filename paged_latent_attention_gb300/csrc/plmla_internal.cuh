@@ -59,6 +59,7 @@ struct DecodeArgs {
     int32_t group_rows;            // rows owned by one CTA: 16, 32 or 64
     int32_t num_groups;            // rows_per_req / group_rows (teams)
     int32_t members;               // CTAs per team
+    int32_t cluster;               // teams of one member per thread-block cluster (1, 2, 4)
     float scale_log2;              // softmax scale * log2(e)
     const int4 *segments;
     const int32_t *seg_member_indptr;
@@ -94,6 +95,15 @@ size_t plan_smem_bytes();
 cudaError_t launch_plan(const int32_t *seq_lens, int num_reqs, int budget, int members,
                         int uniform, PlanBuffers plan, cudaStream_t stream);
 cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream);
+// Teams of 64 query rows that share each KV item through a thread-block
+// cluster (the KV tiles multicast by TMA): 4 or 2 (at most max_teams, and a
+// divisor of the team count), or 1 for the E4M3 decode and narrower teams.
+// kClusterTeams is the default of max_teams.
+constexpr int kClusterTeams = 4;
+int decode_cluster_teams(int group_rows, int groups, bool fp8, int max_teams);
+// Clusters of `cluster` (2 or 4) decode CTAs the current device holds at once
+// (0 if it cannot say).
+int decode_max_clusters(int cluster);
 // The FP8 decode's query quantiser as a kernel of its own (rows of 576 values;
 // q8 holds the hi plane, then the lo plane).
 cudaError_t launch_quantize(const __nv_bfloat16 *q_nope, const __nv_bfloat16 *q_rope, int rows,

@@ -185,3 +185,18 @@ def test_split_mode_switch(lib, env, expect):
                          text=True, timeout=120, cwd=os.path.dirname(os.path.dirname(__file__)))
     assert out.returncode == 0, out.stderr
     assert out.stdout.split() == [str(expect), str(1 - expect), "0", "1"]
+
+
+def test_team_cluster_switch(lib):
+    """Host logic only: the widest cluster of query-row teams defaults to 4, the
+    setter takes 1, 2 and 4 and rejects anything else."""
+    assert lib.mla_get_team_clusters() == 4
+    try:
+        for v in (1, 2, 4):
+            assert lib.mla_set_team_clusters(v) == 0
+            assert lib.mla_get_team_clusters() == v
+        for bad in (0, 3, 8, -1):
+            assert lib.mla_set_team_clusters(bad) == 1
+            assert lib.mla_get_team_clusters() == 4
+    finally:
+        lib.mla_set_team_clusters(4)
