@@ -39,8 +39,6 @@ UNIT = "GB/s"
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
-KERNELS_PER_STEP = 3          # plan (and, for FP8 pages, the query quantiser), split decode,
-                              # combine+gate
 KV_SCALE_FP8 = 6.0 / 448.0    # the synthetic FP8 cache's scale
 DECODE_SOURCES = ["plmla_decode_tc.cu", "plmla_internal.cuh"]
 
@@ -373,6 +371,7 @@ def run_gpu(args):
     kv_bytes_layer = w.kv_tokens * kv_row_bytes(w, fp8)
     kv_bytes_step = kv_bytes_layer * layers
     decode = decoder(plmla, fp8)
+    decode_layers = layers_decoder(plmla, fp8)
 
     K, W = args.steps, args.warmup
     n_ev = K * layers
@@ -382,15 +381,24 @@ def run_gpu(args):
         for e in quad:
             e.record(stream)
 
-    def step(ev_base=None):
+    def step():
+        # the user's call for a step of every layer: one split plan, then each
+        # layer's split decode and combine
+        decode_layers([q[0] for q in qs], [q[1] for q in qs], [q[2] for q in qs], slabs, table,
+                      lens, n_q=w.n_q, out=outs, lse=lses, workspace=ws,
+                      min_splits=w.min_splits)
+
+    def step_staged(ev_base):
+        # per-layer calls with events between the kernels (plan, decode, combine)
         for l in range(layers):
             qn, qr, gate = qs[l]
             decode(qn, qr, gate, slabs[l], table, lens, n_q=w.n_q, out=outs[l],
                    lse=lses[l], workspace=ws, min_splits=w.min_splits,
-                   events=None if ev_base is None else evs[ev_base + l])
+                   events=evs[ev_base + l])
 
     for _ in range(W):
         step()
+        step_staged(0)
     torch.cuda.synchronize(device)
 
     uuid = None
@@ -402,8 +410,8 @@ def run_gpu(args):
     time.sleep(0.3)
     barrier(dist, device)
     torch.cuda.synchronize(device)
-    # timed region 1 (the reported value): K back-to-back calls exactly as a user
-    # makes them; plan, decode and combine overlap through programmatic launch
+    # timed region 1 (the reported value): K back-to-back step calls exactly as a
+    # user makes them; plan, decodes and combines overlap through programmatic launch
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     host_t0 = time.time()
     start.record(stream)
@@ -411,12 +419,13 @@ def run_gpu(args):
         step()
     end.record(stream)
     torch.cuda.synchronize(device)
-    # timed region 2 (per-kernel durations for the roofline): the same K calls
-    # with stage events recorded between the kernels, which serialises them
+    # timed region 2 (per-kernel durations for the roofline): the same K steps as
+    # per-layer calls with stage events recorded between the kernels, which
+    # serialises them
     start2, end2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start2.record(stream)
     for k in range(K):
-        step(k * layers)
+        step_staged(k * layers)
     end2.record(stream)
     torch.cuda.synchronize(device)
     host_t1 = time.time()
@@ -430,7 +439,8 @@ def run_gpu(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode, kv_bytes_layer)
+        e2e = run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode_layers,
+                      kv_bytes_layer)
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(host_t0, host_t1)
@@ -475,18 +485,21 @@ def run_gpu(args):
                    "n_q": w.n_q, "heads": w.num_heads, "layers": layers,
                    "kv_tokens": w.kv_tokens, "kv_bytes_per_step": kv_bytes_step,
                    "l2": "inputs larger than L2 (KV per step >> 129 MB L2), no flush",
-                   "split": args.split, "parallelism": f"replicas x{world}"},
+                   "split": args.split, "parallelism": f"replicas x{world}",
+                   "call": "mla_decode_layers per step (one split plan, then each layer's "
+                           "decode and combine)"},
         "pct_of_hbm_peak": 100.0 * value / world / peak,
         "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
         "request_steps_per_s": w.num_reqs * world / (max_ms / K / 1e3),
         "kernel_ms": {"plan": statistics.mean(plan_ms), "decode": dec_avg,
                       "combine": statistics.mean(combine_ms),
                       "staged_ms_per_step": staged_ms / K,
-                      "note": "from a second timed pass of the same K calls with CUDA events "
-                              "recorded between the kernels (which stops them overlapping); "
-                              "the reported value comes from the first pass, without them"},
+                      "note": "from a second timed pass of the same K steps as per-layer "
+                              "mla_decode calls (a plan per layer) with CUDA events recorded "
+                              "between the kernels (which stops them overlapping); the "
+                              "reported value comes from the first pass, without them"},
         "roofline": roofline,
-        "gpu_launches": KERNELS_PER_STEP * K * layers,
+        "gpu_launches": K * launches_per_step(layers, fp8),
         "clocks": clocks,
     }
     if e2e is not None:
@@ -495,6 +508,23 @@ def run_gpu(args):
         line["cpu_baseline"] = cpu_baseline(w, qs[0][0], qs[0][1], qs[0][2], slabs[0],
                                             args.cpu_seconds, KV_SCALE_FP8 if fp8 else None)
     return line
+
+
+def launches_per_step(layers, fp8):
+    """Kernels of one mla_decode_layers step: the plan, each layer's decode and
+    combine, and for E4M3 pages the query quantiser of every layer after the
+    first (the plan grid quantises the first)."""
+    return 1 + 2 * layers + (layers - 1 if fp8 else 0)
+
+
+def layers_decoder(plmla, fp8):
+    """The public step call for every layer, for the cache format."""
+    if not fp8:
+        return plmla.mla_decode_layers
+
+    def decode_layers_fp8(*a, **k):
+        return plmla.mla_decode_layers(*a, kv_scale=KV_SCALE_FP8, **k)
+    return decode_layers_fp8
 
 
 def decoder(plmla, fp8):
@@ -507,7 +537,7 @@ def decoder(plmla, fp8):
     return decode_fp8
 
 
-def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode, kv_bytes_layer):
+def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode_layers, kv_bytes_layer):
     """Same metric through the public call with pinned host buffers: each step
     copies its inputs host->device, decodes, and reads the result back.  As a
     serving loop would, the copies run on their own streams with two buffer
@@ -559,10 +589,9 @@ def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode, kv_bytes_
             in_ready[b].record(s_in)
         stream.wait_event(in_ready[b])
         stream.wait_event(out_free[b])
-        for l in range(layers):
-            decode(dev_q[b][l][0], dev_q[b][l][1], dev_q[b][l][2], slabs[l], dev_table[b],
-                   dev_lens[b], n_q=w.n_q, out=dev_out[b][l], lse=dev_lse[b][l], workspace=ws,
-                   min_splits=w.min_splits)
+        decode_layers([q[0] for q in dev_q[b]], [q[1] for q in dev_q[b]],
+                      [q[2] for q in dev_q[b]], slabs, dev_table[b], dev_lens[b], n_q=w.n_q,
+                      out=dev_out[b], lse=dev_lse[b], workspace=ws, min_splits=w.min_splits)
         in_free[b].record(stream)
         out_ready[b].record(stream)
         with torch.cuda.stream(s_out):

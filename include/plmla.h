@@ -223,6 +223,40 @@ plmla_status mla_decode(const void *q_nope_absorbed, const void *q_rope, const v
                         size_t workspace_bytes, int32_t cta_budget, int32_t min_splits_per_req,
                         void *stream);
 
+/*
+ * mla_decode_layers -- the decode step of num_layers MLA layers at once [K3,
+ * section "A Generic, Unified Flat KV Layout for Cache Management": the pool's
+ * slabs each hold one MLA page per global page ID, so every layer reads the
+ * same page table with its own slab base].  Each layer l computes exactly what
+ * mla_decode computes with q_nope_absorbed[l], q_rope[l], gate[l], slab_base[l],
+ * out[l] and lse[l] (bit for bit: same plan, same kernels); the split plan and
+ * persistent schedule, which depend only on seq_lens and the shape, are made
+ * once for the step instead of once per layer.
+ *
+ * num_layers       1 .. 1024
+ * q_nope_absorbed, q_rope, gate, slab_base, out
+ *                  HOST arrays of num_layers device pointers, each as in
+ *                  mla_decode (the slabs share num_pages and page_stride_elems)
+ * lse              NULL (no LSE for any layer), or a host array of num_layers
+ *                  device pointers, each NULL or as in mla_decode
+ * other arguments  as in mla_decode; the workspace is mla_workspace_size(...)
+ *                  bytes, the same as for one layer, and its status word covers
+ *                  the whole step (a failed layer makes the later ones stop)
+ *
+ * Enqueues: plan kernel -> for each layer: split-decode kernel -> combine/gate
+ * kernel (each layer's decode starts once the previous layer's combine is
+ * done).  The host arrays are read during the call only.
+ */
+plmla_status mla_decode_layers(int32_t num_layers, const void *const *q_nope_absorbed,
+                               const void *const *q_rope, const void *const *gate,
+                               const void *const *slab_base, int64_t num_pages,
+                               int64_t page_stride_elems, const int32_t *page_table,
+                               int64_t page_table_ld, const int32_t *seq_lens, int32_t num_reqs,
+                               int32_t n_q_per_req, int32_t num_heads, float scale,
+                               void *const *out, float *const *lse, void *workspace,
+                               size_t workspace_bytes, int32_t cta_budget,
+                               int32_t min_splits_per_req, void *stream);
+
 /* Size of the scratch array compiled into the library for mla_decode_static_scratch. */
 #define PLMLA_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
 
@@ -357,6 +391,24 @@ plmla_status mla_decode_fp8(const void *q_nope_absorbed, const void *q_rope, con
                             int32_t num_heads, float scale, void *out, float *lse,
                             void *workspace, size_t workspace_bytes, int32_t cta_budget,
                             int32_t min_splits_per_req, void *stream);
+
+/*
+ * mla_decode_layers_fp8 -- mla_decode_layers over E4M3 pages: layer l computes
+ * what mla_decode_fp8 computes with kv_scale[l] (a HOST array of num_layers
+ * scales) and the layer's pointers; the workspace is mla_workspace_size_fp8(...)
+ * bytes.  The first layer's queries are quantised by the plan grid, each later
+ * layer's by a quantiser kernel before its decode.
+ */
+plmla_status mla_decode_layers_fp8(int32_t num_layers, const void *const *q_nope_absorbed,
+                                   const void *const *q_rope, const void *const *gate,
+                                   const void *const *slab_base, const float *kv_scale,
+                                   int64_t num_pages, int64_t page_stride_elems,
+                                   const int32_t *page_table, int64_t page_table_ld,
+                                   const int32_t *seq_lens, int32_t num_reqs,
+                                   int32_t n_q_per_req, int32_t num_heads, float scale,
+                                   void *const *out, float *const *lse, void *workspace,
+                                   size_t workspace_bytes, int32_t cta_budget,
+                                   int32_t min_splits_per_req, void *stream);
 
 /*
  * mla_quantize_queries_fp8 -- the query step of mla_decode_fp8 on its own: rows

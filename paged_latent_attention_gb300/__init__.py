@@ -13,6 +13,7 @@ from .api import (  # noqa: F401
     mla_dcp_shard,
     mla_decode,
     mla_decode_fp8,
+    mla_decode_layers,
     mla_kv_append,
     mla_kv_append_fp8,
     mla_merge_partials,

@@ -27,6 +27,11 @@ SIGNATURES = {
                                   _f, _p, _p, _p, _sz, _i32, _i32, _p]),
     "mla_decode_ex": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _p, _i64, _p, _i32, _i32, _i32,
                                      _f, _p, _p, _p, _sz, _i32, _i32, _p, _p]),
+    "mla_decode_layers": (ctypes.c_int, [_i32, _p, _p, _p, _p, _i64, _i64, _p, _i64, _p, _i32,
+                                         _i32, _i32, _f, _p, _p, _p, _sz, _i32, _i32, _p]),
+    "mla_decode_layers_fp8": (ctypes.c_int, [_i32, _p, _p, _p, _p, _p, _i64, _i64, _p, _i64, _p,
+                                             _i32, _i32, _i32, _f, _p, _p, _p, _sz, _i32, _i32,
+                                             _p]),
     "mla_split_combine": (ctypes.c_int, [_p, _p, _p, _p, _i32, _i32, _i32, _p, _p, _p]),
     "mla_decode_static_scratch": (ctypes.c_int, [_p, _p, _p, _p, _i64, _i64, _p, _i64, _p, _i32,
                                                  _i32, _i32, _f, _p, _p, _i32, _i32, _p]),

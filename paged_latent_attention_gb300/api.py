@@ -175,6 +175,89 @@ def _decode(q_nope_absorbed, q_rope, gate, slab, page_table, seq_lens, kv_scale,
     return out, lse
 
 
+def mla_decode_layers(q_nope_absorbed, q_rope, gate, slabs, page_table, seq_lens, *, n_q=1,
+                      scale=DEFAULT_SCALE, kv_scale=None, out=None, lse=None, workspace=None,
+                      cta_budget=0, min_splits=1, stream=None, with_lse=True):
+    """The decode step of several MLA layers that share the page table and the
+    history lengths (every layer's pool is paged by the same global page IDs):
+    one split plan for the step, then each layer's split decode and combine.
+    q_nope_absorbed, q_rope, gate and slabs are lists with one tensor per layer,
+    each as in mla_decode (E4M3 slabs with `kv_scale`, a float or one per
+    layer); returns (outs, lses), lists (lses of None without LSE).  Layer l's
+    results equal mla_decode's (or mla_decode_fp8's) on layer l's tensors."""
+    L = len(slabs)
+    _require(L >= 1 and len(q_nope_absorbed) == L and len(q_rope) == L and len(gate) == L,
+             "one query, rope, gate and slab tensor per layer")
+    fp8 = kv_scale is not None
+    scales = None
+    if fp8:
+        scales = list(kv_scale) if isinstance(kv_scale, (list, tuple)) else [kv_scale] * L
+        _require(len(scales) == L and all(math.isfinite(v) and v > 0 for v in scales),
+                 "kv_scale must be finite and > 0 (one value, or one per layer)")
+        slabs = [_byte_view(s) for s in slabs]
+    qn0 = q_nope_absorbed[0]
+    _require(qn0.dim() == 3, "q_nope_absorbed must be [R*n_q, H, 512]")
+    T, H, _ = qn0.shape
+    _require(T % n_q == 0, "first dimension must be num_reqs * n_q")
+    R = T // n_q
+    device = qn0.device
+    want = torch.uint8 if fp8 else torch.bfloat16
+    num_pages, page_stride = slabs[0].shape[0], slabs[0].stride(0)
+    for l in range(L):
+        _check_bf16(q_nope_absorbed[l], "q_nope_absorbed", (T, H, LATENT))
+        _check_bf16(q_rope[l], "q_rope", (T, H, ROPE))
+        _check_bf16(gate[l], "gate", (T, H, LATENT))
+        s = slabs[l]
+        _require(s.is_cuda and s.dtype == want and s.dim() == 2 and s.stride(1) == 1,
+                 f"each slab must be a 2-D CUDA {want} tensor with contiguous pages")
+        _require(s.shape[0] == num_pages and s.stride(0) == page_stride,
+                 "the layers' slabs must share the page count and page stride")
+    _require(slabs[0].shape[1] >= PAGE_TOKENS * ROW, "slab page too small")
+    _require(page_table.is_cuda and page_table.dtype == torch.int32 and page_table.dim() == 2,
+             "page_table must be a 2-D CUDA int32 tensor")
+    _require(page_table.shape[0] == R and page_table.stride(1) == 1,
+             "page_table must be [R, ld] with unit column stride")
+    _require(seq_lens.is_cuda and seq_lens.dtype == torch.int32 and seq_lens.is_contiguous()
+             and tuple(seq_lens.shape) == (R,), "seq_lens must be a contiguous CUDA int32 [R]")
+    if out is None:
+        out = [torch.empty_like(q) for q in q_nope_absorbed]
+    _require(len(out) == L, "one output tensor per layer")
+    for o in out:
+        _check_bf16(o, "out", (T, H, LATENT))
+    if lse is None and with_lse:
+        lse = [torch.empty(T, H, dtype=torch.float32, device=device) for _ in range(L)]
+    if lse is not None:
+        _require(len(lse) == L, "one lse tensor per layer")
+        for v in lse:
+            _require(v is None or (v.is_cuda and v.dtype == torch.float32 and v.is_contiguous()
+                                   and tuple(v.shape) == (T, H)),
+                     "lse must be a contiguous CUDA fp32 [T, H] (or None)")
+    if workspace is None:
+        workspace = allocate_workspace(R, n_q, H, cta_budget, min_splits, device, fp8=fp8)
+    _require(workspace.is_cuda and workspace.is_contiguous(), "workspace must be CUDA memory")
+    nbytes = workspace.numel() * workspace.element_size()
+
+    def ptrs(ts):
+        arr = (ctypes.c_void_p * L)(*[None if t is None else t.data_ptr() for t in ts])
+        return arr, ctypes.cast(arr, ctypes.c_void_p)
+
+    keep = [ptrs(q_nope_absorbed), ptrs(q_rope), ptrs(gate), ptrs(slabs), ptrs(out)]
+    lse_arr = ptrs(lse) if lse is not None else (None, None)
+    lib = _native.lib()
+    head = [L] + [k[1] for k in keep[:4]]
+    tail = [num_pages, page_stride, page_table.data_ptr(), page_table.stride(0),
+            seq_lens.data_ptr(), R, n_q, H, float(scale), keep[4][1], lse_arr[1],
+            workspace.data_ptr(), nbytes, int(cta_budget), int(min_splits),
+            _stream_ptr(stream, device)]
+    if fp8:
+        sc = (ctypes.c_float * L)(*[float(v) for v in scales])
+        status = lib.mla_decode_layers_fp8(*head, ctypes.cast(sc, ctypes.c_void_p), *tail)
+    else:
+        status = lib.mla_decode_layers(*head, *tail)
+    _native.check(status, "mla_decode_layers_fp8" if fp8 else "mla_decode_layers")
+    return out, lse if lse is not None else [None] * L
+
+
 def mla_quantize_queries_fp8(q_nope_absorbed, q_rope, stream=None):
     """The FP8 decode's query step: (hi [rows, 576] uint8, lo [rows, 576] uint8,
     exps [rows] int32) for the rows of [q_nope | q_rope] (any leading shape,

@@ -312,7 +312,7 @@ extern "C" plmla_status mla_split_combine(const float *o_part, const float *lse_
                                      n_q_per_req * num_heads,
                                      static_cast<const __nv_bfloat16 *>(gate), num_reqs,
                                      n_q_per_req, num_heads, static_cast<__nv_bfloat16 *>(out),
-                                     lse, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+                                     lse, nullptr, nullptr, 1, static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PLMLA_OK : PLMLA_CUDA_ERROR;
 }
 
@@ -332,40 +332,59 @@ struct KvFormat {
     float kv_scale;
 };
 
-plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const void *gate,
-                         const void *slab_base, int64_t num_pages, int64_t page_stride_elems,
-                         const int32_t *page_table, int64_t page_table_ld,
-                         const int32_t *seq_lens, int32_t num_reqs, int32_t n_q_per_req,
-                         int32_t num_heads, float scale, void *out, float *lse, void *workspace,
-                         size_t workspace_bytes, int32_t cta_budget, int32_t min_splits_per_req,
-                         void *stream, const plmla_stage_events *events, const KvFormat &fmt)
+// One decode step of `layers` attention layers that share the page table and
+// the history lengths (one paged layout for every layer's pool): one split plan
+// for the step, then per layer the split decode and the gated combine.  The
+// finished-segment counters are zeroed by the plan and count on across the
+// layers, so layer l's combine waits for (l + 1) times each request's segments;
+// layer l's decode starts only after layer l - 1's combine (programmatic
+// launch), so the partial states can be reused.  Layer-indexed arrays are host
+// arrays of device pointers; kv_scale (E4M3 pages) is a host array too.
+plmla_status decode_layers_impl(int32_t layers, const void *const *q_nope_absorbed,
+                                const void *const *q_rope, const void *const *gate,
+                                const void *const *slab_base, const float *kv_scale,
+                                int64_t num_pages, int64_t page_stride_elems,
+                                const int32_t *page_table, int64_t page_table_ld,
+                                const int32_t *seq_lens, int32_t num_reqs, int32_t n_q_per_req,
+                                int32_t num_heads, float scale, void *const *out,
+                                float *const *lse, void *workspace, size_t workspace_bytes,
+                                int32_t cta_budget, int32_t min_splits_per_req, void *stream,
+                                const plmla_stage_events *events, bool fp8)
 {
-    if (q_nope_absorbed == nullptr || q_rope == nullptr || gate == nullptr ||
-        slab_base == nullptr || page_table == nullptr || seq_lens == nullptr ||
-        out == nullptr || workspace == nullptr)
+    if (layers < 1 || layers > kMaxLayers || q_nope_absorbed == nullptr || q_rope == nullptr ||
+        gate == nullptr || slab_base == nullptr || out == nullptr ||
+        (fp8 && kv_scale == nullptr) || (events != nullptr && layers != 1))
+        return PLMLA_INVALID_ARGUMENT;
+    if (page_table == nullptr || seq_lens == nullptr || workspace == nullptr)
         return PLMLA_INVALID_ARGUMENT;
     if (!shape_ok(num_reqs, n_q_per_req, num_heads) || min_splits_per_req < 1 || cta_budget < 0)
         return PLMLA_INVALID_ARGUMENT;
     // page strides are multiples of 16 bytes (a TMA requirement): 8 bf16 or 16 E4M3 elements
     if (num_pages < 1 || num_pages > INT32_MAX || page_table_ld < 1 ||
         page_stride_elems < (int64_t)kPageTokens * kRow ||
-        page_stride_elems % (fmt.fp8 ? 16 : 8) != 0)
+        page_stride_elems % (fp8 ? 16 : 8) != 0)
         return PLMLA_INVALID_ARGUMENT;
     if (!(isfinite(scale)))
         return PLMLA_INVALID_ARGUMENT;
-    if (fmt.fp8 && !(isfinite(fmt.kv_scale) && fmt.kv_scale > 0.f))
+    if (!aligned(workspace, kAlign) || !aligned(page_table, 4) || !aligned(seq_lens, 4))
         return PLMLA_INVALID_ARGUMENT;
-    if (!aligned(q_nope_absorbed, 16) || !aligned(q_rope, 16) || !aligned(gate, 16) ||
-        !aligned(slab_base, 16) || !aligned(out, 16) || !aligned(workspace, kAlign) ||
-        !aligned(page_table, 4) || !aligned(seq_lens, 4) ||
-        (lse != nullptr && !aligned(lse, 4)))
-        return PLMLA_INVALID_ARGUMENT;
+    for (int32_t l = 0; l < layers; ++l) {
+        if (q_nope_absorbed[l] == nullptr || q_rope[l] == nullptr || gate[l] == nullptr ||
+            slab_base[l] == nullptr || out[l] == nullptr)
+            return PLMLA_INVALID_ARGUMENT;
+        if (fp8 && !(isfinite(kv_scale[l]) && kv_scale[l] > 0.f))
+            return PLMLA_INVALID_ARGUMENT;
+        if (!aligned(q_nope_absorbed[l], 16) || !aligned(q_rope[l], 16) ||
+            !aligned(gate[l], 16) || !aligned(slab_base[l], 16) || !aligned(out[l], 16) ||
+            (lse != nullptr && lse[l] != nullptr && !aligned(lse[l], 4)))
+            return PLMLA_INVALID_ARGUMENT;
+    }
 
     Shape sh;
     if (!shape_for(num_reqs, n_q_per_req, num_heads, cta_budget, min_splits_per_req, &sh))
         return (cta_budget == 0 && current_sm_count() <= 0) ? PLMLA_CUDA_ERROR
                                                             : PLMLA_UNSUPPORTED;
-    const WorkspaceLayout w = layout_for(num_reqs, sh, fmt.fp8);
+    const WorkspaceLayout w = layout_for(num_reqs, sh, fp8);
     if (workspace_bytes < w.total)
         return PLMLA_WORKSPACE_TOO_SMALL;
 
@@ -381,10 +400,11 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     plan.seg_member_indptr = reinterpret_cast<int32_t *>(ws + w.seg_member);
     plan.done = reinterpret_cast<int32_t *>(ws + w.done);
     plan.n_done = sh.groups * num_reqs;
-    plan.q_nope = static_cast<const __nv_bfloat16 *>(q_nope_absorbed);
-    plan.q_rope = static_cast<const __nv_bfloat16 *>(q_rope);
-    plan.q8 = fmt.fp8 ? reinterpret_cast<uint8_t *>(ws + w.q8) : nullptr;
-    plan.qexp = fmt.fp8 ? reinterpret_cast<int32_t *>(ws + w.qexp) : nullptr;
+    // E4M3 pages: the plan grid also quantises the first layer's queries
+    plan.q_nope = static_cast<const __nv_bfloat16 *>(q_nope_absorbed[0]);
+    plan.q_rope = static_cast<const __nv_bfloat16 *>(q_rope[0]);
+    plan.q8 = fp8 ? reinterpret_cast<uint8_t *>(ws + w.q8) : nullptr;
+    plan.qexp = fp8 ? reinterpret_cast<int32_t *>(ws + w.qexp) : nullptr;
     plan.q_rows = num_reqs * sh.rows_per_req;
     float *o_part = reinterpret_cast<float *>(ws + w.o_part);
     float *lse_part = reinterpret_cast<float *>(ws + w.lse_part);
@@ -395,13 +415,10 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
         return PLMLA_CUDA_ERROR;
     cudaError_t err = launch_plan(seq_lens, num_reqs, sh.budget, sh.members,
                                   g_split_mode.load(std::memory_order_relaxed), plan, s);
-    if (err != cudaSuccess || record(ev.decode_begin, s) != cudaSuccess)
+    if (err != cudaSuccess)
         return PLMLA_CUDA_ERROR;
 
     DecodeArgs a = {};
-    a.q_nope = static_cast<const __nv_bfloat16 *>(q_nope_absorbed);
-    a.q_rope = static_cast<const __nv_bfloat16 *>(q_rope);
-    a.slab = slab_base;
     a.page_stride = page_stride_elems;
     a.num_pages = num_pages;
     a.page_table = page_table;
@@ -417,7 +434,7 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     // teams of a member in one cluster share its KV items (multicast), when the
     // device holds every cluster of the grid at once; the arithmetic, and so
     // every output bit, is the same either way
-    a.cluster = decode_cluster_teams(sh.group_rows, sh.groups, fmt.fp8,
+    a.cluster = decode_cluster_teams(sh.group_rows, sh.groups, fp8,
                                      g_team_clusters.load(std::memory_order_relaxed));
     while (a.cluster > 1 &&
            (int64_t)sh.members * (sh.groups / a.cluster) > decode_max_clusters(a.cluster))
@@ -430,20 +447,32 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     a.lse_part = lse_part;
     a.status = plan.status;
     a.done = plan.done;
-    a.fp8 = fmt.fp8 ? 1 : 0;
-    a.kv_scale = fmt.kv_scale;
+    a.fp8 = fp8 ? 1 : 0;
     a.q8 = plan.q8;
     a.qexp = plan.qexp;
-    err = launch_decode_tc(a, s);
-    if (err != cudaSuccess || record(ev.combine_begin, s) != cudaSuccess)
-        return PLMLA_CUDA_ERROR;
-
-    err = launch_combine(o_part, lse_part, plan.seg_req_indptr, plan.seg_count, sh.group_rows,
-                         static_cast<const __nv_bfloat16 *>(gate), num_reqs, n_q_per_req,
-                         num_heads, static_cast<__nv_bfloat16 *>(out), lse, plan.done,
-                         plan.status, s);
-    if (err != cudaSuccess || record(ev.combine_end, s) != cudaSuccess)
-        return PLMLA_CUDA_ERROR;
+    for (int32_t l = 0; l < layers; ++l) {
+        if (fp8 && l > 0 &&
+            launch_quantize(static_cast<const __nv_bfloat16 *>(q_nope_absorbed[l]),
+                            static_cast<const __nv_bfloat16 *>(q_rope[l]), plan.q_rows, plan.q8,
+                            plan.qexp, s) != cudaSuccess)
+            return PLMLA_CUDA_ERROR;
+        if (record(ev.decode_begin, s) != cudaSuccess)
+            return PLMLA_CUDA_ERROR;
+        a.q_nope = static_cast<const __nv_bfloat16 *>(q_nope_absorbed[l]);
+        a.q_rope = static_cast<const __nv_bfloat16 *>(q_rope[l]);
+        a.slab = slab_base[l];
+        a.kv_scale = fp8 ? kv_scale[l] : 1.f;
+        err = launch_decode_tc(a, s);
+        if (err != cudaSuccess || record(ev.combine_begin, s) != cudaSuccess)
+            return PLMLA_CUDA_ERROR;
+        err = launch_combine(o_part, lse_part, plan.seg_req_indptr, plan.seg_count,
+                             sh.group_rows, static_cast<const __nv_bfloat16 *>(gate[l]), num_reqs,
+                             n_q_per_req, num_heads, static_cast<__nv_bfloat16 *>(out[l]),
+                             lse != nullptr ? lse[l] : nullptr, plan.done, plan.status, l + 1,
+                             s);
+        if (err != cudaSuccess || record(ev.combine_end, s) != cudaSuccess)
+            return PLMLA_CUDA_ERROR;
+    }
     if (g_page_checks.load(std::memory_order_relaxed) != 0 &&
         launch_check_pages(seq_lens, num_reqs, page_table, page_table_ld,
                                             num_pages, plan.status, s) != cudaSuccess)
@@ -451,7 +480,61 @@ plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const 
     return PLMLA_OK;
 }
 
+// One layer (mla_decode, mla_decode_fp8 and their _ex forms).
+plmla_status decode_impl(const void *q_nope_absorbed, const void *q_rope, const void *gate,
+                         const void *slab_base, int64_t num_pages, int64_t page_stride_elems,
+                         const int32_t *page_table, int64_t page_table_ld,
+                         const int32_t *seq_lens, int32_t num_reqs, int32_t n_q_per_req,
+                         int32_t num_heads, float scale, void *out, float *lse, void *workspace,
+                         size_t workspace_bytes, int32_t cta_budget, int32_t min_splits_per_req,
+                         void *stream, const plmla_stage_events *events, const KvFormat &fmt)
+{
+    void *out_l[1] = {out};
+    float *lse_l[1] = {lse};
+    const float kv_l[1] = {fmt.kv_scale};
+    return decode_layers_impl(1, &q_nope_absorbed, &q_rope, &gate, &slab_base,
+                              fmt.fp8 ? kv_l : nullptr, num_pages, page_stride_elems, page_table,
+                              page_table_ld, seq_lens, num_reqs, n_q_per_req, num_heads, scale,
+                              out_l, lse_l, workspace, workspace_bytes, cta_budget,
+                              min_splits_per_req, stream, events, fmt.fp8);
+}
+
 }  // namespace
+
+extern "C" plmla_status mla_decode_layers(int32_t num_layers, const void *const *q_nope_absorbed,
+                                          const void *const *q_rope, const void *const *gate,
+                                          const void *const *slab_base, int64_t num_pages,
+                                          int64_t page_stride_elems, const int32_t *page_table,
+                                          int64_t page_table_ld, const int32_t *seq_lens,
+                                          int32_t num_reqs, int32_t n_q_per_req,
+                                          int32_t num_heads, float scale, void *const *out,
+                                          float *const *lse, void *workspace,
+                                          size_t workspace_bytes, int32_t cta_budget,
+                                          int32_t min_splits_per_req, void *stream)
+{
+    return decode_layers_impl(num_layers, q_nope_absorbed, q_rope, gate, slab_base, nullptr,
+                              num_pages, page_stride_elems, page_table, page_table_ld, seq_lens,
+                              num_reqs, n_q_per_req, num_heads, scale, out, lse, workspace,
+                              workspace_bytes, cta_budget, min_splits_per_req, stream, nullptr,
+                              false);
+}
+
+extern "C" plmla_status mla_decode_layers_fp8(
+    int32_t num_layers, const void *const *q_nope_absorbed, const void *const *q_rope,
+    const void *const *gate, const void *const *slab_base, const float *kv_scale,
+    int64_t num_pages, int64_t page_stride_elems, const int32_t *page_table,
+    int64_t page_table_ld, const int32_t *seq_lens, int32_t num_reqs, int32_t n_q_per_req,
+    int32_t num_heads, float scale, void *const *out, float *const *lse, void *workspace,
+    size_t workspace_bytes, int32_t cta_budget, int32_t min_splits_per_req, void *stream)
+{
+    if (kv_scale == nullptr)
+        return PLMLA_INVALID_ARGUMENT;
+    return decode_layers_impl(num_layers, q_nope_absorbed, q_rope, gate, slab_base, kv_scale,
+                              num_pages, page_stride_elems, page_table, page_table_ld, seq_lens,
+                              num_reqs, n_q_per_req, num_heads, scale, out, lse, workspace,
+                              workspace_bytes, cta_budget, min_splits_per_req, stream, nullptr,
+                              true);
+}
 
 extern "C" plmla_status mla_decode_ex(const void *q_nope_absorbed, const void *q_rope,
                                       const void *gate, const void *slab_base,

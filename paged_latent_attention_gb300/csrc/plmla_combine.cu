@@ -72,7 +72,7 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
                const int32_t *__restrict__ indptr, const int32_t *__restrict__ seg_stride,
                int group_rows, const __nv_bfloat16 *__restrict__ gate, int num_reqs, int n_q,
                int num_heads, __nv_bfloat16 *__restrict__ out, float *__restrict__ lse,
-               const int32_t *__restrict__ done, int32_t *status)
+               const int32_t *__restrict__ done, int32_t *status, int epoch)
 {
     // The next kernel on the stream may launch now (the decode step's planner
     // waits on entry for this grid to complete).
@@ -104,8 +104,9 @@ combine_kernel(const float *__restrict__ o_part, const float *__restrict__ lse_p
     for (int k = 0; k < KG; ++k)
         graw[k] = gp[f0 + 32 * k];
     // With counters: this request's partial states are complete once all its
-    // segments of this team are published (other requests may still run).
-    if (done != nullptr && !wait_segments(done + g * num_reqs + r, s1 - s0, status))
+    // segments of this team are published for this layer (other requests may
+    // still run; the counters hold the earlier layers' segments too).
+    if (done != nullptr && !wait_segments(done + g * num_reqs + r, (s1 - s0) * epoch, status))
         return;
 
     // The segments' log-sum-exps are read by the lanes in parallel, 32 at a
@@ -266,7 +267,7 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, const int
                            const int32_t *seg_stride, int group_rows,
                            const __nv_bfloat16 *gate, int num_reqs, int n_q, int num_heads,
                            __nv_bfloat16 *out, float *lse, const int32_t *done,
-                           int32_t *status, cudaStream_t stream)
+                           int32_t *status, int epoch, cudaStream_t stream)
 {
     const int64_t rows = (int64_t)num_reqs * n_q * num_heads;
     // warps per row: enough warps for about one CTA of 8 per SM
@@ -287,11 +288,11 @@ cudaError_t launch_combine(const float *o_part, const float *lse_part, const int
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if ((done == nullptr) != (status == nullptr))
+    if ((done == nullptr) != (status == nullptr) || epoch < 1)
         return cudaErrorInvalidValue;
     auto kernel = split == 1 ? combine_kernel<1> : (split == 2 ? combine_kernel<2> : combine_kernel<4>);
     return cudaLaunchKernelEx(&cfg, kernel, o_part, lse_part, indptr, seg_stride, group_rows, gate,
-                              num_reqs, n_q, num_heads, out, lse, done, status);
+                              num_reqs, n_q, num_heads, out, lse, done, status, epoch);
 }
 
 }  // namespace plmla

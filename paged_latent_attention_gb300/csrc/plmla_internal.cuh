@@ -12,6 +12,7 @@ constexpr int kLatent = 512;      // compressed latent width (c_kv)
 constexpr int kRope = 64;         // rope key width
 constexpr int kRow = kLatent + kRope;
 constexpr int kPageTokens = 1536; // token rows per MLA page
+constexpr int kMaxLayers = 1024;  // layers of one mla_decode_layers step
 constexpr int kTile = 128;        // KV tokens per decode tile; chunks are multiples of it
 constexpr int kMaxReqs = 1024;
 // query tokens per request: draft tokens of a verify step (4) up to a chunk of
@@ -135,13 +136,14 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi)
 // of segments [g*stride + indptr[r], g*stride + indptr[r + 1]), where stride is
 // *seg_stride (or 0 when seg_stride is null).
 // With `done` (and `status`) set, the combine is launched while the decode is
-// still running and waits, per request, until done[team * R + r] counts all of
-// the request's segments; without it, it waits for the previous grid to finish.
+// still running and waits, per request, until done[team * R + r] counts `epoch`
+// times the request's segments (the counters run on across the layers of one
+// step: epoch = layer + 1); without it, it waits for the previous grid to finish.
 cudaError_t launch_combine(const float *o_part, const float *lse_part, const int32_t *indptr,
                            const int32_t *seg_stride, int group_rows,
                            const __nv_bfloat16 *gate, int num_reqs, int n_q, int num_heads,
                            __nv_bfloat16 *out, float *lse, const int32_t *done,
-                           int32_t *status, cudaStream_t stream);
+                           int32_t *status, int epoch, cudaStream_t stream);
 
 __device__ __forceinline__ float fast_exp2(float x)
 {

@@ -200,3 +200,37 @@ def test_team_cluster_switch(lib):
             assert lib.mla_get_team_clusters() == 4
     finally:
         lib.mla_set_team_clusters(4)
+
+
+def test_layered_decode_arguments_are_checked_on_the_host(lib):
+    """mla_decode_layers / _fp8: the layer count, the per-layer pointer arrays
+    and the E4M3 scales are validated before any launch."""
+    fake = 1 << 20  # never dereferenced: validation fails first
+    L = 3
+    arr = (ctypes.c_void_p * L)(fake, fake, fake)
+    p = ctypes.cast(arr, ctypes.c_void_p)
+    holes = (ctypes.c_void_p * L)(fake, None, fake)
+    ph = ctypes.cast(holes, ctypes.c_void_p)
+    odd = (ctypes.c_void_p * L)(fake, fake + 8, fake)
+    po = ctypes.cast(odd, ctypes.c_void_p)
+
+    def call(n=L, q=p, slabs=p, out=p, ws=fake):
+        return lib.mla_decode_layers(n, q, p, p, slabs, 8, 1536 * 576, fake, 1, fake, 2, 1, 16,
+                                     ctypes.c_float(0.07), out, None, ws, 1 << 30, 152, 1, None)
+    assert call(n=0) == 1
+    assert call(n=1025) == 1
+    assert call(q=None) == 1
+    assert call(q=ph) == 1                  # a missing layer pointer
+    assert call(out=po) == 1                # a layer's output not 16-byte aligned
+    assert call(slabs=ph) == 1
+    assert call(ws=fake + 128) == 1
+    good = (ctypes.c_float * L)(0.5, 0.25, 1.0)
+    bad = (ctypes.c_float * L)(0.5, 0.0, 1.0)
+
+    def call8(scales):
+        return lib.mla_decode_layers_fp8(L, p, p, p, p, scales, 8, 1536 * 576, fake, 1, fake, 2,
+                                         1, 16, ctypes.c_float(0.07), p, None, fake + 128,
+                                         1 << 30, 152, 1, None)
+    assert call8(None) == 1
+    assert call8(ctypes.cast(bad, ctypes.c_void_p)) == 1
+    assert call8(ctypes.cast(good, ctypes.c_void_p)) == 1   # workspace misaligned
