@@ -381,12 +381,19 @@ def run_gpu(args):
         for e in quad:
             e.record(stream)
 
-    def step():
+    def call_step(q_layers, tbl, ln, out_layers, lse_layers):
         # the user's call for a step of every layer: one split plan, then each
-        # layer's split decode and combine
-        decode_layers([q[0] for q in qs], [q[1] for q in qs], [q[2] for q in qs], slabs, table,
-                      lens, n_q=w.n_q, out=outs, lse=lses, workspace=ws,
-                      min_splits=w.min_splits)
+        # layer's split decode and combine (one layer: the plain decode call)
+        if layers == 1:
+            decode(*q_layers[0], slabs[0], tbl, ln, n_q=w.n_q, out=out_layers[0],
+                   lse=lse_layers[0], workspace=ws, min_splits=w.min_splits)
+        else:
+            decode_layers([q[0] for q in q_layers], [q[1] for q in q_layers],
+                          [q[2] for q in q_layers], slabs, tbl, ln, n_q=w.n_q, out=out_layers,
+                          lse=lse_layers, workspace=ws, min_splits=w.min_splits)
+
+    def step():
+        call_step(qs, table, lens, outs, lses)
 
     def step_staged(ev_base):
         # per-layer calls with events between the kernels (plan, decode, combine)
@@ -439,8 +446,7 @@ def run_gpu(args):
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode_layers,
-                      kv_bytes_layer)
+        e2e = run_e2e(args, w, qs, table, lens, device, dist, call_step, kv_bytes_layer)
     time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(host_t0, host_t1)
@@ -486,8 +492,8 @@ def run_gpu(args):
                    "kv_tokens": w.kv_tokens, "kv_bytes_per_step": kv_bytes_step,
                    "l2": "inputs larger than L2 (KV per step >> 129 MB L2), no flush",
                    "split": args.split, "parallelism": f"replicas x{world}",
-                   "call": "mla_decode_layers per step (one split plan, then each layer's "
-                           "decode and combine)"},
+                   "call": ("mla_decode_layers per step (one split plan, then each layer's "
+                            "decode and combine)" if layers > 1 else "mla_decode per step")},
         "pct_of_hbm_peak": 100.0 * value / world / peak,
         "pct_of_nominal_8tbs": 100.0 * value / world / NOMINAL_HBM_GBS,
         "request_steps_per_s": w.num_reqs * world / (max_ms / K / 1e3),
@@ -514,7 +520,7 @@ def launches_per_step(layers, fp8):
     """Kernels of one mla_decode_layers step: the plan, each layer's decode and
     combine, and for E4M3 pages the query quantiser of every layer after the
     first (the plan grid quantises the first)."""
-    return 1 + 2 * layers + (layers - 1 if fp8 else 0)
+    return 1 + 2 * layers + (layers - 1 if fp8 else 0) if layers > 1 else 3
 
 
 def layers_decoder(plmla, fp8):
@@ -537,7 +543,7 @@ def decoder(plmla, fp8):
     return decode_fp8
 
 
-def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode_layers, kv_bytes_layer):
+def run_e2e(args, w, qs, table, lens, device, dist, call_step, kv_bytes_layer):
     """Same metric through the public call with pinned host buffers: each step
     copies its inputs host->device, decodes, and reads the result back.  As a
     serving loop would, the copies run on their own streams with two buffer
@@ -589,9 +595,7 @@ def run_e2e(args, w, qs, slabs, table, lens, ws, device, dist, decode_layers, kv
             in_ready[b].record(s_in)
         stream.wait_event(in_ready[b])
         stream.wait_event(out_free[b])
-        decode_layers([q[0] for q in dev_q[b]], [q[1] for q in dev_q[b]],
-                      [q[2] for q in dev_q[b]], slabs, dev_table[b], dev_lens[b], n_q=w.n_q,
-                      out=dev_out[b], lse=dev_lse[b], workspace=ws, min_splits=w.min_splits)
+        call_step(dev_q[b], dev_table[b], dev_lens[b], dev_out[b], dev_lse[b])
         in_free[b].record(stream)
         out_ready[b].record(stream)
         with torch.cuda.stream(s_out):

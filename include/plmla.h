@@ -129,7 +129,7 @@ int32_t mla_get_split_mode(void);
 
 /*
  * mla_set_team_clusters -- process-wide widest thread-block cluster of query-row
- * teams (1, 2 or 4; default 4) for the bf16 decode.  When a step has two or more
+ * teams (1, 2 or 4; default 2) for the bf16 decode.  When a step has two or more
  * teams of 64 rows (n_q * num_heads a multiple of 128), the CTAs that hold the
  * same member's work for 2 or 4 teams run as one cluster and every KV tile is
  * read from memory once and multicast by TMA into all of them, instead of once

@@ -305,9 +305,9 @@ def get_split_mode() -> str:
 
 
 def set_team_clusters(max_teams: int) -> None:
-    """Process-wide widest cluster (1, 2 or 4) of 64-row query teams that share
-    each KV tile's load (TMA multicast) in the bf16 decode; the outputs do not
-    depend on it."""
+    """Process-wide widest cluster (1, 2 or 4; default 2) of 64-row query teams
+    that share each KV tile's load (TMA multicast) in the bf16 decode; the
+    outputs do not depend on it."""
     _require(max_teams in (1, 2, 4), "max_teams must be 1, 2 or 4")
     _native.check(_native.lib().mla_set_team_clusters(int(max_teams)), "mla_set_team_clusters")
 

@@ -188,18 +188,18 @@ def test_split_mode_switch(lib, env, expect):
 
 
 def test_team_cluster_switch(lib):
-    """Host logic only: the widest cluster of query-row teams defaults to 4, the
+    """Host logic only: the widest cluster of query-row teams defaults to 2, the
     setter takes 1, 2 and 4 and rejects anything else."""
-    assert lib.mla_get_team_clusters() == 4
+    assert lib.mla_get_team_clusters() == 2
     try:
-        for v in (1, 2, 4):
+        for v in (1, 4, 2):
             assert lib.mla_set_team_clusters(v) == 0
             assert lib.mla_get_team_clusters() == v
         for bad in (0, 3, 8, -1):
             assert lib.mla_set_team_clusters(bad) == 1
-            assert lib.mla_get_team_clusters() == 4
+            assert lib.mla_get_team_clusters() == 2
     finally:
-        lib.mla_set_team_clusters(4)
+        lib.mla_set_team_clusters(2)
 
 
 def test_layered_decode_arguments_are_checked_on_the_host(lib):
