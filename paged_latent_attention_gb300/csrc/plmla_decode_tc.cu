@@ -55,6 +55,16 @@
 // before, zeros written at kernel start or earlier history rows, finite either
 // way, so stale or NaN page contents never reach the output (0 * NaN would).
 //
+// Teams in clusters (CL = 2 or 4, bf16 pages): the CTAs of CL teams of one
+// member, which stream the same KV items, run as one thread-block cluster.  Item
+// n of each ring is loaded by the CTA of rank n % CL with a TMA multicast into
+// the same slot of every CTA (each CTA's own producer posts the expected bytes
+// on its own full barrier), and every MMA thread releases a slot with a
+// multicast commit to the empty barrier of every CTA, which thus counts CL
+// releases.  Cluster barriers after initialisation and before exit keep every
+// remote write inside the lifetime of its target.  Only the loads change, never
+// the arithmetic.
+//
 // Every mbarrier wait is bounded: after kWaitLimitNs the waiting thread sets
 // the workspace status word and a CTA-wide abort flag, the producer waits (with
 // its own bound) for the copies it issued, each MMA thread waits for its MMAs,
