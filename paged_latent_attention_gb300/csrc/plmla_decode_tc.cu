@@ -260,17 +260,8 @@ __device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity)
     }
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
-                                            int c2, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
-        "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-
-// The same load with an L2 eviction-priority policy (from createpolicy).
+// A 3-D tiled TMA load into shared memory, completing on an mbarrier, with an
+// L2 eviction-priority policy (from createpolicy).
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                                  int c2, uint32_t bar, uint64_t policy)
 {
@@ -1218,7 +1209,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                     }
                     tc_fence_after();
                     const uint32_t d_s = tmem + kTmemS + F::s_stride * b;
-#pragma unroll
+                    // not unrolled: the issuers' code competes with the softmax warps'
+                    // for the instruction cache (measured: steady decode -4%, E4M3 -11%)
+#pragma unroll 1
                     for (int k = 0; k < F::sub; ++k) {
                         if (!wait_bounded(bar_full_k + 8 * slot, phase, abort_flag, a.status, 4)) {
                             ok = false;
@@ -1285,7 +1278,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                         break;
                     }
                     tc_fence_after();
-#pragma unroll
+                    // not unrolled either, except in the clustered variant, whose extend
+                    // workload lost 3% to it (the single-team and E4M3 variants gained a
+                    // further 0-6%)
+#pragma unroll(CL == 1 ? 1 : F::v_items)
                     for (int v = 0; v < F::v_items; ++v) {
                         if (!wait_bounded(bar_full_v + 8 * slot, phase, abort_flag, a.status, 14)) {
                             ok = false;
