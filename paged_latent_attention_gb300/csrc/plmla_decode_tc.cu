@@ -968,6 +968,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                         const int t = seg.y + i * kTile;
                         const int page = trow[t / kPageTokens];
                         const int tok = t % kPageTokens;
+                        // the producers' and issuers' item loops stay rolled: the kernel is
+                        // bound by instruction fetch as much as by its streams
+#pragma unroll 1
                         for (int k = 0; k < F::sub; ++k) {
                             if (!wait_bounded(bar_empty_k + 8 * slot, phase ^ 1, abort_flag,
                                               a.status, 2)) {
@@ -1045,6 +1048,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                                     tma_prefetch_3d(&tail.m[0], 0, tb, np);
                             }
                         }
+#pragma unroll 1
                         for (int k = 0; k < F::sub; ++k) {
                             if (pending >= 0 && issued >= q_deadline) {
                                 if (!load_q(pending)) {
@@ -1107,6 +1111,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                 const int t = seg.y + i * kTile;
                 const int page = trow[t / kPageTokens];
                 const int tok = t % kPageTokens;
+#pragma unroll 1
                 for (int v = 0; v < F::v_items; ++v) {
                     // first token of the item within the tile
                     const int toff = (v % F::v_per_block) * F::v_tokens;
@@ -1137,7 +1142,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constan
                             constexpr int halves = F8 ? 1 : 2;
                             mbar_arrive_expect_tx(fb, (uint32_t)(live * 128 * halves));
                             int r0 = 0;
-#pragma unroll
+#pragma unroll 1
                             for (int b = kTailMaps - 1; b >= 0 && mine; --b) {
                                 if ((live >> b) & 1) {
                                     kv_load<CL>(dst + r0 * 128, &tail.m[b], col, tk + r0, page, fb,
