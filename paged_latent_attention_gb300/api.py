@@ -255,7 +255,7 @@ def mla_decode_layers(q_nope_absorbed, q_rope, gate, slabs, page_table, seq_lens
     else:
         status = lib.mla_decode_layers(*head, *tail)
     _native.check(status, "mla_decode_layers_fp8" if fp8 else "mla_decode_layers")
-    return out, lse if lse is not None else [None] * L
+    return out, (lse if lse is not None else [None] * L)
 
 
 def mla_quantize_queries_fp8(q_nope_absorbed, q_rope, stream=None):
