@@ -207,7 +207,9 @@ plmla_status mla_plan_splits(const int32_t *seq_lens, int32_t num_reqs, int32_t 
  * stream           cudaStream_t
  *
  * Enqueues: plan kernel (split plan + persistent schedule) -> split-decode
- * kernel (one persistent CTA per SM and row group) -> combine/gate kernel.
+ * kernel (one persistent CTA per SM and row group; with two or more 64-row
+ * groups, in 2-CTA clusters that share each KV tile's load, see
+ * mla_set_team_clusters) -> combine/gate kernel.
  * Page IDs are not checked on the hot path: an ID outside [0, num_pages) is a
  * tensor-map coordinate out of range, which the TMA unit reads as zeros (no
  * fault), so the affected rows come out wrong.  With page checks on (see
