@@ -130,12 +130,13 @@ int32_t mla_get_split_mode(void);
 /*
  * mla_set_team_clusters -- process-wide widest thread-block cluster of query-row
  * teams (1, 2 or 4; default 2) for the bf16 decode.  When a step has two or more
- * teams of 64 rows (n_q * num_heads a multiple of 128), the CTAs that hold the
- * same member's work for 2 or 4 teams run as one cluster and every KV tile is
- * read from memory once and multicast by TMA into all of them, instead of once
- * per team.  The width used is the largest of 4, 2 within max_teams that divides
- * the team count and whose clusters the device holds at once (all of the grid's
- * CTAs must be resident together), else 1.  Only the loads change: the outputs
+ * teams of 64 rows (n_q * num_heads a multiple of 128) and each team has at most
+ * 8 persistent CTAs (members; e.g. a chunked extend of 128 tokens at 64 heads),
+ * the CTAs that hold the same member's work for 2 or 4 teams run as one cluster
+ * and every KV tile is read from memory once and multicast by TMA into all of
+ * them, instead of once per team.  The width used is the largest of 4, 2 within
+ * max_teams that divides the team count and whose clusters the device holds at
+ * once (all of the grid's CTAs must be resident together), else 1.  Only the loads change: the outputs
  * are bit-identical for every setting.  PLMLA_INVALID_ARGUMENT for another value.
  * mla_get_team_clusters returns the setting.
  */

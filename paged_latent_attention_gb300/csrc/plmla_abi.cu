@@ -56,6 +56,12 @@ std::atomic<int> g_split_mode{initial_split_mode()};
 // Widest cluster of 64-row teams that share KV loads (1 = none, 2 or 4).
 std::atomic<int> g_team_clusters{kClusterTeams};
 
+// Teams share loads in clusters only when each has at most this many members:
+// then every CTA streams long stretches of history alone (measured: the
+// 128-team extend, one member per team, 2.6% faster in pairs; the 4-draft
+// decode, 38 members per team, 1.6% slower).
+constexpr int32_t kClusterMaxMembers = 8;
+
 size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -434,8 +440,10 @@ plmla_status decode_layers_impl(int32_t layers, const void *const *q_nope_absorb
     // teams of a member in one cluster share its KV items (multicast), when the
     // device holds every cluster of the grid at once; the arithmetic, and so
     // every output bit, is the same either way
-    a.cluster = decode_cluster_teams(sh.group_rows, sh.groups, fp8,
-                                     g_team_clusters.load(std::memory_order_relaxed));
+    a.cluster = sh.members <= kClusterMaxMembers
+                    ? decode_cluster_teams(sh.group_rows, sh.groups, fp8,
+                                           g_team_clusters.load(std::memory_order_relaxed))
+                    : 1;
     while (a.cluster > 1 &&
            (int64_t)sh.members * (sh.groups / a.cluster) > decode_max_clusters(a.cluster))
         a.cluster /= 2;

@@ -99,9 +99,9 @@ cudaError_t launch_decode_tc(const DecodeArgs &args, cudaStream_t stream);
 // Teams of 64 query rows that share each KV item through a thread-block
 // cluster (the KV tiles multicast by TMA): 4 or 2 (at most max_teams, and a
 // divisor of the team count), or 1 for the E4M3 decode and narrower teams.
-// kClusterTeams is the default of max_teams: pairs (measured: the 4-draft
-// decode 1% faster with half its DRAM reads, the 128-team extend step 6%
-// faster; clusters of 4 made the extend step 12% slower).
+// kClusterTeams is the default of max_teams: pairs (measured on the 128-team
+// extend, where clusters of 4 were slower than pairs).  The library uses
+// clusters only for teams of few members (plmla_abi.cu).
 constexpr int kClusterTeams = 2;
 int decode_cluster_teams(int group_rows, int groups, bool fp8, int max_teams);
 // Clusters of `cluster` (2 or 4) decode CTAs the current device holds at once

@@ -2,12 +2,13 @@
 multicast; include/plmla.h, mla_set_team_clusters).
 
 When a step's query rows form two or more teams of 64 (several draft tokens, or
-128 heads), the CTAs holding the same member's work for 2 or 4 teams run as one
-cluster and each KV tile is loaded once for all of them.  Only the loads change,
-so every cluster width must give the same bits, and match the oracle -- on
-ragged histories whose pages past each history hold NaN, with both the default
-grid (clusters of at most 2 on a 152-SM GB300, where 38 clusters of 4 do not fit
-at once) and a small one (clusters of 4 when the width allows it).
+128 heads) of at most 8 members each, the CTAs holding the same member's work
+for 2 or 4 teams run as one cluster and each KV tile is loaded once for all of
+them.  Only the loads change, so every cluster width must give the same bits,
+and match the oracle -- on ragged histories whose pages past each history hold
+NaN, with the default grid (many members per team: no clusters) and a small one
+of 16 CTAs (2 to 8 members per team: clusters of 2, or 4 when the width allows
+it and the team count divides).
 """
 import pytest
 import torch
