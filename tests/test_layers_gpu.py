@@ -141,3 +141,70 @@ def test_captured_layered_step_follows_new_lengths():
             ref_out, ref_lse = oracle_decode(w2, *host[l], rows=rows)
             assert_parity(outs[l], lses[l], ref_out, ref_lse, rows=rows,
                           what=f"replay {trial} layer {l}")
+
+
+def test_one_layer_equals_mla_decode():
+    w = inputs.custom_workload([3000, 17, 9000], 2, 64, seed=640, spare_pages=1)
+    host, dev = _layers(w, 1)
+    table = torch.as_tensor(w.page_table, device="cuda")
+    lens = torch.as_tensor(w.seq_lens, device="cuda")
+    outs, lses = api.mla_decode_layers([dev[0][0]], [dev[0][1]], [dev[0][2]], [dev[0][3]], table,
+                                       lens, n_q=2, scale=SCALE)
+    one_out, one_lse = api.mla_decode(*dev[0][:3], dev[0][3], table, lens, n_q=2, scale=SCALE)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0].view(torch.int16), one_out.view(torch.int16))
+    assert torch.equal(lses[0], one_lse)
+
+
+def test_layers_under_the_uniform_split_rule():
+    """The uniform baseline of the pages' Figure 5 plans the step once for every
+    layer too: each layer equals its single-layer call under the same rule."""
+    L = 2
+    w = inputs.custom_workload([20_000, 300, 7000, 1537], 1, 64, seed=650, spare_pages=2)
+    host, dev = _layers(w, L)
+    table = torch.as_tensor(w.page_table, device="cuda")
+    lens = torch.as_tensor(w.seq_lens, device="cuda")
+    api.set_split_mode("uniform")
+    try:
+        outs, lses = api.mla_decode_layers([d[0] for d in dev], [d[1] for d in dev],
+                                           [d[2] for d in dev], [d[3] for d in dev], table, lens,
+                                           n_q=1, scale=SCALE)
+        singles = [api.mla_decode(*d[:3], d[3], table, lens, n_q=1, scale=SCALE) for d in dev]
+        torch.cuda.synchronize()
+    finally:
+        api.set_split_mode("per-request")
+    rows = sample_rows(w, heads_per_token=4, seed=11)
+    for l in range(L):
+        assert torch.equal(outs[l].view(torch.int16), singles[l][0].view(torch.int16)), l
+        assert torch.equal(lses[l], singles[l][1]), l
+        ref_out, ref_lse = oracle_decode(w, *host[l], rows=rows)
+        assert_parity(outs[l], lses[l], ref_out, ref_lse, rows=rows, what=f"uniform layer {l}")
+
+
+def test_page_check_covers_the_layered_step():
+    """With page checks on, one check after the layered step reports a table
+    entry outside the pool (status 40); requests that do not use it keep their
+    results in every layer."""
+    L = 2
+    lengths = [4000, 9000, 3000]
+    w = inputs.custom_workload(lengths, 1, 64, seed=660, spare_pages=2)
+    host, dev = _layers(w, L, poison=False)
+    table_np = w.page_table.copy()
+    table_np[1, (lengths[1] - 1) // inputs.PAGE_TOKENS] = w.num_pages + 5
+    table = torch.as_tensor(table_np, device="cuda")
+    lens = torch.as_tensor(w.seq_lens, device="cuda")
+    ws = api.allocate_workspace(w.num_reqs, 1, 64, 0, 1, "cuda")
+    api.set_page_checks(True)
+    try:
+        outs, lses = api.mla_decode_layers([d[0] for d in dev], [d[1] for d in dev],
+                                           [d[2] for d in dev], [d[3] for d in dev], table, lens,
+                                           n_q=1, scale=SCALE, workspace=ws)
+        torch.cuda.synchronize()
+    finally:
+        api.set_page_checks(False)
+    assert api.device_status(ws) == 40
+    rows = sample_rows(w, heads_per_token=4, seed=12)
+    good = rows[rows // w.num_heads != 1]
+    for l in range(L):
+        ref_out, ref_lse = oracle_decode(w, *host[l], rows=good)
+        assert_parity(outs[l], lses[l], ref_out, ref_lse, rows=good, what=f"good requests, layer {l}")
