@@ -427,7 +427,8 @@ def run_gpu(args):
         # previous step's combine (programmatic edges inside the graph); captured
         # and replayed once before the timed region
         graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
+        # thread-local capture: other threads (a process group's) may use CUDA meanwhile
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
             run_steps()
         graph.replay()
         torch.cuda.synchronize(device)
