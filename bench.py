@@ -49,9 +49,13 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["plmla", "reference"], default="plmla")
-    ap.add_argument("--op", choices=["decode", "append"], default="decode",
+    ap.add_argument("--op", choices=["decode", "append", "dcp"], default="decode",
                     help="decode: the hot path (default); append: the KV append kernel "
-                         "writing a block of new rows per request into the same pool")
+                         "writing a block of new rows per request into the same pool; dcp: "
+                         "decode context parallelism's device work (shard, each rank's "
+                         "decode, merge) for one layer, the ranks run one after another")
+    ap.add_argument("--dcp-world", type=int, default=4,
+                    help="ranks of the decode context parallelism group for --op dcp")
     ap.add_argument("--append-tokens", type=int, default=4096,
                     help="new tokens per request for --op append")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
@@ -714,6 +718,94 @@ def time_append_graph(plmla, lat, rope, slab, table, lens, n_new, stream, per_gr
     return start.elapsed_time(end) / (replays * per_graph)
 
 
+DCP_METRIC = ("decode context parallelism, ranks serialised on one GPU: projected step time "
+              "(slowest rank's shard + decode, plus the merge), KV GB/s")
+
+
+def run_dcp(args):
+    """Decode context parallelism's device work for one layer of the workload:
+    every rank's page shard (mla_dcp_shard) and decode on its pages, then the
+    merge of the ranks' gated outputs (mla_merge_partials).  The ranks run one
+    after another on this GPU, each timed alone; the projected step of a group
+    of GPUs is the slowest rank plus the merge.  The all-gather between them is
+    not measured (one GPU), and no rank waits on another."""
+    import torch
+    import paged_latent_attention_gb300 as plmla
+    from paged_latent_attention_gb300 import inputs
+
+    world_procs, rank_proc, local = dist_env()
+    if world_procs > 1:
+        raise SystemExit("--op dcp runs in one process (the ranks are serialised)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    G = args.dcp_world
+    if not 1 <= G <= 64:
+        raise SystemExit("--dcp-world must lie in [1, 64]")
+    w = inputs.make_workload(args.workload)
+    qn, qr, gate = inputs.make_queries(w, device)
+    slab = inputs.make_slab(w, device)
+    table = torch.as_tensor(w.page_table, device=device)
+    lens = torch.as_tensor(w.seq_lens, device=device)
+    T, H = w.num_tokens, w.num_heads
+    ws = plmla.allocate_workspace(w.num_reqs, w.n_q, H, 0, 1, device)
+    out_parts = torch.empty(G, T, H, 512, dtype=torch.bfloat16, device=device)
+    lse_parts = torch.empty(G, T, H, dtype=torch.float32, device=device)
+    shards = [plmla.mla_dcp_shard(table, lens, G, k) for k in range(G)]
+    stream = torch.cuda.current_stream(device)
+    K, W = args.steps, max(3, args.warmup)
+
+    def timed(fn):
+        for _ in range(W):
+            fn()
+        torch.cuda.synchronize(device)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for _ in range(K):
+            fn()
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        return start.elapsed_time(end) / K
+
+    def rank_step(k):
+        def fn():
+            t_k, l_k = plmla.mla_dcp_shard(table, lens, G, k)
+            plmla.mla_decode(qn, qr, gate, slab, t_k, l_k, n_q=w.n_q, out=out_parts[k],
+                             lse=lse_parts[k], workspace=ws)
+        return fn
+
+    rank_ms = [timed(rank_step(k)) for k in range(G)]
+    merge_ms = timed(lambda: plmla.mla_merge_partials(out_parts, lse_parts))
+    whole_out = torch.empty_like(qn)
+    whole_lse = torch.empty(T, H, dtype=torch.float32, device=device)
+    whole_ms = timed(lambda: plmla.mla_decode(qn, qr, gate, slab, table, lens, n_q=w.n_q,
+                                              out=whole_out, lse=whole_lse, workspace=ws))
+    merged_out, merged_lse = plmla.mla_merge_partials(out_parts, lse_parts)
+    torch.cuda.synchronize(device)
+    lse_err = float((merged_lse - whole_lse).abs().max())
+    rank_tokens = [int(l_k.sum()) for _, l_k in shards]
+    kv_bytes = w.kv_tokens * kv_row_bytes(w, False)
+    step_ms = max(rank_ms) + merge_ms
+    parts_bytes = G * T * H * (512 * 2 + 4) + T * H * (512 * 2 + 4)
+    return {
+        "metric": DCP_METRIC, "value": kv_bytes / (step_ms / 1e3) / 1e9, "unit": UNIT,
+        "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": workload_description(w) + " (layer 0)", "dcp_world": G,
+                   "parallelism": f"dcp{G}, ranks serialised on one GPU"},
+        "rank_ms": rank_ms, "rank_kv_tokens": rank_tokens,
+        "rank_balance": max(rank_ms) / (sum(rank_ms) / G),
+        "merge_ms": merge_ms, "merge_gbs": parts_bytes / (merge_ms / 1e3) / 1e9,
+        "unsharded_decode_ms": whole_ms,
+        "projected_speedup_vs_one_gpu": whole_ms / step_ms,
+        "merged_vs_unsharded_max_lse_diff": lse_err,
+        "note": "each rank's shard and decode timed alone on one GPU; the projected step is the "
+                "slowest rank plus the merge, without the all-gather of T x H x 1,028 bytes per "
+                "rank (not measurable on one GPU)",
+        "gpu_launches": K * (G * 4 + 1),
+    }
+
+
 def run_append(args):
     import torch
     import paged_latent_attention_gb300 as plmla
@@ -930,6 +1022,8 @@ def main(argv=None):
         line = run_reference(args)
     elif args.op == "append":
         line = run_append(args)
+    elif args.op == "dcp":
+        line = run_dcp(args)
     else:
         line = run_gpu(args)
     if line is not None:
